@@ -1,0 +1,107 @@
+// Internal launcher interface between the C ABI (msa_api.cu) and the kernel translation
+// units. Every launcher only queues work on `stream` and returns the launch status.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+// ------------------------------------------------------------------ stage 1
+struct ScoreArgs {
+  const uint16_t* q_idx;       // [B*N, Hkv, Di]
+  const uint16_t* k_idx;       // [num_pages, 128, Hkv, Di]
+  const int32_t* page_table;   // [B, max_blocks]
+  const int32_t* seq_lens;     // [B]
+  int32_t B, N, Hkv, Di, max_blocks, topk;
+  int64_t num_pages;
+  int32_t* block_ids;          // [B*N, Hkv, topk]
+  float* sel_scores;           // [B*N, Hkv, topk] or null
+  float* scores;               // workspace [B*N, Hkv, max_blocks]
+  int32_t* tickets;            // workspace [B], cleared by the launcher before each call
+};
+// Streaming scorer for N <= kDecodeMaxN with the top-k fused into the last CTA per request.
+constexpr int kDecodeMaxN = 8;
+cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream);
+// Generic scorer (any N) writing every block score, followed by the top-k kernel.
+cudaError_t launch_score_rows(const ScoreArgs& a, cudaStream_t stream);
+cudaError_t launch_topk_rows(const ScoreArgs& a, cudaStream_t stream);
+size_t score_decode_smem_bytes(int N, int Hkv, int Di, int* nstage);
+
+// ------------------------------------------------------------------ page table
+cudaError_t launch_build_page_table(const int32_t* block_ids, const int32_t* page_table,
+                                   const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,
+                                   int32_t topk, int32_t max_blocks, int64_t num_pages,
+                                   int32_t* fpt, int32_t* lens, cudaStream_t stream);
+
+// ------------------------------------------------------------------ paged decode
+struct DecodeArgs {
+  const uint16_t* q;           // [R, Hq, D]
+  const uint16_t* k_cache;     // [num_pages, 128, Hkv, D]
+  const uint16_t* v_cache;
+  const int32_t* fpt;          // [R*Hkv, topk]
+  const int32_t* lens;         // [R*Hkv]
+  int32_t R, Hq, Hkv, D, topk;
+  int64_t num_pages;
+  uint16_t* o;                 // [R, Hq, D]
+  float* lse;                  // [R, Hq] or null
+  float* part_o;               // workspace [R*Hkv, nsplit, G, D]
+  float* part_lse;             // workspace [R*Hkv, nsplit, G]
+  int32_t nsplit, pages_per_split;
+};
+void decode_split(int32_t topk, int32_t* nsplit, int32_t* pages_per_split);
+cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------ LSE merge
+// skip_ids: optional [U, S]; partial s of unit u is ignored when skip_ids[u*S+s] < 0.
+cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* lse_parts,
+                             const int32_t* skip_ids, int64_t U, int32_t S, int32_t G, int32_t D,
+                             uint16_t* o, float* lse, cudaStream_t stream);
+
+// ------------------------------------------------------------------ prefill
+// Workspace carve-up shared by the C ABI (size query) and the launcher. Offsets in bytes,
+// each 256-byte aligned.
+struct PrefillWorkspace {
+  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, total;
+};
+inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, int32_t nblk,
+                                          int32_t G, bool attention) {
+  PrefillWorkspace w{};
+  size_t off = 0;
+  w.counts = off;       off = ws_align(off + 4 * (size_t)Hkv * nblk);
+  w.group_base = off;   off = ws_align(off + 4 * (size_t)(Hkv + 1));
+  w.tile_offsets = off; off = ws_align(off + 4 * ((size_t)Hkv * nblk + 1));
+  if (attention) {
+    const size_t sel = (size_t)T * Hkv * topk;
+    w.offsets = off;    off = ws_align(off + 4 * (size_t)Hkv * (nblk + 1));
+    w.entries = off;    off = ws_align(off + 4 * sel);
+    w.part_o = off;     off = ws_align(off + 2 * sel * G * 128);
+    w.part_lse = off;   off = ws_align(off + 4 * sel * G);
+  }
+  w.total = off;
+  return w;
+}
+// (a) bucketing; tiles of `qpt` queries are laid out for the attention kernel.
+cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
+                          int32_t nblk, int32_t qpt, int32_t* offsets, int32_t* entries,
+                          int32_t* counts, int32_t* group_base, int32_t* tile_offsets,
+                          cudaStream_t stream);
+struct PrefillArgs {
+  const uint16_t* q;           // [T, Hq, D]
+  const uint16_t* k;           // [S_kv, Hkv, D]
+  const uint16_t* v;
+  const int32_t* block_ids;    // [T, Hkv, topk]
+  int32_t T, Hq, Hkv, D, topk, nblk;
+  int64_t S_kv;
+  uint16_t* o;                 // [T, Hq, D]
+  float* lse;                  // [T, Hq] or null
+  uint8_t* workspace;          // carved by prefill_ws_layout(..., attention = true)
+};
+cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------ device errors
+cudaError_t read_device_errors(uint32_t* word);
+
+}  // namespace msa

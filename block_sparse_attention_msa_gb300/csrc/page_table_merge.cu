@@ -1,0 +1,145 @@
+// Sparse page table (decode) and the Log-Sum-Exp merge of partial attention outputs.
+//
+// Page table -- Together AI MiniMax-M3 serving article, section "MSA needs a new
+// paged-attention integration": at decode a page table is built from the selected blocks,
+// the KV-group dimension is flattened into the batch, and a strided view of the KV cache
+// gives each flattened row its own pages (page address steps by D to select the virtual
+// page start, tokens step by Hkv*D). Because the number of selected blocks is bounded the
+// mapping kernel is tiny: one warp per flattened row, one lane per slot.
+//
+// LSE merge -- same article, section "KV-block-major sparse attention reduces redundant KV
+// movement": every KV block yields a partial O, and a Log-Sum-Exp reduction rescales and
+// sums the partials. The same merge finishes the split-K decode. One warp per (unit, head):
+// lanes own 4 consecutive channels, partials are read once, coalesced, and the result is
+// written as bf16 with its fp32 LSE.
+#include "common.cuh"
+#include "kernels.h"
+
+MSA_DEFINE_ERROR_WORD(ptm)
+
+namespace msa {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+    page_table_kernel(const int32_t* __restrict__ block_ids, const int32_t* __restrict__ page_table,
+                      const int32_t* __restrict__ seq_lens, int32_t B, int32_t N, int32_t Hkv,
+                      int32_t topk, int32_t max_blocks, int64_t num_pages,
+                      int32_t* __restrict__ fpt, int32_t* __restrict__ lens) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t f = (int64_t)blockIdx.x * 8 + warp;
+  if (f >= (int64_t)B * N * Hkv) return;
+  const int64_t r = f / Hkv;
+  const int g = (int)(f % Hkv);
+  const int64_t b = r / N;
+  bool bad = false;
+  const int q_pos = clamp_seq(seq_lens, (int)b, N, max_blocks, bad) - N + (int)(r % N);
+  if (bad && lane == 0 && g == 0) msa_record_error(kErrBadBlock);
+  const int local = q_pos / MSA_BLOCK_TOKENS;
+  int len = 0;
+  for (int i = lane; i < topk; i += 32) {
+    const int32_t j = block_ids[f * topk + i];
+    int32_t v = -1;
+    if (j >= 0) {
+      if (j > local || j >= max_blocks) {
+        msa_record_error(kErrBadBlock);
+      } else {
+        const int32_t p = page_table[b * max_blocks + j];
+        if (p < 0 || p >= num_pages) {
+          msa_record_error(kErrBadPage);
+        } else {
+          v = (int32_t)((int64_t)p * MSA_BLOCK_TOKENS * Hkv + g);
+          len += (j == local) ? (q_pos % MSA_BLOCK_TOKENS) + 1 : MSA_BLOCK_TOKENS;
+        }
+      }
+    }
+    fpt[f * topk + i] = v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) len += __shfl_xor_sync(0xffffffffu, len, o);
+  if (lane == 0) lens[f] = len;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+    lse_merge_kernel(const void* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                     const int32_t* __restrict__ skip_ids, int64_t U, int32_t S, int32_t G,
+                     int32_t D, uint16_t* __restrict__ o, float* __restrict__ lse) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * 8 + warp;  // = u*G + e
+  if (item >= U * G) return;
+  const int64_t u = item / G;
+  const int e = (int)(item % G);
+  // pass 1: max of the partial LSEs (lanes stride over the S partials)
+  float m = -INFINITY;
+  // skip_ids (optional, [U, S]): a partial whose id is negative was never written
+  for (int s = lane; s < S; s += 32)
+    if (!skip_ids || skip_ids[u * S + s] >= 0) m = fmaxf(m, lse_parts[(u * S + s) * G + e]);
+  m = warp_max(m);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float total = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      if (skip_ids && skip_ids[u * S + s] < 0) continue;
+      const float ls = lse_parts[(u * S + s) * G + e];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - m);
+      total += w;
+      const int64_t row = ((u * S + s) * G + e) * (int64_t)D;
+      for (int d = lane * 4; d < D; d += 128) {
+        if (BF16) {
+          const uint2 v = *reinterpret_cast<const uint2*>(
+              reinterpret_cast<const uint16_t*>(o_parts) + row + d);
+          acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+          acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+          acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+          acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+        } else {
+          const float4 v =
+              *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o_parts) + row + d);
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]);
+          acc[3] = fmaf(w, v.w, acc[3]);
+        }
+      }
+    }
+  }
+  const float inv = total > 0.f ? 1.0f / total : 0.f;
+  const int64_t orow = (u * G + e) * (int64_t)D;
+  for (int d = lane * 4; d < D; d += 128) {
+    uint2 out;
+    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(o + orow + d) = out;
+  }
+  if (lse && lane == 0) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_build_page_table(const int32_t* block_ids, const int32_t* page_table,
+                                   const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,
+                                   int32_t topk, int32_t max_blocks, int64_t num_pages,
+                                   int32_t* fpt, int32_t* lens, cudaStream_t stream) {
+  const int64_t rows = (int64_t)B * N * Hkv;
+  page_table_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      block_ids, page_table, seq_lens, B, N, Hkv, topk, max_blocks, num_pages, fpt, lens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* lse_parts,
+                             const int32_t* skip_ids, int64_t U, int32_t S, int32_t G, int32_t D,
+                             uint16_t* o, float* lse, cudaStream_t stream) {
+  const int64_t items = U * G;
+  const unsigned grid = (unsigned)((items + 7) / 8);
+  if (parts_bf16)
+    lse_merge_kernel<true>
+        <<<grid, 256, 0, stream>>>(o_parts, lse_parts, skip_ids, U, S, G, D, o, lse);
+  else
+    lse_merge_kernel<false>
+        <<<grid, 256, 0, stream>>>(o_parts, lse_parts, skip_ids, U, S, G, D, o, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,614 @@
+// Stage 1 of MSA: index scoring with a fused per-block max, and top-k block selection.
+//
+// Together AI MiniMax-M3 serving article, section "The index scorer becomes the decode
+// critical path": every decode query compares its query-side index vector with the
+// key-side index vectors of all candidate 128-token blocks, each block is reduced to one
+// score and only the top blocks are kept. The shape is a small query index against a long
+// key index; the pages stage each 128-token K-index page with asynchronous copies, prefetch
+// the next page, take bf16 dot products and reduce each page to one block score.
+//
+// GB300 design. At decode the scorer is a streaming read of the whole paged K-index (one
+// byte read per flop), so it is written for HBM bandwidth, not for tensor cores:
+//  * one persistent CTA per SM walks a contiguous range of the batch's (request, page)
+//    list; a producer warp streams each page through a ring of TMA stages (256 index rows
+//    of all KV groups per stage, 128-byte swizzle so that 32 lanes reading 32 different
+//    rows hit 32 different bank groups);
+//  * each consumer thread owns one (token, group) row per stage and takes its full dot
+//    product with every query row of the request in fp32 (exact bf16 products), keeping a
+//    running max per query row; a shuffle + shared-memory reduction turns the page into
+//    one score per (query row, group);
+//  * the top-k is fused: the CTA that completes a request's last page (an atomic ticket
+//    per request, no spinning) selects the blocks of every (query row, group) of that
+//    request with a warp-level radix select.
+// Long query chunks (prefill, N > 8) use a tiled CUDA-core scorer writing every block
+// score, then the same warp top-k in a separate launch.
+#include "common.cuh"
+#include "host_util.h"
+#include "kernels.h"
+
+MSA_DEFINE_ERROR_WORD(score)
+
+namespace msa {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStageRows = 256;
+constexpr int kTopkMax = 64;
+
+struct TopkScratch {
+  uint32_t hist[256];
+  int32_t sel[kTopkMax];
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Top-k of one (query row, group), executed by one full warp.
+// s: the row's block scores (global, written by other CTAs: read with ld.global.cg).
+// Blocks 0 and `local` are forced; the remaining slots take blocks 1..local-1 by score
+// descending with ties to the lower id (radix select on order-preserving keys, then the
+// lowest ids among the keys equal to the threshold). Writes ids ascending, -1 padding.
+__device__ void warp_topk(const float* __restrict__ s, int local, int topk, int32_t* ids_out,
+                          float* sc_out, TopkScratch& ws) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t full = 0xffffffffu;
+  const int nforced = local > 0 ? 2 : 1;
+  const int ncand = local > 1 ? local - 1 : 0;
+  int m = topk - nforced;
+  if (m > ncand) m = ncand;
+  if (m < 0) m = 0;
+  if (lane == 0) {
+    ws.sel[0] = 0;
+    if (local > 0) ws.sel[1] = local;
+  }
+  if (m == ncand) {
+    for (int j = 1 + lane; j < local; j += 32) ws.sel[nforced + j - 1] = j;
+  } else if (m > 0) {
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = m;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int b = lane; b < 256; b += 32) ws.hist[b] = 0;
+      __syncwarp();
+      for (int j = 1 + lane; j < local; j += 32) {
+        uint32_t key = float_key(__ldcg(s + j));
+        if ((key & pmask) == prefix) atomicAdd(&ws.hist[(key >> shift) & 255u], 1u);
+      }
+      __syncwarp();
+      // lane l owns digits 255-8l .. 248-8l (descending)
+      int c[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = (int)ws.hist[255 - (lane * 8 + q)];
+        sum += c[q];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(full, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - sum;
+      const uint32_t bal = __ballot_sync(full, excl < remaining && incl >= remaining);
+      const int src = __ffs(bal) - 1;
+      int digit = 0, above = 0;
+      if (lane == src) {
+        int acc = excl;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (acc + c[q] >= remaining) {
+            digit = 255 - (lane * 8 + q);
+            above = acc;
+            break;
+          }
+          acc += c[q];
+        }
+      }
+      digit = __shfl_sync(full, digit, src);
+      above = __shfl_sync(full, above, src);
+      remaining -= above;
+      prefix |= (uint32_t)digit << shift;
+      pmask |= 255u << shift;
+      __syncwarp();
+    }
+    // prefix is the threshold key; take every key above it and the `remaining` lowest
+    // ids among the keys equal to it.
+    int base = nforced, eq_seen = 0;
+    for (int j0 = 1; j0 < local; j0 += 32) {
+      const int j = j0 + lane;
+      const uint32_t key = j < local ? float_key(__ldcg(s + j)) : 0u;
+      const bool gt = j < local && key > prefix;
+      const bool eq = j < local && key == prefix;
+      const uint32_t eqm = __ballot_sync(full, eq);
+      const int eqrank = eq_seen + __popc(eqm & lanemask_lt());
+      const bool take = gt || (eq && eqrank < remaining);
+      const uint32_t tm = __ballot_sync(full, take);
+      const int dst = base + __popc(tm & lanemask_lt());
+      if (take && dst < kTopkMax) ws.sel[dst] = j;
+      base += __popc(tm);
+      eq_seen += __popc(eqm);
+    }
+  }
+  __syncwarp();
+  const int nsel = nforced + m;
+  // rank sort of the (distinct) kept ids, then write ids and their scores
+  for (int k = lane; k < topk; k += 32) {
+    if (k < nsel) {
+      const int e = ws.sel[k];
+      int rank = 0;
+      for (int q = 0; q < nsel; ++q) rank += ws.sel[q] < e;
+      ids_out[rank] = e;
+      if (sc_out) sc_out[rank] = __ldcg(s + e);
+    } else {
+      ids_out[k] = -1;
+      if (sc_out) sc_out[k] = -INFINITY;
+    }
+  }
+  __syncwarp();
+}
+
+struct DecodeSmemLayout {
+  uint32_t stage_bytes, q_off, red_off, topk_off, bar_off, misc_off, total;
+};
+
+__host__ __device__ inline DecodeSmemLayout decode_layout(int N, int Hkv, int Di, int nstage) {
+  DecodeSmemLayout L;
+  const int rows = kStageRows < 128 * Hkv ? kStageRows : 128 * Hkv;
+  L.stage_bytes = (uint32_t)(rows * Di * 2);
+  uint32_t off = L.stage_bytes * (uint32_t)nstage;           // stages at offset 0 (1024-aligned)
+  L.q_off = off;
+  off += (uint32_t)(N * Hkv * (Di + 4) * 4);
+  L.red_off = off;
+  off += (uint32_t)(kConsumerWarps * N * Hkv * 4);
+  off = (off + 15u) & ~15u;
+  L.topk_off = off;
+  off += (uint32_t)(kConsumerWarps * sizeof(TopkScratch));
+  off = (off + 7u) & ~7u;
+  L.bar_off = off;
+  off += (uint32_t)(2 * nstage * 8);
+  L.misc_off = off;
+  off += 64;
+  L.total = off + 1024;  // slack for aligning the base to 1024 bytes
+  return L;
+}
+
+struct DecodeKParams {
+  const uint16_t* q_idx;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t B, N, Hkv, max_blocks, topk, nstage;
+  int64_t num_pages;
+  int32_t* block_ids;
+  float* sel_scores;
+  float* scores;
+  int32_t* tickets;
+};
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_decode_kernel(const __grid_constant__ CUtensorMap kmap, const DecodeKParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int Hkv = p.Hkv, N = p.N, nstage = p.nstage;
+  const DecodeSmemLayout L = decode_layout(N, Hkv, DI, nstage);
+  float* sq = reinterpret_cast<float*>(smem + L.q_off);
+  float* sred = reinterpret_cast<float*>(smem + L.red_off);
+  TopkScratch* stopk = reinterpret_cast<TopkScratch*>(smem + L.topk_off);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty_bar = full_bar + nstage;
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.misc_off);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rows = kStageRows < 128 * Hkv ? kStageRows : 128 * Hkv;
+  const int stages_per_page = (128 * Hkv) / rows;
+  const int tok_per_stage = rows / Hkv;
+
+  // ---- range of (request, page) items of this CTA: warp 0 scans the request lengths
+  if (warp == 0) {
+    int total = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      bool bad = false;
+      const int nb = b < p.B ? (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128 : 0;
+      if (bad && blockIdx.x == 0) msa_record_error(kErrBadBlock);
+      total += __reduce_add_sync(0xffffffffu, nb);
+    }
+    const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int p0 = min(total, (int)blockIdx.x * per);
+    const int p1 = min(total, p0 + per);
+    // locate the request holding item p0
+    int run = 0, b_start = p.B, j_start = 0;
+    for (int b0 = 0; b0 < p.B && b_start == p.B; b0 += 32) {
+      const int b = b0 + lane;
+      bool bad = false;
+      const int nb = b < p.B ? (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128 : 0;
+      int incl = nb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - nb;
+      const uint32_t hit = __ballot_sync(0xffffffffu, b < p.B && run + excl <= p0 && p0 < run + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        b_start = b0 + src;
+        j_start = p0 - run - __shfl_sync(0xffffffffu, excl, src);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      misc[0] = p0;
+      misc[1] = p1;
+      misc[2] = b_start;
+      misc[3] = j_start;
+      misc[5] = 0;  // set to 1 by any consumer whose bounded wait gave up
+    }
+  }
+  if (tid == kConsumers) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int p0 = misc[0], p1 = misc[1];
+  if (p0 >= p1) return;
+
+  if (warp == kConsumerWarps) {
+    // ================================ producer warp
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      int b = misc[2], j = misc[3];
+      bool bad = false;
+      int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+      uint32_t it = 0;
+      for (int item = p0; item < p1; ++item) {
+        int32_t page = p.page_table[(int64_t)b * p.max_blocks + j];
+        if (page < 0 || page >= p.num_pages) {
+          msa_record_error(kErrBadPage);
+          page = 0;
+        }
+        for (int sp = 0; sp < stages_per_page; ++sp, ++it) {
+          const uint32_t slot = it % nstage;
+          if (it >= (uint32_t)nstage && !mbar_wait(&empty_bar[slot], ((it / nstage) - 1) & 1)) {
+            msa_record_error(kErrTimeout);
+            // let the copies already issued land before the CTA exits (bounded)
+            for (uint32_t k = it - nstage + 1; k < it; ++k)
+              mbar_wait(&full_bar[k % nstage], (k / nstage) & 1);
+            return;
+          }
+          uint8_t* dst = smem + slot * L.stage_bytes;
+          mbar_expect_tx(&full_bar[slot], L.stage_bytes);
+          const int32_t row = (int32_t)((int64_t)page * 128 * Hkv + (int64_t)sp * rows);
+          tma_load_2d(dst, &kmap, &full_bar[slot], 0, row);
+          if (DI == 128) tma_load_2d(dst + rows * 128, &kmap, &full_bar[slot], 64, row);
+        }
+        if (++j == nb) {
+          j = 0;
+          ++b;
+          if (b < p.B) nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+        }
+      }
+      // wait for the copies still in flight before the CTA may exit
+      for (uint32_t k = (it > (uint32_t)nstage ? it - nstage : 0); k < it; ++k)
+        if (!mbar_wait(&empty_bar[k % nstage], (k / nstage) & 1)) msa_record_error(kErrTimeout);
+    }
+    return;
+  }
+
+  // ================================== consumer warps
+  int b = misc[2], j = misc[3];
+  bool bad = false;
+  int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+  int cur_b = -1, done_pages = 0;
+  int qpos[kDecodeMaxN];
+  uint32_t it = 0;
+  const int g = tid % Hkv;
+  const bool has_row = tid < rows;
+
+  auto finish_request = [&](int rb, int count) {
+    // every writer fenced its scores; publish this CTA's share of the request
+    consumer_sync();
+    if (tid == 0) {
+      bool bad_r = false;
+      const int nbr = (clamp_seq(p.seq_lens, rb, N, p.max_blocks, bad_r) + 127) / 128;
+      const int old = atomicAdd(&p.tickets[rb], count);
+      misc[4] = (old + count == nbr) ? 1 : 0;
+    }
+    consumer_sync();
+    if (misc[4]) {
+      __threadfence();
+      for (int item = warp; item < N * Hkv; item += kConsumerWarps) {
+        const int i = item / Hkv, gg = item % Hkv;
+        const int64_t r = (int64_t)rb * N + i;
+        bool bad_r = false;
+        const int qp = clamp_seq(p.seq_lens, rb, N, p.max_blocks, bad_r) - N + i;
+        const int64_t orow = (r * Hkv + gg) * p.topk;
+        warp_topk(p.scores + (r * Hkv + gg) * p.max_blocks, qp / 128, p.topk, p.block_ids + orow,
+                  p.sel_scores ? p.sel_scores + orow : nullptr, stopk[warp]);
+      }
+    }
+    consumer_sync();
+  };
+
+  for (int item = p0; item < p1; ++item) {
+    if (b != cur_b) {
+      if (cur_b >= 0) finish_request(cur_b, done_pages);
+      cur_b = b;
+      done_pages = 0;
+      // query index rows of request b -> fp32 shared memory (rows padded by 4 floats)
+      const uint16_t* qsrc = p.q_idx + (int64_t)b * N * Hkv * DI;
+      for (int e = tid; e < N * Hkv * DI; e += kConsumers) {
+        const int row = e / DI, d = e % DI;
+        sq[row * (DI + 4) + d] = __uint_as_float((uint32_t)qsrc[e] << 16);
+      }
+#pragma unroll
+      for (int i = 0; i < kDecodeMaxN; ++i)
+        qpos[i] = clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) - N + i;
+      consumer_sync();
+    }
+    float rm[kDecodeMaxN];
+#pragma unroll
+    for (int i = 0; i < kDecodeMaxN; ++i) rm[i] = -INFINITY;
+
+    for (int sp = 0; sp < stages_per_page; ++sp, ++it) {
+      const uint32_t slot = it % nstage;
+      // A failed wait is recorded and the thread keeps following the same barriers as
+      // the others; the CTA leaves the loop together after the page-end barrier.
+      const bool ok = mbar_wait(&full_bar[slot], (it / nstage) & 1);
+      if (!ok) {
+        msa_record_error(kErrTimeout);
+        misc[5] = 1;
+      }
+      if (ok && has_row) {
+        const uint8_t* st = smem + slot * L.stage_bytes;
+        const int tok = sp * tok_per_stage + tid / Hkv;
+        const int pos = j * 128 + tok;
+        float acc[kDecodeMaxN];
+#pragma unroll
+        for (int i = 0; i < kDecodeMaxN; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int h = 0; h < DI / 64; ++h) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(st + h * rows * 128 + sw128(tid, c));
+            float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                           bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+#pragma unroll
+            for (int i = 0; i < kDecodeMaxN; ++i) {
+              if (i < N) {
+                const float* qr = sq + (i * Hkv + g) * (DI + 4) + h * 64 + c * 8;
+                const float4 qa = *reinterpret_cast<const float4*>(qr);
+                const float4 qb = *reinterpret_cast<const float4*>(qr + 4);
+                acc[i] = fmaf(qa.x, kf[0], acc[i]);
+                acc[i] = fmaf(qa.y, kf[1], acc[i]);
+                acc[i] = fmaf(qa.z, kf[2], acc[i]);
+                acc[i] = fmaf(qa.w, kf[3], acc[i]);
+                acc[i] = fmaf(qb.x, kf[4], acc[i]);
+                acc[i] = fmaf(qb.y, kf[5], acc[i]);
+                acc[i] = fmaf(qb.z, kf[6], acc[i]);
+                acc[i] = fmaf(qb.w, kf[7], acc[i]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kDecodeMaxN; ++i)
+          if (i < N && pos <= qpos[i]) rm[i] = fmaxf(rm[i], acc[i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    }
+    // ---- page end: max over the page's tokens for each (query row, group)
+#pragma unroll
+    for (int i = 0; i < kDecodeMaxN; ++i) {
+      if (i < N) {
+        float v = rm[i];
+        for (int off = 16; off >= Hkv; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane < Hkv) sred[(warp * N + i) * Hkv + lane] = v;
+      }
+    }
+    consumer_sync();
+    if (tid < N * Hkv) {
+      float v = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) v = fmaxf(v, sred[w * N * Hkv + tid]);
+      const int i = tid / Hkv, gg = tid % Hkv;
+      const int64_t r = (int64_t)b * N + i;
+      p.scores[(r * Hkv + gg) * p.max_blocks + j] = v;
+      __threadfence();
+    }
+    consumer_sync();
+    if (misc[5]) return;  // uniform: read by every consumer after the same barrier
+    ++done_pages;
+    if (++j == nb) {
+      j = 0;
+      ++b;
+      if (b < p.B) nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+    }
+  }
+  if (cur_b >= 0) finish_request(cur_b, done_pages);
+}
+
+// ---------------------------------------------------------------------------------------
+// Generic scorer: CTA = (request, 32 query rows, group, chunk of 16 blocks).
+constexpr int kRowTile = 32;
+constexpr int kBlkChunk = 16;
+
+template <int DI>
+__global__ void __launch_bounds__(256) score_rows_kernel(const ScoreArgs a, int tiles_per_req) {
+  __shared__ __align__(16) float sq[kRowTile][DI + 4];
+  __shared__ __align__(16) uint16_t sk[128][DI + 8];
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x / tiles_per_req;
+  const int i0 = (blockIdx.x % tiles_per_req) * kRowTile;
+  const int g = blockIdx.y;
+  const int j_begin = blockIdx.z * kBlkChunk;
+  const int j_end = min(a.max_blocks, j_begin + kBlkChunk);
+  bool bad = false;
+  const int seq = clamp_seq(a.seq_lens, b, a.N, a.max_blocks, bad);
+  if (bad && threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) msa_record_error(kErrBadBlock);
+  const int nrows = min(kRowTile, a.N - i0);
+  for (int e = tid; e < kRowTile * DI; e += 256) {
+    const int rr = e / DI, d = e % DI;
+    float v = 0.0f;
+    if (rr < nrows) {
+      const int64_t r = (int64_t)b * a.N + i0 + rr;
+      v = __uint_as_float((uint32_t)a.q_idx[(r * a.Hkv + g) * DI + d] << 16);
+    }
+    sq[rr][d] = v;
+  }
+  const int rr = tid >> 3, sub = tid & 7;
+  const int qp = seq - a.N + i0 + rr;                  // this thread's query position
+  const int tile_local = (seq - a.N + i0 + nrows - 1) / 128;
+  for (int j = j_begin; j < j_end; ++j) {
+    float best = -INFINITY;
+    if (j <= tile_local) {
+      int32_t page = a.page_table[(int64_t)b * a.max_blocks + j];
+      if (page < 0 || page >= a.num_pages) {
+        msa_record_error(kErrBadPage);
+        page = 0;
+      }
+      __syncthreads();
+      for (int e = tid; e < 128 * (DI / 8); e += 256) {
+        const int tok = e / (DI / 8), c = e % (DI / 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            a.k_idx + (((int64_t)page * 128 + tok) * a.Hkv + g) * DI + c * 8);
+        *reinterpret_cast<uint4*>(&sk[tok][c * 8]) = v;
+      }
+      __syncthreads();
+      float acc[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
+#pragma unroll 4
+      for (int c = 0; c < DI / 8; ++c) {
+        const float4 qa = *reinterpret_cast<const float4*>(&sq[rr][c * 8]);
+        const float4 qb = *reinterpret_cast<const float4*>(&sq[rr][c * 8 + 4]);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(&sk[sub + 8 * m][c * 8]);
+          acc[m] = fmaf(qa.x, bf16_lo(kv.x), acc[m]);
+          acc[m] = fmaf(qa.y, bf16_hi(kv.x), acc[m]);
+          acc[m] = fmaf(qa.z, bf16_lo(kv.y), acc[m]);
+          acc[m] = fmaf(qa.w, bf16_hi(kv.y), acc[m]);
+          acc[m] = fmaf(qb.x, bf16_lo(kv.z), acc[m]);
+          acc[m] = fmaf(qb.y, bf16_hi(kv.z), acc[m]);
+          acc[m] = fmaf(qb.z, bf16_lo(kv.w), acc[m]);
+          acc[m] = fmaf(qb.w, bf16_hi(kv.w), acc[m]);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (j * 128 + sub + 8 * m <= qp) best = fmaxf(best, acc[m]);
+    }
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 4));
+    if (sub == 0 && rr < nrows) {
+      const int64_t r = (int64_t)b * a.N + i0 + rr;
+      a.scores[(r * a.Hkv + g) * a.max_blocks + j] = best;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) topk_rows_kernel(const ScoreArgs a) {
+  __shared__ TopkScratch ws[8];
+  const int warp = threadIdx.x >> 5;
+  const int64_t item = (int64_t)blockIdx.x * 8 + warp;
+  const int64_t R = (int64_t)a.B * a.N;
+  if (item >= R * a.Hkv) return;
+  const int64_t r = item / a.Hkv;
+  const int b = (int)(r / a.N);
+  bool bad = false;
+  const int qp = clamp_seq(a.seq_lens, b, a.N, a.max_blocks, bad) - a.N + (int)(r % a.N);
+  warp_topk(a.scores + item * a.max_blocks, qp / 128, a.topk, a.block_ids + item * a.topk,
+            a.sel_scores ? a.sel_scores + item * a.topk : nullptr, ws[warp]);
+}
+
+constexpr size_t kSmemMax = 232448;  // opt-in shared memory per block on sm_100/sm_103
+
+}  // namespace
+
+size_t score_decode_smem_bytes(int N, int Hkv, int Di, int* nstage) {
+  for (int ns = 4; ns >= 2; --ns) {
+    const DecodeSmemLayout L = decode_layout(N, Hkv, Di, ns);
+    if (L.total <= kSmemMax) {
+      if (nstage) *nstage = ns;
+      return L.total;
+    }
+  }
+  if (nstage) *nstage = 0;
+  return 0;
+}
+
+cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
+  int nstage = 0;
+  const size_t smem = score_decode_smem_bytes(a.N, a.Hkv, a.Di, &nstage);
+  if (nstage < 2) return cudaErrorInvalidValue;
+  const int rows = kStageRows < 128 * a.Hkv ? kStageRows : 128 * a.Hkv;
+  CUtensorMap map;
+  const uint64_t dims[2] = {(uint64_t)a.Di, (uint64_t)a.num_pages * 128 * a.Hkv};
+  const uint64_t strides[1] = {(uint64_t)a.Di * 2};
+  const uint32_t box[2] = {64, (uint32_t)rows};
+  if (!encode_bf16_map(&map, a.k_idx, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+  DecodeKParams p;
+  p.q_idx = a.q_idx;
+  p.page_table = a.page_table;
+  p.seq_lens = a.seq_lens;
+  p.B = a.B;
+  p.N = a.N;
+  p.Hkv = a.Hkv;
+  p.max_blocks = a.max_blocks;
+  p.topk = a.topk;
+  p.nstage = nstage;
+  p.num_pages = a.num_pages;
+  p.block_ids = a.block_ids;
+  p.sel_scores = a.sel_scores;
+  p.scores = a.scores;
+  p.tickets = a.tickets;
+  const int grid = sm_count();
+  cudaError_t e;
+  if (a.Di == 128) {
+    e = cudaFuncSetAttribute(score_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    score_decode_kernel<128><<<grid, kThreads, smem, stream>>>(map, p);
+  } else {
+    e = cudaFuncSetAttribute(score_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    score_decode_kernel<64><<<grid, kThreads, smem, stream>>>(map, p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_rows(const ScoreArgs& a, cudaStream_t stream) {
+  const int tiles = (a.N + kRowTile - 1) / kRowTile;
+  dim3 grid((unsigned)(a.B * tiles), (unsigned)a.Hkv,
+            (unsigned)((a.max_blocks + kBlkChunk - 1) / kBlkChunk));
+  if (a.Di == 128)
+    score_rows_kernel<128><<<grid, 256, 0, stream>>>(a, tiles);
+  else
+    score_rows_kernel<64><<<grid, 256, 0, stream>>>(a, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_rows(const ScoreArgs& a, cudaStream_t stream) {
+  const int64_t items = (int64_t)a.B * a.N * a.Hkv;
+  topk_rows_kernel<<<(unsigned)((items + 7) / 8), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

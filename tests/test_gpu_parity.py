@@ -1,0 +1,216 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Sizes span several tiles and ragged tails (sequence lengths not multiples of 128, fewer
+causal blocks than k, a query inside block 0) and finish in seconds on the oracle.
+Tolerances (tests/_compare.py): block ids bit-exact up to near-tie swaps (1e-3 relative
+on the oracle's scores), scores 1e-3 relative, attention o 2e-2 max-abs / 5e-3 mean-abs,
+LSE 1e-3; page tables and bucket lists bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_msa_gb300 as msa
+import oracle
+import workloads
+from _compare import (check_attention, check_selected_scores, check_selection, f32, u16)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_sparse_attention_msa_gb300 import build
+    build.build()
+    msa.load()
+    yield
+    assert msa.device_error() == 0
+
+
+def _score_case(seq_lens, N, Hkv, Di, topk, seed, n_planted=0):
+    w = workloads.index_workload(seq_lens, N, Hkv, Di, seed=seed, device="cpu", n_planted=n_planted)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    ids, sc = msa.index_score_topk(d["q_idx"], d["k_idx_pages"], d["page_table"], d["seq_lens"], N,
+                                   topk)
+    torch.cuda.synchronize()
+    s_ref = oracle.block_scores(u16(w["q_idx"]), u16(w["k_idx_pages"]), w["page_table"].numpy(),
+                                w["seq_lens"].numpy(), N)
+    ids_ref, _ = oracle.topk(s_ref, oracle.query_positions(w["seq_lens"].numpy(), N), topk)
+    ids_np = ids.cpu().numpy()
+    check_selection(ids_np, ids_ref, s_ref)
+    check_selected_scores(ids_np, sc.cpu().numpy(), s_ref)
+    return w, ids_np, ids_ref
+
+
+@pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
+    ([517, 300, 1000, 128, 60], 1, 8, 128, 4),      # ragged, fewer blocks than k, one block
+    ([5000, 129, 3000], 1, 2, 64, 16),              # Di 64, Hkv 2
+    ([2000, 2049], 1, 16, 128, 6),                  # Hkv 16 (16 tokens per stage)
+    ([1500, 700], 1, 1, 64, 3),                     # Hkv 1 (128-row stages)
+    ([4096, 3000, 999, 12000], 4, 8, 128, 8),       # multi-token decode N = 4
+    ([7000, 6100], 8, 4, 64, 16),                   # N = 8
+])
+def test_score_topk_streaming_path(seq_lens, N, Hkv, Di, topk):
+    _score_case(seq_lens, N, Hkv, Di, topk, seed=hash((tuple(seq_lens), N, Hkv)) % 1000)
+
+
+@pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
+    ([700], 300, 2, 64, 4),                         # prefill chunk, ragged row tile
+    ([2048, 1500], 33, 4, 128, 5),                  # two requests, N just above the streaming cap
+])
+def test_score_topk_row_path(seq_lens, N, Hkv, Di, topk):
+    _score_case(seq_lens, N, Hkv, Di, topk, seed=7)
+
+
+def test_score_topk_planted_blocks_found():
+    w, ids, _ = _score_case([60 * 128, 45 * 128 + 3, 70 * 128], 1, 8, 128, 16, seed=3, n_planted=8)
+    planted = w["planted"].numpy()
+    for b in range(3):
+        for g in range(8):
+            assert set(planted[b, g].tolist()) <= set(ids[b, g].tolist())
+
+
+def test_score_topk_workspace_reuse_and_ties():
+    # identical keys in every block -> all scores tie; the lower ids must win every time,
+    # on repeated calls with the same (kept-zero) workspace
+    seq_lens, N, Hkv, Di, k = [640, 1280], 1, 2, 64, 4
+    w = workloads.index_workload(seq_lens, N, Hkv, Di, seed=1, device="cpu")
+    w["k_idx_pages"][:] = w["k_idx_pages"][0:1, 0:1]
+    ws = msa.Workspace()
+    for _ in range(3):
+        ids, _ = msa.index_score_topk(w["q_idx"].to(DEV), w["k_idx_pages"].to(DEV),
+                                      w["page_table"].to(DEV), w["seq_lens"].to(DEV), N, k,
+                                      workspace=ws)
+        s_ref = oracle.block_scores(u16(w["q_idx"]), u16(w["k_idx_pages"]), w["page_table"].numpy(),
+                                    w["seq_lens"].numpy(), N)
+        ids_ref, _ = oracle.topk(s_ref, oracle.query_positions(w["seq_lens"].numpy(), N), k)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+
+
+@pytest.mark.parametrize("N", [1, 3])
+def test_sparse_page_table_bit_exact(N):
+    w = workloads.decode_workload([517, 1500, 129, 9000], N, 16, 8, 128, 7, seed=2, device="cpu")
+    fpt, lens = msa.build_sparse_page_table(w["block_ids"].to(DEV), w["page_table"].to(DEV),
+                                            w["seq_lens"].to(DEV), N, w["num_pages"])
+    fpt_ref, lens_ref = oracle.build_sparse_page_table(w["block_ids"].numpy(), w["page_table"].numpy(),
+                                                       w["seq_lens"].numpy(), N)
+    assert np.array_equal(fpt.cpu().numpy(), fpt_ref)
+    assert np.array_equal(lens.cpu().numpy(), lens_ref)
+
+
+@pytest.mark.parametrize("seq_lens,N,Hq,Hkv,topk", [
+    ([517, 1500, 129, 9000, 40], 1, 64, 8, 16),      # G 8, ragged, 1-block request
+    ([3000, 700], 1, 16, 4, 5),                       # G 4
+    ([2500, 2600, 2700], 2, 32, 2, 9),                # G 16, N 2
+    ([20000], 1, 8, 8, 32),                           # G 1, k 32 (8 splits)
+])
+def test_paged_sparse_decode(seq_lens, N, Hq, Hkv, topk):
+    w = workloads.decode_workload(seq_lens, N, Hq, Hkv, 128, topk, seed=5, device="cpu")
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    fpt, lens = msa.build_sparse_page_table(d["block_ids"], d["page_table"], d["seq_lens"], N,
+                                            w["num_pages"])
+    o, lse = msa.paged_sparse_decode(d["q"], d["k_cache"], d["v_cache"], fpt, lens)
+    torch.cuda.synchronize()
+    ref = oracle.sparse_decode(u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"]), w["page_table"].numpy(),
+                               w["seq_lens"].numpy(), w["block_ids"].numpy(), N)
+    check_attention(o, lse, ref, what="decode")
+
+
+@pytest.mark.parametrize("T,S,Hq,Hkv,topk,n_shared", [
+    (300, 700, 16, 2, 4, 2),        # chunk after a prefix, ragged
+    (1000, 1000, 64, 8, 16, 12),    # causal, cfg3 structure at small T
+    (200, 200, 8, 8, 3, 0),         # G 1
+    (129, 5000, 32, 2, 8, 4),       # G 16, long prefix
+])
+def test_sparse_prefill(T, S, Hq, Hkv, topk, n_shared):
+    w = workloads.prefill_workload(T, S, Hq, Hkv, 128, topk, seed=11, device="cpu", n_shared=n_shared)
+    o, lse = msa.sparse_prefill(w["q"].to(DEV), w["k"].to(DEV), w["v"].to(DEV), w["block_ids"].to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sparse_prefill(u16(w["q"]), u16(w["k"]), u16(w["v"]), w["block_ids"].numpy())
+    check_attention(o, lse, ref, what="prefill")
+
+
+def test_prefill_bucket_lists():
+    w = workloads.prefill_workload(900, 1500, 16, 4, 128, 6, seed=4, device="cpu", n_shared=3)
+    nblk = (1500 + 127) // 128
+    off, ent = msa.prefill_bucket(w["block_ids"].to(DEV), nblk)
+    off_ref, ent_ref = oracle.prefill_buckets(w["block_ids"].numpy(), nblk)
+    off = off.cpu().numpy()
+    ent = ent.cpu().numpy()
+    assert np.array_equal(off, off_ref)
+    base = 0
+    for g in range(off.shape[0]):
+        for j in range(nblk):
+            a, b = base + off[g, j], base + off[g, j + 1]
+            assert np.array_equal(np.sort(ent[a:b]), ent_ref[a:b])  # order inside a list is free
+        base += off[g, nblk]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_lse_merge(dtype):
+    g = torch.Generator().manual_seed(0)
+    U, S, G, D = 37, 9, 4, 128
+    o_parts = torch.randn(U, S, G, D, generator=g).to(dtype)
+    lse_parts = torch.randn(U, S, G, generator=g) * 3
+    lse_parts[0, :, :] = -float("inf")              # unit with no partial
+    lse_parts[1, 1:, :] = -float("inf")             # single partial
+    lse_parts[2, ::2, 1] = -float("inf")
+    o, lse = msa.lse_merge(o_parts.to(DEV), lse_parts.to(DEV))
+    torch.cuda.synchronize()
+    o_np, lse_np = f32(o), lse.cpu().numpy()
+    op = o_parts.float().numpy()
+    lp = lse_parts.numpy()
+    for u in range(U):
+        for e in range(G):
+            ref_o, ref_l = oracle.lse_merge(op[u, :, e], lp[u, :, e])
+            assert np.abs(o_np[u, e] - ref_o).max() <= 1e-2
+            if np.isfinite(ref_l):
+                assert abs(lse_np[u, e] - ref_l) <= 1e-4
+            else:
+                assert lse_np[u, e] == -np.inf
+
+
+def test_pr1_layer_end_to_end():
+    """PR1: 2048-token layer (Hq 8, Hkv 2, Di 64, k 4): prefill then 16 decode steps."""
+    w = workloads.cfg_pr1("cpu", seed=0)
+    T, Hq, Hkv, D, Di, k, P = w["T"], w["Hq"], w["Hkv"], w["D"], w["Di"], w["topk"], w["P"]
+    kidx = w["k_idx"].view(P, 128, Hkv, Di)
+    kc, vc = w["k"].view(P, 128, Hkv, D), w["v"].view(P, 128, Hkv, D)
+    pt = w["page_table"]
+    g_kidx, g_kc, g_vc, g_pt = kidx.to(DEV), kc.to(DEV), vc.to(DEV), pt.to(DEV)
+    # prefill: score + top-k for all 2048 rows, then block-major attention on the GPU's selection
+    sl = torch.tensor([T], dtype=torch.int32)
+    ids, sc = msa.index_score_topk(w["q_idx"][:T].to(DEV), g_kidx, g_pt, sl.to(DEV), T, k)
+    s_ref = oracle.block_scores(u16(w["q_idx"][:T]), u16(kidx), pt.numpy(), sl.numpy(), T)
+    ids_ref, _ = oracle.topk(s_ref, oracle.query_positions(sl.numpy(), T), k)
+    check_selection(ids.cpu().numpy(), ids_ref, s_ref)
+    check_selected_scores(ids.cpu().numpy(), sc.cpu().numpy(), s_ref)
+    o, lse = msa.sparse_prefill(w["q"][:T].to(DEV), w["k"][:T].to(DEV), w["v"][:T].to(DEV), ids)
+    ref = oracle.sparse_prefill(u16(w["q"][:T]), u16(w["k"][:T]), u16(w["v"][:T]), ids.cpu().numpy())
+    check_attention(o, lse, ref, what="pr1 prefill")
+    # 16 decode steps: the cache already holds every token; step s sees seq_len T+s+1
+    for s in range(16):
+        pos = T + s
+        sl = torch.tensor([pos + 1], dtype=torch.int32)
+        q_idx = w["q_idx"][pos:pos + 1]
+        ids, _ = msa.index_score_topk(q_idx.to(DEV), g_kidx, g_pt, sl.to(DEV), 1, k)
+        s_ref = oracle.block_scores(u16(q_idx), u16(kidx), pt.numpy(), sl.numpy(), 1)
+        ids_ref, _ = oracle.topk(s_ref, oracle.query_positions(sl.numpy(), 1), k)
+        check_selection(ids.cpu().numpy(), ids_ref, s_ref)
+        fpt, lens = msa.build_sparse_page_table(ids, g_pt, sl.to(DEV), 1, P)
+        o, lse = msa.paged_sparse_decode(w["q"][pos:pos + 1].to(DEV), g_kc, g_vc, fpt, lens)
+        ref = oracle.sparse_decode(u16(w["q"][pos:pos + 1]), u16(kc), u16(vc), pt.numpy(), sl.numpy(),
+                                   ids.cpu().numpy(), 1)
+        check_attention(o, lse, ref, what=f"pr1 decode step {s}")
+
+
+def test_full_selection_equals_dense_causal_attention():
+    """k >= number of causal blocks: MSA prefill is dense causal attention (oracle-checked)."""
+    T = 600
+    w = workloads.prefill_workload(T, T, 16, 2, 128, 5, seed=9, device="cpu", n_shared=0)
+    assert (w["block_ids"][-1] >= 0).all()  # the last query keeps all 5 blocks
+    o, lse = msa.sparse_prefill(w["q"].to(DEV), w["k"].to(DEV), w["v"].to(DEV), w["block_ids"].to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sparse_prefill(u16(w["q"]), u16(w["k"]), u16(w["v"]), w["block_ids"].numpy())
+    check_attention(o, lse, ref, what="dense-equivalent prefill")
