@@ -1,0 +1,464 @@
+"""Benchmark of the GB300 MSA layer hot path.
+
+One step = one pass of every hot-path stage over its synthetic workload, inputs resident in
+HBM (all larger than the 129 MB L2, so no flush is needed between steps):
+  * index score + top-k     decode scoring: 8 requests x 60032 tokens, Hkv 8, Di 128, k 16
+                            (8 planted high-affinity blocks per request and group)
+  * sparse page table + paged sparse decode: 64 requests, context ~U[8K, 128K], Hq 64,
+                            Hkv 8, D 128, k 16 (KV groups flattened into 512 rows)
+  * block-major sparse prefill (bucketing, attention partials, LSE merge): 32768-token
+                            causal chunk, Hq 64, Hkv 8, D 128, k 16, clustered selections
+The headline `value` is the index-score + top-k HBM throughput (GB/s of K-index scanned);
+`stages` carries every stage's throughput and roofline fraction.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica of the workload (the layer shards by
+request and KV group with no exchange): value = all ranks' bytes / max-over-ranks time.
+`--impl reference` times the CPU oracle instead (rank 0 only) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "index-score+topk & sparse-decode HBM GB/s; prefill sparse-attn TFLOP/s (%peak)"
+BLOCK = 128
+
+
+# --------------------------------------------------------------------------- environment
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workloads
+
+def visible_keys(block_ids: torch.Tensor, q_pos: torch.Tensor) -> torch.Tensor:
+    """Visible keys per (row, group) for kept blocks: 128 below the local block, q_pos%128+1 in it."""
+    local = (q_pos // BLOCK)[:, None, None]
+    ids = block_ids.to(torch.int64)
+    n = torch.where(ids < local, torch.full_like(ids, BLOCK),
+                    torch.where(ids == local, (q_pos % BLOCK + 1)[:, None, None].expand_as(ids),
+                                torch.zeros_like(ids)))
+    n = torch.where(ids >= 0, n, torch.zeros_like(n))
+    return n.sum(dim=2)
+
+
+def build_workloads(dev, seed_offset: int):
+    c2 = workloads.cfg2(dev, seed=2 + seed_offset)
+    c4 = workloads.cfg4(dev, seed=4 + seed_offset)
+    c3 = workloads.cfg3(dev, seed=3 + seed_offset)
+    # algorithmic work per stage
+    B, Hkv, Di = c2["B"], c2["Hkv"], c2["Di"]
+    sl2 = c2["seq_lens"].to(torch.int64)
+    c2["bytes"] = int(sl2.sum().item()) * Hkv * Di * 2 + c2["q_idx"].numel() * 2 \
+        + c2["page_table"].numel() * 4 + B * Hkv * c2["topk"] * 8
+    q_pos4 = c4["seq_lens"].to(torch.int64) - 1
+    keys4 = visible_keys(c4["block_ids"], q_pos4)                 # [B, Hkv]
+    G4 = c4["Hq"] // c4["Hkv"]
+    c4["bytes"] = int(keys4.sum().item()) * c4["D"] * 2 * 2 + c4["q"].numel() * 2 * 2 \
+        + c4["B"] * c4["Hq"] * 4
+    c4["kv_bytes"] = int(keys4.sum().item()) * c4["D"] * 2 * 2
+    q_pos3 = torch.arange(c3["S_kv"] - c3["T"], c3["S_kv"], device=dev, dtype=torch.int64)
+    keys3 = visible_keys(c3["block_ids"], q_pos3)                 # [T, Hkv]
+    G3 = c3["Hq"] // c3["Hkv"]
+    c3["flops"] = 4 * c3["D"] * G3 * int(keys3.sum().item())
+    del G4
+    return c2, c4, c3
+
+
+def src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_attention_msa_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, source_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != source_hash:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank, local):
+    import block_sparse_attention_msa_gb300 as msa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    msa.load(build_if_missing=True)
+    pk = peaks()
+    c2, c4, c3 = build_workloads(dev, seed_offset=1000 * rank)
+    wsp = msa.Workspace()
+    # preallocated outputs
+    R2 = c2["B"]
+    ids2 = torch.empty((R2, c2["Hkv"], c2["topk"]), dtype=torch.int32, device=dev)
+    sc2 = torch.empty((R2, c2["Hkv"], c2["topk"]), dtype=torch.float32, device=dev)
+    R4 = c4["B"]
+    fpt4 = torch.empty((R4 * c4["Hkv"], c4["topk"]), dtype=torch.int32, device=dev)
+    len4 = torch.empty((R4 * c4["Hkv"],), dtype=torch.int32, device=dev)
+    o4 = torch.empty((R4, c4["Hq"], c4["D"]), dtype=torch.bfloat16, device=dev)
+    lse4 = torch.empty((R4, c4["Hq"]), dtype=torch.float32, device=dev)
+    o3 = torch.empty((c3["T"], c3["Hq"], c3["D"]), dtype=torch.bfloat16, device=dev)
+    lse3 = torch.empty((c3["T"], c3["Hq"]), dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        msa.index_score_topk(c2["q_idx"], c2["k_idx_pages"], c2["page_table"], c2["seq_lens"], 1,
+                             c2["topk"], workspace=wsp, out=(ids2, sc2))
+        if ev is not None:
+            ev[1].record()
+        msa.build_sparse_page_table(c4["block_ids"], c4["page_table"], c4["seq_lens"], 1,
+                                    c4["num_pages"], out=(fpt4, len4))
+        if ev is not None:
+            ev[2].record()
+        msa.paged_sparse_decode(c4["q"], c4["k_cache"], c4["v_cache"], fpt4, len4, workspace=wsp,
+                                out=(o4, lse4))
+        if ev is not None:
+            ev[3].record()
+        msa.sparse_prefill(c3["q"], c3["k"], c3["v"], c3["block_ids"], workspace=wsp, out=(o3, lse3))
+        if ev is not None:
+            ev[4].record()
+
+    for _ in range(args.warmup):
+        step()
+    # per-kernel breakdown of the prefill call (separate entry points, timed once, not in value)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(args.steps):
+            step(evs[k])
+        stop.record()
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(4)]
+    if ws > 1:
+        t = torch.tensor([total_ms] + stage_ms, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, stage_ms = float(t[0]), [float(x) for x in t[1:]]
+    ms_per_step = total_ms / args.steps
+    score_ms, pt_ms, dec_ms, pre_ms = stage_ms
+    # device error word: none expected
+    err = msa.device_error()
+
+    # prefill sub-steps, timed separately after the main loop: bucketing and merge alone
+    sub = prefill_breakdown(msa, c3, wsp, dev, reps=max(3, args.steps))
+
+    score_gbs = c2["bytes"] / (score_ms * 1e-3) / 1e9
+    dec_gbs = c4["bytes"] / ((pt_ms + dec_ms) * 1e-3) / 1e9
+    pre_tflops = c3["flops"] / (pre_ms * 1e-3) / 1e12
+    attn_ms = max(pre_ms - sub["bucket_ms"] - sub["merge_ms"], 1e-6)
+    attn_tflops = c3["flops"] / (attn_ms * 1e-3) / 1e12
+    value = score_gbs * ws
+
+    # e2e through host buffers for the headline stage
+    e2e = e2e_score(msa, c2, wsp, dev, args.steps, ws)
+
+    h_score = src_hash("score_topk.cu")
+    roofline = {"kernel": "score_decode_kernel (msa_index_score_topk)", "bound": "hbm",
+                "achieved": round(score_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(score_gbs / pk["hbm_gbs"], 4),
+                "traffic": recorded_traffic("score_decode_kernel", h_score),
+                "algorithmic_bytes": c2["bytes"], "peak_source": pk["source"]}
+    stages = {
+        "index_score_topk": {"config": "8 x 60032 tokens, Hkv 8, Di 128, k 16", "ms": round(score_ms, 4),
+                             "GB/s": round(score_gbs, 1), "frac_hbm": round(score_gbs / pk["hbm_gbs"], 4),
+                             "bytes": c2["bytes"]},
+        "sparse_decode": {"config": "64 req, ctx U[8K,128K], Hq 64, Hkv 8, D 128, k 16",
+                          "ms_page_table": round(pt_ms, 4), "ms_decode": round(dec_ms, 4),
+                          "GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
+                          "bytes": c4["bytes"], "kv_bytes": c4["kv_bytes"],
+                          "traffic": recorded_traffic("paged_decode_kernel", src_hash("decode.cu"))},
+        "sparse_prefill": {"config": "T 32768 causal, Hq 64, Hkv 8, D 128, k 16", "ms": round(pre_ms, 4),
+                           "TFLOP/s": round(pre_tflops, 1),
+                           "frac_bf16": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
+                           "attention_only_ms": round(attn_ms, 4),
+                           "attention_only_TFLOP/s": round(attn_tflops, 1),
+                           "attention_only_frac_bf16": round(attn_tflops / pk["bf16_tflops_sustained"], 4),
+                           "bucket_ms": round(sub["bucket_ms"], 4), "merge_ms": round(sub["merge_ms"], 4),
+                           "flops": c3["flops"],
+                           "traffic": recorded_traffic("prefill_partials_kernel", src_hash("prefill.cu"))},
+    }
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, device-generated)",
+        "config": {"workload": "decode index score + top-k: 8 requests x 60032 tokens (469 blocks), "
+                               "Hkv 8, Di 128, k 16; step also runs paged sparse decode (64 req) and "
+                               "block-major sparse prefill (32768 tokens)",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "stages": stages, "e2e": e2e,
+        "gpu_launches": 9 * args.steps,
+        "clocks": clk.summary(), "device_error_word": err,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(c2, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def prefill_breakdown(msa, c3, wsp, dev, reps: int):
+    """Bucketing and merge timed alone on the prefill workload (same entry points the
+    prefill call runs internally), to attribute the prefill call's time."""
+    nblk = (c3["S_kv"] + BLOCK - 1) // BLOCK
+    T, Hkv, k, G = c3["T"], c3["Hkv"], c3["topk"], c3["Hq"] // c3["Hkv"]
+    parts_o = torch.zeros((T * Hkv, k, G, c3["D"]), dtype=torch.bfloat16, device=dev)
+    parts_l = torch.zeros((T * Hkv, k, G), dtype=torch.float32, device=dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    c = torch.cuda.Event(enable_timing=True)
+    msa.prefill_bucket(c3["block_ids"], nblk, workspace=wsp)
+    msa.lse_merge(parts_o, parts_l)
+    torch.cuda.synchronize()
+    bt = mt = 0.0
+    for _ in range(reps):
+        a.record()
+        msa.prefill_bucket(c3["block_ids"], nblk, workspace=wsp)
+        b.record()
+        msa.lse_merge(parts_o, parts_l)
+        c.record()
+        torch.cuda.synchronize()
+        bt += a.elapsed_time(b)
+        mt += b.elapsed_time(c)
+    del parts_o, parts_l
+    return {"bucket_ms": bt / reps, "merge_ms": mt / reps}
+
+
+def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
+    """Headline stage through the public API with pinned host buffers: per step the query
+    index rows, page table and lengths go host->device and the selection comes back; the
+    paged K-index cache is resident state (it is written once per token, not per step)."""
+    h_q = c2["q_idx"].cpu().pin_memory()
+    h_pt = c2["page_table"].cpu().pin_memory()
+    h_sl = c2["seq_lens"].cpu().pin_memory()
+    R, Hkv, k = c2["B"], c2["Hkv"], c2["topk"]
+    h_ids = torch.empty((R, Hkv, k), dtype=torch.int32).pin_memory()
+    h_sc = torch.empty((R, Hkv, k), dtype=torch.float32).pin_memory()
+    d_q = torch.empty_like(c2["q_idx"])
+    d_pt = torch.empty_like(c2["page_table"])
+    d_sl = torch.empty_like(c2["seq_lens"])
+    ids = torch.empty((R, Hkv, k), dtype=torch.int32, device=dev)
+    sc = torch.empty((R, Hkv, k), dtype=torch.float32, device=dev)
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        d_pt.copy_(h_pt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        msa.index_score_topk(d_q, c2["k_idx_pages"], d_pt, d_sl, 1, k, workspace=wsp, out=(ids, sc))
+        h_ids.copy_(ids, non_blocking=True)
+        h_sc.copy_(sc, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = h_q.numel() * 2 + h_pt.numel() * 4 + h_sl.numel() * 4
+    d2h = h_ids.numel() * 4 + h_sc.numel() * 4
+    return {"value": round(c2["bytes"] / (ms * 1e-3) / 1e9 * ws, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "per-step inputs copied from pinned host memory; paged K-index resident"}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def _oracle_score_step(oracle, h):
+    s = oracle.block_scores(h["q_idx"], h["k_idx"], h["pt"], h["sl"], 1, rows=h["rows"])
+    ids, _ = oracle.topk(s, h["q_pos"][h["rows"]], h["topk"])
+    return ids
+
+
+def _host_cfg2(c2, rows):
+    import numpy as np
+    u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    sl = c2["seq_lens"].cpu().numpy()
+    return {"q_idx": u16(c2["q_idx"]), "k_idx": u16(c2["k_idx_pages"]),
+            "pt": c2["page_table"].cpu().numpy(), "sl": sl, "topk": c2["topk"],
+            "q_pos": (sl.astype("int64") - 1), "rows": np.asarray(rows, dtype=np.int64)}
+
+
+def cpu_baseline(c2, seconds: float):
+    """The oracle as it stands, timed on this host's cores on the headline workload."""
+    import oracle
+    B = c2["B"]
+    h = _host_cfg2(c2, list(range(B)))
+    per_row = c2["bytes"] / B
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        _oracle_score_step(oracle, h)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    gbs = n * B * per_row / dt / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": min(os.cpu_count() or 1, B),
+            "kind": "oracle",
+            "sample": f"{n} full passes of all {B} requests (scores + top-k) in {dt:.1f} s"}
+
+
+def run_reference(args, ws, rank, local):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    c2 = workloads.cfg2(dev, seed=2)
+    B = c2["B"]
+    c2["bytes"] = int(c2["seq_lens"].to(torch.int64).sum().item()) * c2["Hkv"] * c2["Di"] * 2 \
+        + c2["q_idx"].numel() * 2 + c2["page_table"].numel() * 4 + B * c2["Hkv"] * c2["topk"] * 8
+    h = _host_cfg2(c2, list(range(B)))
+    for _ in range(args.warmup):
+        _oracle_score_step(oracle, h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_score_step(oracle, h)
+    dt = time.perf_counter() - t0
+    ms = dt / args.steps * 1e3
+    gbs = c2["bytes"] / (ms * 1e-3) / 1e9
+    cores = min(os.cpu_count() or 1, B)
+    line = {"metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "impl": "reference",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "decode index score + top-k: 8 requests x 60032 tokens (469 blocks), "
+                                   "Hkv 8, Di 128, k 16", "parallelism": "cpu oracle"},
+            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step scores and selects all {B} requests"},
+            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_info()
+    if ws > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank, local)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
