@@ -20,7 +20,7 @@ import torch
 from . import _lib
 from ._lib import MSAError, library_path, load
 
-__all__ = ["index_score_topk", "build_sparse_page_table", "paged_sparse_decode", "sparse_prefill",
+__all__ = ["index_score_topk", "index_score_topk_noalloc", "build_sparse_page_table", "paged_sparse_decode", "sparse_prefill",
            "prefill_bucket", "lse_merge", "device_error", "Workspace", "MSAError", "load",
            "library_path", "BLOCK"]
 
@@ -113,6 +113,38 @@ def index_score_topk(q_idx, k_idx_pages, page_table, seq_lens, N: int, topk: int
                                   B, N, Hkv, Di, max_blocks, k_idx_pages.shape[0], topk, _ptr(ids),
                                   _ptr(sc), _ptr(buf), buf.numel(), _stream(dev))
     _lib.check("msa_index_score_topk", rc)
+    return ids, sc
+
+
+def index_score_topk_noalloc(q_idx, k_idx_pages, page_table, seq_lens, N: int, topk: int,
+                             with_scores: bool = True, out=None):
+    """``index_score_topk`` without a workspace (``msa_index_score_topk_noalloc``).
+
+    For callers that cannot hand the library device scratch memory: the library uses a
+    fixed 8 MiB array of its own on each device instead. Calls on one device share that
+    array, so calls that may overlap on the GPU must not use this function. The first
+    call on a device resolves the array's address; make it before any stream capture.
+    Raises MSAError (MSA_ERR_UNSUPPORTED) when B*N*Hkv*max_blocks needs more scratch.
+    """
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx_pages, "k_idx_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, max_blocks = page_table.shape
+    R, Hkv, Di = q_idx.shape
+    if R != B * N or k_idx_pages.shape[1:] != (BLOCK, Hkv, Di) or seq_lens.numel() != B:
+        raise ValueError("index_score_topk_noalloc: inconsistent shapes")
+    dev = q_idx.device
+    if out is None:
+        ids = torch.empty((R, Hkv, topk), dtype=torch.int32, device=dev)
+        sc = torch.empty((R, Hkv, topk), dtype=torch.float32, device=dev) if with_scores else None
+    else:
+        ids, sc = out
+    rc = load().msa_index_score_topk_noalloc(_ptr(q_idx), _ptr(k_idx_pages), _ptr(page_table),
+                                             _ptr(seq_lens), B, N, Hkv, Di, max_blocks,
+                                             k_idx_pages.shape[0], topk, _ptr(ids), _ptr(sc),
+                                             _stream(dev))
+    _lib.check("msa_index_score_topk_noalloc", rc)
     return ids, sc
 
 

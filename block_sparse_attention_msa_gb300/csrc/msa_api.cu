@@ -6,6 +6,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "host_util.h"
@@ -283,6 +284,63 @@ int msa_lse_merge(const void* o_parts, int32_t parts_bf16, const float* lse_part
   return cuda_status(msa::launch_lse_merge(o_parts, parts_bf16 != 0, lse_parts, nullptr, U, S, G,
                                            D, o, lse, as_stream(stream)),
                      "msa_lse_merge");
+}
+
+// ------------------------------------------------------------------------------ scoring without
+// a caller workspace
+//
+// Scratch of msa_index_score_topk_noalloc: one fixed array in device memory, created when
+// the library is loaded on a device and held until the process exits. Host code only sees a
+// host-side stand-in for it, so its device address is looked up once per device (below).
+static __device__ __align__(256) unsigned char g_noalloc_score_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, resolved on first use.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "msa_index_score_topk_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_score_scratch);
+    if (e != cudaSuccess || !p)
+      return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                         "msa_index_score_topk_noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MSA_OK;
+}
+}  // namespace
+
+int msa_index_score_topk_noalloc(const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                                 const int32_t* page_table, const int32_t* seq_lens, int32_t B,
+                                 int32_t N, int32_t Hkv, int32_t Di, int32_t max_blocks,
+                                 int64_t num_pages, int32_t topk, int32_t* block_ids,
+                                 float* scores, void* stream) {
+  if (B == 0 || N == 0) return ok();
+  const size_t need = msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks);
+  if (need > (size_t)MSA_NOALLOC_SCRATCH_BYTES)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "msa_index_score_topk_noalloc: this call needs %zu bytes of scratch but the "
+                "built-in scratch holds %zu (B*N*Hkv*max_blocks too large); call "
+                "msa_index_score_topk with a workspace instead",
+                need, (size_t)MSA_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != MSA_OK) return rc;
+  // Same checks, kernels and per-call clearing of the ticket counters as the workspace
+  // entry point; the scratch array simply stands in for the workspace.
+  return msa_index_score_topk(q_idx, k_idx_pages, page_table, seq_lens, B, N, Hkv, Di,
+                              max_blocks, num_pages, topk, block_ids, scores, scratch,
+                              (size_t)MSA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 // ------------------------------------------------------------------------------ diagnostics

@@ -226,6 +226,39 @@ MSA_API int msa_lse_merge(const void* o_parts, int32_t parts_bf16, const float* 
                   int32_t S, int32_t G, int32_t D, uint16_t* o, float* lse, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Stage 1 without a caller workspace.
+ *
+ * The pages have no counterpart to this call: it exists for callers that cannot provide
+ * device scratch memory. Examples are a plugin inside a host framework that owns all
+ * device memory and gives its plugins no allocator, or a decode loop that must not call
+ * cudaMalloc because the allocation would synchronise the device and stall the stream.
+ *
+ * Same arguments, results and errors as msa_index_score_topk, minus the workspace. The
+ * scratch is a fixed array of MSA_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory inside the
+ * library. Every GPU on which the library is loaded holds this array until the process
+ * exits. The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
+ *  - Limit: the call needs msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks)
+ *    <= MSA_NOALLOC_SCRATCH_BYTES, i.e. about B*N*Hkv*max_blocks <= 2 million block
+ *    scores. Larger calls return MSA_ERR_UNSUPPORTED before anything is queued.
+ *  - First call on a device: it looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current and caches it. Make that first call on each device before
+ *    any stream capture begins.
+ *  - Sharing: every call on a device uses the same array, which keeps the previous call's
+ *    contents. Each call clears the counters it needs at zero (an asynchronous memset on
+ *    `stream`). Calls whose execution may overlap on the GPU (different streams, no
+ *    ordering between them) race on the array and give undefined results. Order such
+ *    calls, or give each of them a workspace through msa_index_score_topk.
+ * ------------------------------------------------------------------------------------ */
+#define MSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+MSA_API int msa_index_score_topk_noalloc(const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                                         const int32_t* page_table, const int32_t* seq_lens,
+                                         int32_t B, int32_t N, int32_t Hkv, int32_t Di,
+                                         int32_t max_blocks, int64_t num_pages, int32_t topk,
+                                         int32_t* block_ids, float* scores, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------------------ */
 /* Thread-local message of the last failing call on this host thread ("" if none). */
