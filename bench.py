@@ -126,10 +126,11 @@ def visible_keys(block_ids: torch.Tensor, q_pos: torch.Tensor) -> torch.Tensor:
     return n.sum(dim=2)
 
 
-def build_workloads(dev, seed_offset: int):
+def build_workloads(dev, seed_offset: int, small: bool = False):
+    # --small (profiling captures only): 8 decode requests and an 8192-token prefill chunk
     c2 = workloads.cfg2(dev, seed=2 + seed_offset)
-    c4 = workloads.cfg4(dev, seed=4 + seed_offset)
-    c3 = workloads.cfg3(dev, seed=3 + seed_offset)
+    c4 = workloads.cfg4(dev, seed=4 + seed_offset, B=8 if small else None)
+    c3 = workloads.cfg3(dev, seed=3 + seed_offset, T=8192 if small else None)
     # algorithmic work per stage
     B, Hkv, Di = c2["B"], c2["Hkv"], c2["Di"]
     sl2 = c2["seq_lens"].to(torch.int64)
@@ -178,7 +179,8 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(dev)
     msa.load(build_if_missing=True)
     pk = peaks()
-    c2, c4, c3 = build_workloads(dev, seed_offset=1000 * rank)
+    c2, c4, c3 = build_workloads(dev, seed_offset=1000 * rank, small=args.small)
+    run = set(args.stages.split(","))
     wsp = msa.Workspace()
     # preallocated outputs
     R2 = c2["B"]
@@ -195,19 +197,24 @@ def run_ours(args, ws, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record()
-        msa.index_score_topk(c2["q_idx"], c2["k_idx_pages"], c2["page_table"], c2["seq_lens"], 1,
-                             c2["topk"], workspace=wsp, out=(ids2, sc2))
+        if "score" in run:
+            msa.index_score_topk(c2["q_idx"], c2["k_idx_pages"], c2["page_table"], c2["seq_lens"], 1,
+                                 c2["topk"], workspace=wsp, out=(ids2, sc2))
         if ev is not None:
             ev[1].record()
-        msa.build_sparse_page_table(c4["block_ids"], c4["page_table"], c4["seq_lens"], 1,
-                                    c4["num_pages"], out=(fpt4, len4))
+        if "decode" in run:
+            msa.build_sparse_page_table(c4["block_ids"], c4["page_table"], c4["seq_lens"], 1,
+                                        c4["num_pages"], out=(fpt4, len4))
         if ev is not None:
             ev[2].record()
-        msa.paged_sparse_decode(c4["q"], c4["k_cache"], c4["v_cache"], fpt4, len4, workspace=wsp,
-                                out=(o4, lse4))
+        if "decode" in run:
+            msa.paged_sparse_decode(c4["q"], c4["k_cache"], c4["v_cache"], fpt4, len4, workspace=wsp,
+                                    out=(o4, lse4))
         if ev is not None:
             ev[3].record()
-        msa.sparse_prefill(c3["q"], c3["k"], c3["v"], c3["block_ids"], workspace=wsp, out=(o3, lse3))
+        if "prefill" in run:
+            msa.sparse_prefill(c3["q"], c3["k"], c3["v"], c3["block_ids"], workspace=wsp,
+                               out=(o3, lse3))
         if ev is not None:
             ev[4].record()
 
@@ -241,17 +248,19 @@ def run_ours(args, ws, rank, local):
     err = msa.device_error()
 
     # prefill sub-steps, timed separately after the main loop: bucketing and merge alone
-    sub = prefill_breakdown(msa, c3, wsp, dev, reps=max(3, args.steps))
+    sub = prefill_breakdown(msa, c3, wsp, dev, reps=max(3, args.steps)) if "prefill" in run \
+        else {"bucket_ms": 0.0, "merge_ms": 0.0}
 
-    score_gbs = c2["bytes"] / (score_ms * 1e-3) / 1e9
-    dec_gbs = c4["bytes"] / ((pt_ms + dec_ms) * 1e-3) / 1e9
-    pre_tflops = c3["flops"] / (pre_ms * 1e-3) / 1e12
+    eps = 1e-9
+    score_gbs = c2["bytes"] / (max(score_ms, eps) * 1e-3) / 1e9
+    dec_gbs = c4["bytes"] / (max(pt_ms + dec_ms, eps) * 1e-3) / 1e9
+    pre_tflops = c3["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
     attn_ms = max(pre_ms - sub["bucket_ms"] - sub["merge_ms"], 1e-6)
     attn_tflops = c3["flops"] / (attn_ms * 1e-3) / 1e12
     value = score_gbs * ws
 
     # e2e through host buffers for the headline stage
-    e2e = e2e_score(msa, c2, wsp, dev, args.steps, ws)
+    e2e = e2e_score(msa, c2, wsp, dev, args.steps, ws) if "score" in run else None
 
     h_score = src_hash("score_topk.cu")
     roofline = {"kernel": "score_decode_kernel (msa_index_score_topk)", "bound": "hbm",
@@ -288,10 +297,16 @@ def run_ours(args, ws, rank, local):
                                "block-major sparse prefill (32768 tokens)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
-        "gpu_launches": 9 * args.steps,
+        "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
+                                      + ("prefill" in run) * 5),
         "clocks": clk.summary(), "device_error_word": err,
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
+        if key not in run:
+            stages[name] = None
+    if args.small or run != {"score", "decode", "prefill"}:
+        line["config"]["partial_run"] = f"stages={sorted(run)} small={args.small} (profiling only)"
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and "score" in run:
         line["cpu_baseline"] = cpu_baseline(c2, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -439,11 +454,15 @@ def run_reference(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--stages", default="score,decode,prefill",
+                    help="comma list of stages to run (profiling captures)")
+    ap.add_argument("--small", action="store_true",
+                    help="smaller decode/prefill workloads (profiling captures only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_info()

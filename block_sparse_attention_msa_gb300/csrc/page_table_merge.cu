@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lens[f] = len;
 }
 
+// One warp per (unit u, head e). Lane s < S loads partial s's LSE (and skip id) and turns it
+// into a weight; the partial rows are then streamed with independent 16-byte loads (bf16: a
+// half-warp covers one 256-byte row, two partials per step; fp32: one 512-byte row per step).
 template <bool BF16>
 __global__ void __launch_bounds__(256)
     lse_merge_kernel(const void* __restrict__ o_parts, const float* __restrict__ lse_parts,
@@ -70,48 +73,83 @@ __global__ void __launch_bounds__(256)
   if (item >= U * G) return;
   const int64_t u = item / G;
   const int e = (int)(item % G);
-  // pass 1: max of the partial LSEs (lanes stride over the S partials)
-  float m = -INFINITY;
-  // skip_ids (optional, [U, S]): a partial whose id is negative was never written
-  for (int s = lane; s < S; s += 32)
-    if (!skip_ids || skip_ids[u * S + s] >= 0) m = fmaxf(m, lse_parts[(u * S + s) * G + e]);
-  m = warp_max(m);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float total = 0.f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      if (skip_ids && skip_ids[u * S + s] < 0) continue;
-      const float ls = lse_parts[(u * S + s) * G + e];
-      if (ls == -INFINITY) continue;
-      const float w = __expf(ls - m);
-      total += w;
-      const int64_t row = ((u * S + s) * G + e) * (int64_t)D;
-      for (int d = lane * 4; d < D; d += 128) {
+  // lane owns partials `lane` and `lane + 32` (S <= 64); absent or skipped ones weigh 0
+  float my_l[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    my_l[h] = -INFINITY;
+    if (s < S && (!skip_ids || skip_ids[u * S + s] >= 0)) my_l[h] = lse_parts[(u * S + s) * G + e];
+  }
+  const float m = warp_max(fmaxf(my_l[0], my_l[1]));
+  float wts[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    wts[h] = (m == -INFINITY || my_l[h] == -INFINITY) ? 0.f : __expf(my_l[h] - m);
+  const float my_w = wts[0];
+  const float total = warp_sum(wts[0] + wts[1]);
+  const float inv = total > 0.f ? 1.0f / total : 0.f;
+  const int64_t orow = (u * G + e) * (int64_t)D;
+  if (BF16 && D == 128 && S <= 32) {
+    const int half = lane >> 4, c = lane & 15;  // channels c*8 .. c*8+7
+    const uint16_t* base = reinterpret_cast<const uint16_t*>(o_parts);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int s0 = 0; s0 < S; s0 += 2) {
+      const int s = s0 + half;
+      const float w = __shfl_sync(0xffffffffu, my_w, s < 32 ? s : 0);
+      if (s < S && w != 0.f) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(base + ((u * S + s) * G + e) * 128) + c);
+        acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+        acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+        acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+        acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+        acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
+        acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
+        acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
+        acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
+    if (half == 0) {
+      uint4 out;
+      out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(o + orow + c * 8) = out;
+    }
+  } else {
+    // generic path: lanes own 4 consecutive channels, partials in sequence
+    for (int d0 = 0; d0 < D; d0 += 128) {
+      const int d = d0 + lane * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < S; ++s) {
+        const float w = __shfl_sync(0xffffffffu, s < 32 ? wts[0] : wts[1], s & 31);
+        if (w == 0.f || d >= D) continue;
+        const int64_t row = ((u * S + s) * G + e) * (int64_t)D;
         if (BF16) {
-          const uint2 v = *reinterpret_cast<const uint2*>(
-              reinterpret_cast<const uint16_t*>(o_parts) + row + d);
+          const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(o_parts) + row + d);
           acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
           acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
           acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
           acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
         } else {
-          const float4 v =
-              *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o_parts) + row + d);
+          const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o_parts) + row + d);
           acc[0] = fmaf(w, v.x, acc[0]);
           acc[1] = fmaf(w, v.y, acc[1]);
           acc[2] = fmaf(w, v.z, acc[2]);
           acc[3] = fmaf(w, v.w, acc[3]);
         }
       }
+      if (d < D) {
+        uint2 out;
+        out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(o + orow + d) = out;
+      }
     }
-  }
-  const float inv = total > 0.f ? 1.0f / total : 0.f;
-  const int64_t orow = (u * G + e) * (int64_t)D;
-  for (int d = lane * 4; d < D; d += 128) {
-    uint2 out;
-    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(o + orow + d) = out;
   }
   if (lse && lane == 0) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
 }

@@ -164,7 +164,7 @@ __host__ __device__ inline DecodeSmemLayout decode_layout(int N, int Hkv, int Di
   L.q_off = off;
   off += (uint32_t)(N * Hkv * (Di + 4) * 4);
   L.red_off = off;
-  off += (uint32_t)(kConsumerWarps * N * Hkv * 4);
+  off += (uint32_t)(2 * kConsumerWarps * N * Hkv * 4);  // double-buffered by page parity
   off = (off + 15u) & ~15u;
   L.topk_off = off;
   off += (uint32_t)(kConsumerWarps * sizeof(TopkScratch));
@@ -193,7 +193,7 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
-template <int DI>
+template <int DI, int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
     score_decode_kernel(const __grid_constant__ CUtensorMap kmap, const DecodeKParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -312,14 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   int b = misc[2], j = misc[3];
   bool bad = false;
   int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
-  int cur_b = -1, done_pages = 0;
-  int qpos[kDecodeMaxN];
+  int cur_b = -1, done_pages = 0, page_par = 0;
+  int qpos[NQ];
   uint32_t it = 0;
   const int g = tid % Hkv;
   const bool has_row = tid < rows;
 
   auto finish_request = [&](int rb, int count) {
-    // every writer fenced its scores; publish this CTA's share of the request
+    // make this CTA's block scores of request rb visible device-wide, then publish its share
+    if (tid < N * Hkv) __threadfence();
     consumer_sync();
     if (tid == 0) {
       bool bad_r = false;
@@ -355,13 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq[row * (DI + 4) + d] = __uint_as_float((uint32_t)qsrc[e] << 16);
       }
 #pragma unroll
-      for (int i = 0; i < kDecodeMaxN; ++i)
+      for (int i = 0; i < NQ; ++i)
         qpos[i] = clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) - N + i;
       consumer_sync();
     }
-    float rm[kDecodeMaxN];
+    float rm[NQ];
 #pragma unroll
-    for (int i = 0; i < kDecodeMaxN; ++i) rm[i] = -INFINITY;
+    for (int i = 0; i < NQ; ++i) rm[i] = -INFINITY;
 
     for (int sp = 0; sp < stages_per_page; ++sp, ++it) {
       const uint32_t slot = it % nstage;
@@ -376,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* st = smem + slot * L.stage_bytes;
         const int tok = sp * tok_per_stage + tid / Hkv;
         const int pos = j * 128 + tok;
-        float acc[kDecodeMaxN];
+        float acc[NQ];
 #pragma unroll
-        for (int i = 0; i < kDecodeMaxN; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < NQ; ++i) acc[i] = 0.0f;
 #pragma unroll
         for (int h = 0; h < DI / 64; ++h) {
 #pragma unroll
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
                            bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
-            for (int i = 0; i < kDecodeMaxN; ++i) {
+            for (int i = 0; i < NQ; ++i) {
               if (i < N) {
                 const float* qr = sq + (i * Hkv + g) * (DI + 4) + h * 64 + c * 8;
                 const float4 qa = *reinterpret_cast<const float4*>(qr);
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < kDecodeMaxN; ++i)
+        for (int i = 0; i < NQ; ++i)
           if (i < N && pos <= qpos[i]) rm[i] = fmaxf(rm[i], acc[i]);
       }
       __syncwarp();
@@ -413,25 +414,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- page end: max over the page's tokens for each (query row, group)
 #pragma unroll
-    for (int i = 0; i < kDecodeMaxN; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       if (i < N) {
         float v = rm[i];
         for (int off = 16; off >= Hkv; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane < Hkv) sred[(warp * N + i) * Hkv + lane] = v;
+        if (lane < Hkv) sred[((page_par * kConsumerWarps + warp) * N + i) * Hkv + lane] = v;
       }
     }
     consumer_sync();
+    if (misc[5]) return;  // uniform: read by every consumer after the same barrier
     if (tid < N * Hkv) {
       float v = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v = fmaxf(v, sred[w * N * Hkv + tid]);
+      for (int w = 0; w < kConsumerWarps; ++w)
+        v = fmaxf(v, sred[(page_par * kConsumerWarps + w) * N * Hkv + tid]);
       const int i = tid / Hkv, gg = tid % Hkv;
       const int64_t r = (int64_t)b * N + i;
       p.scores[(r * Hkv + gg) * p.max_blocks + j] = v;
-      __threadfence();
     }
-    consumer_sync();
-    if (misc[5]) return;  // uniform: read by every consumer after the same barrier
+    page_par ^= 1;  // the other half of sred is free: its readers passed this page's barrier
     ++done_pages;
     if (++j == nb) {
       j = 0;
@@ -579,18 +580,21 @@ cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
   p.scores = a.scores;
   p.tickets = a.tickets;
   const int grid = sm_count();
+  auto launch = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, stream>>>(map, p);
+    return cudaSuccess;
+  };
+  const int nq = a.N <= 1 ? 1 : a.N <= 2 ? 2 : a.N <= 4 ? 4 : 8;
   cudaError_t e;
-  if (a.Di == 128) {
-    e = cudaFuncSetAttribute(score_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    score_decode_kernel<128><<<grid, kThreads, smem, stream>>>(map, p);
-  } else {
-    e = cudaFuncSetAttribute(score_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    score_decode_kernel<64><<<grid, kThreads, smem, stream>>>(map, p);
-  }
+  if (a.Di == 128)
+    e = nq == 1 ? launch(score_decode_kernel<128, 1>) : nq == 2 ? launch(score_decode_kernel<128, 2>)
+        : nq == 4 ? launch(score_decode_kernel<128, 4>) : launch(score_decode_kernel<128, 8>);
+  else
+    e = nq == 1 ? launch(score_decode_kernel<64, 1>) : nq == 2 ? launch(score_decode_kernel<64, 2>)
+        : nq == 4 ? launch(score_decode_kernel<64, 4>) : launch(score_decode_kernel<64, 8>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
