@@ -63,7 +63,7 @@ cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* 
 // Workspace carve-up shared by the C ABI (size query) and the launcher. Offsets in bytes,
 // each 256-byte aligned.
 struct PrefillWorkspace {
-  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, total;
+  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc, total;
 };
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, int32_t nblk,
@@ -79,6 +79,8 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
     w.entries = off;    off = ws_align(off + 4 * sel);
     w.part_o = off;     off = ws_align(off + 2 * sel * G * 128);
     w.part_lse = off;   off = ws_align(off + 4 * sel * G);
+    // one 16-byte descriptor per work tile of 128/G queries: at most sel/(128/G) + lists
+    w.tile_desc = off;  off = ws_align(off + 16 * (sel * G / 128 + (size_t)Hkv * nblk + 1));
   }
   w.total = off;
   return w;

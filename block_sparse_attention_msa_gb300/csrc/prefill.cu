@@ -134,23 +134,59 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int
   }
 }
 
+// Compact descriptor of every work tile: (list gj = g*nblk + j, first entry, valid queries).
+// One warp per list; lanes over the list's tiles.
+__global__ void __launch_bounds__(256)
+    tile_desc_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ group_base,
+                     const int32_t* __restrict__ tile_offsets, int32_t Hkv, int32_t nblk,
+                     int32_t qpt, int4* __restrict__ desc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gj = blockIdx.x * 8 + warp;
+  if (gj >= Hkv * nblk) return;
+  const int g = gj / nblk, j = gj % nblk;
+  const int32_t* off = offsets + (int64_t)g * (nblk + 1) + j;
+  const int lbeg = off[0], lcnt = off[1] - off[0];
+  const int first = group_base[g] + lbeg;
+  const int t0 = tile_offsets[gj], nt = tile_offsets[gj + 1] - t0;
+  for (int c = lane; c < nt; c += 32)
+    desc[t0 + c] = make_int4(gj, first + c * qpt, min(qpt, lcnt - c * qpt), 0);
+}
+
 // ------------------------------------------------------------------------------ attention
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 128;                       // query-head rows per tile
+// One CTA per SM (tcgen05 path). Warp 0 produces (TMA), warp 1 owns tensor memory and issues
+// the MMAs, two softmax warpgroups (warps 4-7: even tiles, warps 8-11: odd tiles; one row per
+// thread) run softmax and the epilogue.
+constexpr int kThreads = 384;
+constexpr int kRows = 128;                       // query-head rows per tile (MMA M)
 constexpr uint32_t kBox = 128 * 64 * 2;          // 128 rows x 64 channels bf16 = 16 KB
-constexpr uint32_t kQBytes = 2 * kBox;           // one Q tile (two channel halves)
-constexpr uint32_t kKVBytes = 4 * kBox;          // K lo/hi + V lo/hi
+constexpr uint32_t kTileBytes = 2 * kBox;        // Q tile, P tile, K block or V block: 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/384
+
+// shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
+// query tiles hides the latency of the scattered row gathers; P, S and O are double buffered
+constexpr int kQStages = 2;
+constexpr uint32_t kOffQ = 0;                                  // Q[kQStages]
+constexpr uint32_t kOffP = kQStages * kTileBytes;              // P[2]
+constexpr uint32_t kOffK = (kQStages + 2) * kTileBytes;        // K block
+constexpr uint32_t kOffV = (kQStages + 3) * kTileBytes;        // V block
+constexpr uint32_t kOffBar = (kQStages + 4) * kTileBytes;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+
+struct Bars {
+  uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2];
+  uint64_t kv_full, kv_empty;
+  uint32_t tmem_base;
+  int32_t fail;
+};
 
 struct PreKParams {
-  const uint16_t* q;
-  int32_t T, Hq, Hkv, G, topk, nblk, qpt;
-  int64_t S_kv;
-  const int32_t* offsets;
-  const int32_t* group_base;
   const int32_t* entries;
+  const int4* desc;                // per-tile (gj, first entry, valid queries)
   const int32_t* tile_offsets;
+  int32_t Hkv, G, topk, nblk, qpt;
+  int64_t q_start;
   uint16_t* part_o;
   float* part_lse;
 };
@@ -161,242 +197,300 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// Cursor over the global tile list: tile `tile` belongs to list gj = g*nblk + j, chunk c.
-struct TileCursor {
-  int64_t tile;
-  int gj;
-  int c;
-};
-
-__device__ __forceinline__ void cursor_seek(const int32_t* tile_offsets, int n_gj, int64_t tile,
-                                            TileCursor& cur) {
-  int lo = 0, hi = n_gj - 1;  // largest gj with tile_offsets[gj] <= tile and a nonempty list
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tile_offsets[mid] <= tile) lo = mid; else hi = mid - 1;
-  }
-  while (lo + 1 < n_gj && tile_offsets[lo + 1] <= tile) ++lo;  // skip empty lists
-  cur.tile = tile;
-  cur.gj = lo;
-  cur.c = (int)(tile - tile_offsets[lo]);
+// Tile descriptor: list gj = g*nblk + j, first entry of the tile, valid query slots.
+__device__ __forceinline__ int4 load_desc(const PreKParams& p, int64_t tile) {
+  return __ldg(p.desc + tile);
 }
 
-__device__ __forceinline__ void cursor_next(const int32_t* tile_offsets, int n_gj, TileCursor& cur) {
-  ++cur.tile;
-  ++cur.c;
-  while (cur.gj < n_gj && tile_offsets[cur.gj + 1] <= cur.tile) {
-    ++cur.gj;
-    cur.c = 0;
-  }
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int32_t* fail) {
+  if (*fail) return false;
+  if (mbar_wait(bar, parity)) return true;
+  msa_record_error(kErrTimeout);
+  *fail = 1;
+  return false;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_partials_kernel(const __grid_constant__ CUtensorMap kmap,
+    prefill_block_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                            const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const PreKParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* kv = smem;                         // K lo, K hi, V lo, V hi
-  uint8_t* qbuf = smem + kKVBytes;            // two Q tiles
-  uint64_t* kv_bar = reinterpret_cast<uint64_t*>(qbuf + 2 * kQBytes);
-  int32_t* s_ent = reinterpret_cast<int32_t*>(kv_bar + 1);  // [2][128] entry per query slot
-
+  Bars& B = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int32_t* fail = &B.fail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
   const int n_gj = p.Hkv * p.nblk;
   const int64_t total = p.tile_offsets[n_gj];
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   const int64_t t0 = (int64_t)blockIdx.x * per;
   const int64_t t1 = t0 + per < total ? t0 + per : total;
-  if (t0 >= t1) return;
+  if (t0 >= t1) return;  // uniform for the CTA
+  const int n = (int)(t1 - t0);
+
   if (tid == 0) {
-    mbar_init(kv_bar, 1);
+    for (int q = 0; q < kQStages; ++q) {
+      mbar_init(&B.q_full[q], 1);
+      mbar_init(&B.q_empty[q], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B.s_full[b], 1);
+      mbar_init(&B.s_free[b], 4);
+      mbar_init(&B.p_full[b], 4);
+      mbar_init(&B.o_full[b], 1);
+      mbar_init(&B.o_free[b], 4);
+    }
+    mbar_init(&B.kv_full, 1);
+    mbar_init(&B.kv_empty, 1);
+    B.fail = 0;
     mbar_fence_init();
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
   }
+  if (warp == 1) {  // the whole warp allocates the tensor memory, then gives up the permit
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&B.tmem_base)), "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
   __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  const uint32_t sbase = smem_u32(smem);
 
-  const int G = p.G, qpt = p.qpt;
-  const int64_t q_start = p.S_kv - p.T;
-  // gather of one Q tile: thread -> (row = tid/2, channel half = tid%2), 8 x 16 bytes
-  auto issue_q = [&](const TileCursor& cur, int buf) {
-    const int g = cur.gj / p.nblk;
-    const int gbase = p.group_base[g];
-    const int32_t* off = p.offsets + (int64_t)g * (p.nblk + 1) + (cur.gj % p.nblk);
-    const int lbeg = off[0], lcnt = off[1] - off[0];
-    const int r = tid >> 1, half = tid & 1;
-    const int qi = r / G, h = r % G;
-    const int li = cur.c * qpt + qi;
-    int32_t ent = -1;
-    if (qi < qpt && li < lcnt) ent = p.entries[gbase + lbeg + li];
-    if (h == 0 && half == 0 && qi < qpt) s_ent[buf * 128 + qi] = ent;
-    uint8_t* dstb = qbuf + buf * kQBytes + half * kBox;
-    if (ent >= 0) {
-      const int64_t t = ent / p.topk;
-      const uint16_t* src = p.q + ((t * p.Hq + (int64_t)g * G + h) * 128 + half * 64);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) cp_async16(smem_u32(dstb + sw128(r, c)), src + c * 8);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dstb + sw128(r, c)) = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    // ================================================================ producer (whole warp)
+    // Each lane gathers the query rows of up to kMaxQPerLane query slots of the tile (lane,
+    // lane+32, ...). Descriptors are prefetched two tiles ahead and entries one tile ahead so
+    // that no global-memory latency sits between two tiles' copies.
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
     }
-    cp_async_commit();
-  };
-
-  TileCursor cur;
-  cursor_seek(p.tile_offsets, n_gj, t0, cur);
-  int loaded_gj = -1;
-  uint32_t kv_phase = 0;
-  int buf = 0;
-  issue_q(cur, 0);
-  const int gid = lane >> 2, tig = lane & 3;
-
-  for (int64_t tile = t0; tile < t1; ++tile) {
-    const int g = cur.gj / p.nblk, j = cur.gj % p.nblk;
-    // K/V block of this tile (shared by the CTA's consecutive tiles of the same list)
-    if (cur.gj != loaded_gj) {
-      if (tid == 0) {
-        // the previous block was read through the generic proxy; order those reads before
-        // the asynchronous-proxy (TMA) writes that replace it
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(kv_bar, kKVBytes);
-        tma_load_3d(kv, &kmap, kv_bar, 0, g, j * 128);
-        tma_load_3d(kv + kBox, &kmap, kv_bar, 64, g, j * 128);
-        tma_load_3d(kv + 2 * kBox, &vmap, kv_bar, 0, g, j * 128);
-        tma_load_3d(kv + 3 * kBox, &vmap, kv_bar, 64, g, j * 128);
-      }
-      if (!mbar_wait(kv_bar, kv_phase)) {
-        msa_record_error(kErrTimeout);
-        cp_async_wait_all();
-        return;  // every thread times out on the same phase
-      }
-      kv_phase ^= 1;
-      loaded_gj = cur.gj;
+    constexpr int kMaxQPerLane = 4;  // qpt = 128/G <= 128
+    int4 d0 = load_desc(p, t0);
+    int4 d1 = n > 1 ? load_desc(p, t0 + 1) : d0;
+    int32_t e0[kMaxQPerLane];
+#pragma unroll
+    for (int r = 0; r < kMaxQPerLane; ++r) {
+      const int q = lane + 32 * r;
+      e0[r] = q < d0.z ? p.entries[d0.y + q] : -1;
     }
-    // prefetch the next tile's queries into the other buffer
-    TileCursor nxt = cur;
-    cursor_next(p.tile_offsets, n_gj, nxt);
-    cp_async_wait_all();
-    __syncthreads();  // Q tile `buf` and s_ent[buf] visible to all
-    if (tile + 1 < t1) issue_q(nxt, buf ^ 1);
-
-    // ---------------- compute: warp owns rows 16*warp .. +15 of the tile
-    const uint32_t qb = smem_u32(qbuf + buf * kQBytes);
-    const uint32_t kb = smem_u32(kv), vb = kb + 2 * kBox;
-    float sc[16][4];
+    int loaded_gj = -1, kv_loads = 0;
+    for (int i = 0; i < n; ++i) {
+      const int qs = i % kQStages;
+      const int4 d = d0;
+      int32_t e[kMaxQPerLane];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-    {
-      const int mi = lane >> 3;
-      const uint32_t arow = warp * 16 + (mi & 1) * 8 + (lane & 7);
-      const uint32_t brow = (mi >> 1) * 8 + (lane & 7);
+      for (int r = 0; r < kMaxQPerLane; ++r) e[r] = e0[r];
+      if (i + 1 < n) {  // prefetch: entries of tile i+1, descriptor of tile i+2
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        const uint32_t adc = 2 * ks + (mi >> 1);
-        ldmatrix_x4(qb + (adc >> 3) * kBox + sw128(arow, adc & 7), a[0], a[1], a[2], a[3]);
-        const uint32_t bdc = 2 * ks + (mi & 1);
+        for (int r = 0; r < kMaxQPerLane; ++r) {
+          const int q = lane + 32 * r;
+          e0[r] = q < d1.z ? p.entries[d1.y + q] : -1;
+        }
+        d0 = d1;
+        if (i + 2 < n) d1 = load_desc(p, t0 + i + 2);
+      }
+      if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
+      const int g = d.x / p.nblk, j = d.x % p.nblk;
+      uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
+      if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
+      __syncwarp();
 #pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kb + (bdc >> 3) * kBox + sw128(np * 16 + brow, bdc & 7), b0, b1, b2, b3);
-          mma_bf16_16816(sc[2 * np], a, b0, b1);
-          mma_bf16_16816(sc[2 * np + 1], a, b2, b3);
+      for (int r = 0; r < kMaxQPerLane; ++r) {
+        const int q = lane + 32 * r;
+        if (q < d.z) {
+          const int t = e[r] / p.topk;
+          tma_load_3d(qdst + q * p.G * 128, &qmap, &B.q_full[qs], 0, g * p.G, t);
+          tma_load_3d(qdst + kBox + q * p.G * 128, &qmap, &B.q_full[qs], 64, g * p.G, t);
         }
       }
-    }
-    // causal mask: row -> query slot -> position
-    int64_t qpos[2];
-    int32_t ent[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = warp * 16 + gid + 8 * r;
-      ent[r] = (row / G < qpt) ? s_ent[buf * 128 + row / G] : -1;
-      qpos[r] = ent[r] >= 0 ? q_start + ent[r] / p.topk : -1;
-    }
-    const int64_t kpos0 = (int64_t)j * 128;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int r = c >> 1;
-        const int64_t kp = kpos0 + nt * 8 + tig * 2 + (c & 1);
-        if (kp > qpos[r]) sc[nt][c] = -INFINITY;
-        mx[r] = fmaxf(mx[r], sc[nt][c]);
-      }
-    float lsum[2] = {0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    const float mref[2] = {mx[0] == -INFINITY ? 0.f : mx[0], mx[1] == -INFINITY ? 0.f : mx[1]};
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int r = c >> 1;
-        sc[nt][c] = ex2((sc[nt][c] - mref[r]) * kLog2e);
-        lsum[r] += sc[nt][c];
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lsum[r] += __shfl_xor_sync(0xffffffffu, lsum[r], 1);
-      lsum[r] += __shfl_xor_sync(0xffffffffu, lsum[r], 2);
-    }
-    // O = P V
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    {
-      const int mi = lane >> 3;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-        pa[1] = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
-        pa[2] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        pa[3] = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-        const uint32_t tok = kk * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int nd = 0; nd < 16; nd += 2) {
-          const uint32_t dc = nd + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vb + (dc >> 3) * kBox + sw128(tok, dc & 7), b0, b1, b2, b3);
-          mma_bf16_16816(o[nd], pa, b0, b1);
-          mma_bf16_16816(o[nd + 1], pa, b2, b3);
+      if (d.x != loaded_gj) {
+        if (loaded_gj != -1 && !wait_or_fail(&B.kv_empty, (kv_loads - 1) & 1, fail)) break;
+        if (lane == 0) {
+          mbar_expect_tx(&B.kv_full, 4 * kBox);
+          const int tok = j * 128;
+          tma_load_3d(smem + kOffK, &kmap, &B.kv_full, 0, g, tok);
+          tma_load_3d(smem + kOffK + kBox, &kmap, &B.kv_full, 64, g, tok);
+          tma_load_3d(smem + kOffV, &vmap, &B.kv_full, 0, g, tok);
+          tma_load_3d(smem + kOffV + kBox, &vmap, &B.kv_full, 64, g, tok);
         }
+        ++kv_loads;
+        loaded_gj = d.x;
       }
     }
-    // epilogue: normalised bf16 partial + fp32 LSE per (entry, head)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (ent[r] < 0) continue;
-      const int row = warp * 16 + gid + 8 * r;
-      const int h = row % G;
-      const int64_t t = ent[r] / p.topk;
-      const int slot = ent[r] % p.topk;
-      const int64_t pidx = ((t * p.Hkv + g) * p.topk + slot) * G + h;
-      const float inv = lsum[r] > 0.f ? 1.0f / lsum[r] : 0.f;
-      uint16_t* dst = p.part_o + pidx * 128;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd)
-        *reinterpret_cast<uint32_t*>(dst + nd * 8 + tig * 2) =
-            pack_bf16x2(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
-      if (tig == 0) p.part_lse[pidx] = lsum[r] > 0.f ? mx[r] + __logf(lsum[r]) : -INFINITY;
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
+      const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
+      auto issue_o = [&](int k, bool release_kv) -> bool {
+        const int b = k & 1;
+        if (!wait_or_fail(&B.p_full[b], (k >> 1) & 1, fail)) return false;
+        if (k >= 2 && !wait_or_fail(&B.o_free[b], ((k - 2) >> 1) & 1, fail)) return false;
+        tmem_fence_after();
+        const uint32_t pa = sbase + kOffP + b * kTileBytes;
+        const uint32_t va = sbase + kOffV;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
+          umma_bf16(tmem + 256 + b * 128, ad, bd, idesc_o, kk > 0);
+        }
+        umma_commit(&B.o_full[b]);
+        if (release_kv) umma_commit(&B.kv_empty);
+        return true;
+      };
+      int kv_gj = -1, kv_loads = 0, pending = -1;
+      bool ok = true;
+      int next_gj = load_desc(p, t0).x;
+      for (int i = 0; i < n && ok; ++i) {
+        const int b = i & 1;
+        const int gj = next_gj;
+        if (i + 1 < n) next_gj = load_desc(p, t0 + i + 1).x;
+        if (gj != kv_gj) {
+          if (pending >= 0) {
+            ok = issue_o(pending, true);
+            pending = -1;
+            if (!ok) break;
+          }
+          if (!wait_or_fail(&B.kv_full, kv_loads & 1, fail)) break;
+          ++kv_loads;
+          kv_gj = gj;
+        }
+        const int qs = i % kQStages;
+        if (!wait_or_fail(&B.q_full[qs], (i / kQStages) & 1, fail)) break;
+        if (i >= 2 && !wait_or_fail(&B.s_free[b], ((i - 2) >> 1) & 1, fail)) break;
+        tmem_fence_after();
+        const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
+        const uint32_t ka = sbase + kOffK;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          umma_bf16(tmem + b * 128, umma_desc_sw128(qa + off, 16, 1024),
+                    umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+        }
+        umma_commit(&B.s_full[b]);
+        umma_commit(&B.q_empty[qs]);
+        if (pending >= 0) ok = issue_o(pending, false);
+        pending = i;
+      }
+      if (ok && pending >= 0) issue_o(pending, true);
     }
-    __syncthreads();  // everyone done with Q tile `buf` (and K/V) before they are reused
-    buf ^= 1;
-    cur = nxt;
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================================================================ softmax + epilogue
+    // Warpgroup wg handles tiles k = wg, wg+2, ... with S[wg], P[wg], O[wg].
+    const int wg = (warp - 4) >> 2;
+    const int row = (tid - 128) & 127;         // tile row = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+    const int G = p.G;
+    const int qi = row / G, h = row % G;
+    // software prefetch: descriptors two of this warpgroup's tiles ahead, entry one ahead
+    int4 d_next = wg < n ? load_desc(p, t0 + wg) : make_int4(0, 0, 0, 0);
+    int4 d_next2 = wg + 2 < n ? load_desc(p, t0 + wg + 2) : d_next;
+    int32_t e_next = qi < d_next.z ? p.entries[d_next.y + qi] : -1;
+    const uint32_t s_tmem = tmem + lane_addr + wg * 128;
+    const uint32_t o_tmem = tmem + lane_addr + 256 + wg * 128;
+    uint8_t* prow = smem + kOffP + wg * kTileBytes;
+    for (int k = wg; k < n; k += 2) {
+      const int use = k >> 1;  // this warpgroup's use count of its buffers
+      const int4 d = d_next;
+      const int32_t ent = e_next;
+      if (k + 2 < n) {
+        e_next = qi < d_next2.z ? p.entries[d_next2.y + qi] : -1;
+        d_next = d_next2;
+        if (k + 4 < n) d_next2 = load_desc(p, t0 + k + 4);
+      }
+      const int j = d.x % p.nblk;
+      // ---------------- softmax of tile k
+      if (!wait_or_fail(&B.s_full[wg], use & 1, fail)) break;
+      tmem_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, s + c * 32);
+      tmem_wait_ld();
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.s_free[wg]);
+      // causal mask: key j*128 + col is visible to the query iff it is <= the query position
+      const int64_t qpos = ent >= 0 ? p.q_start + ent / p.topk : -1;
+      const int64_t lim = qpos - (int64_t)j * 128;  // last visible column
+      if (lim < 127) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) mx8[r] = s[r];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mref = mx == -INFINITY ? 0.f : mx;
+      const float mscaled = mref * kLog2e;
+      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        s[c] = ex2(fmaf(s[c], kLog2e, -mscaled));
+        l8[c & 7] += s[c];
+      }
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      // P row (bf16) into the swizzled K-major A-operand tile
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int k0 = kh * 64 + c * 8;
+          uint4 v;
+          v.x = pack_bf16x2(s[k0 + 0], s[k0 + 1]);
+          v.y = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
+          v.z = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
+          v.w = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
+          *reinterpret_cast<uint4*>(prow + kh * kBox + sw128(row, c)) = v;
+        }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.p_full[wg]);
+      // ---------------- epilogue of tile k: normalised bf16 partial + fp32 LSE
+      if (!wait_or_fail(&B.o_full[wg], use & 1, fail)) break;
+      tmem_fence_after();
+      float o[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(o_tmem + c * 32, o + c * 32);
+      tmem_wait_ld();
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.o_free[wg]);
+      if (ent >= 0) {
+        const int64_t t = ent / p.topk;
+        const int slot = ent % p.topk;
+        const int64_t pidx = ((t * p.Hkv + d.x / p.nblk) * p.topk + slot) * G + h;
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.part_o + pidx * 128);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          uint4 v;
+          v.x = pack_bf16x2(o[c * 8 + 0] * inv, o[c * 8 + 1] * inv);
+          v.y = pack_bf16x2(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv);
+          v.z = pack_bf16x2(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv);
+          v.w = pack_bf16x2(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv);
+          dst[c] = v;
+        }
+        p.part_lse[pidx] = l > 0.f ? mx + __logf(l) : -INFINITY;
+      }
+    }
   }
-  cp_async_wait_all();
+  // ------------------------------------------------------------------ teardown
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
+                 : "memory");
+  }
 }
 
 }  // namespace
@@ -428,38 +522,42 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   int32_t* entries = reinterpret_cast<int32_t*>(a.workspace + W.entries);
   uint16_t* part_o = reinterpret_cast<uint16_t*>(a.workspace + W.part_o);
   float* part_lse = reinterpret_cast<float*>(a.workspace + W.part_lse);
+  int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
   cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, qpt, offsets, entries,
                                 counts, group_base, tile_offsets, stream);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap kmap, vmap;
+  CUtensorMap qmap, kmap, vmap;
+  const uint64_t qdims[3] = {(uint64_t)a.D, (uint64_t)a.Hq, (uint64_t)a.T};
+  const uint64_t qstrides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hq * a.D * 2};
+  const uint32_t qbox[3] = {64, (uint32_t)G, 1};
   const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.Hkv, (uint64_t)a.S_kv};
   const uint64_t strides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hkv * a.D * 2};
   const uint32_t box[3] = {64, 1, 128};
-  if (!encode_bf16_map(&kmap, a.k, 3, dims, strides, box, true) ||
+  if (!encode_bf16_map(&qmap, a.q, 3, qdims, qstrides, qbox, true) ||
+      !encode_bf16_map(&kmap, a.k, 3, dims, strides, box, true) ||
       !encode_bf16_map(&vmap, a.v, 3, dims, strides, box, true))
     return cudaErrorInvalidValue;
+  tile_desc_kernel<<<(unsigned)((a.Hkv * a.nblk + 7) / 8), 256, 0, stream>>>(
+      offsets, group_base, tile_offsets, a.Hkv, a.nblk, qpt, tile_desc);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   PreKParams p;
-  p.q = a.q;
-  p.T = a.T;
-  p.Hq = a.Hq;
+  p.entries = entries;
+  p.desc = tile_desc;
+  p.tile_offsets = tile_offsets;
   p.Hkv = a.Hkv;
   p.G = G;
   p.topk = a.topk;
   p.nblk = a.nblk;
   p.qpt = qpt;
-  p.S_kv = a.S_kv;
-  p.offsets = offsets;
-  p.group_base = group_base;
-  p.entries = entries;
-  p.tile_offsets = tile_offsets;
+  p.q_start = a.S_kv - a.T;
   p.part_o = part_o;
   p.part_lse = part_lse;
-  const size_t smem = 1024 + kKVBytes + 2 * kQBytes + 8 + 2 * 128 * 4;
-  e = cudaFuncSetAttribute(prefill_partials_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  e = cudaFuncSetAttribute(prefill_block_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  prefill_partials_kernel<<<sm_count(), kThreads, smem, stream>>>(kmap, vmap, p);
+  prefill_block_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_lse_merge(part_o, true, part_lse, a.block_ids, (int64_t)a.T * a.Hkv, a.topk, G,
