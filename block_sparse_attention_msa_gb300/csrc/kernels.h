@@ -59,6 +59,12 @@ cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* 
                              const int32_t* skip_ids, int64_t U, int32_t S, int32_t G, int32_t D,
                              uint16_t* o, float* lse, cudaStream_t stream);
 
+// Prefill merge of chunk-major partials part_o[16][U*S*G][8] bf16 (row = (u*S+s)*G+e); a
+// partial s of unit u is skipped when ids[u*S+s] < 0 (never written). G in {1,2,4,8,16}.
+cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
+                                     const int32_t* ids, int64_t U, int32_t S, int32_t G,
+                                     uint16_t* o, float* lse, cudaStream_t stream);
+
 // ------------------------------------------------------------------ prefill
 // Workspace carve-up shared by the C ABI (size query) and the launcher. Offsets in bytes,
 // each 256-byte aligned.

@@ -154,7 +154,90 @@ __global__ void __launch_bounds__(256)
   if (lse && lane == 0) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
 }
 
+// Prefill merge over chunk-major partials: part_o[c][row][8] bf16 with c = 16 channel chunks
+// and row = (u*S + s)*G + e; one warp per unit u (all G heads). Lane slot idx = lane + 32*r
+// covers head idx % G and chunk idx / G, so for a fixed r the lanes of one chunk plane read the
+// G adjacent rows of a partial: 16*G contiguous bytes.
+template <int G>
+__global__ void __launch_bounds__(256)
+    lse_merge_chunked_kernel(const uint4* __restrict__ part_o, int64_t part_rows,
+                             const float* __restrict__ lse_parts, const int32_t* __restrict__ ids,
+                             int64_t U, int32_t S, uint16_t* __restrict__ o, float* __restrict__ lse) {
+  constexpr int R = (G * 16 + 31) / 32;  // chunk slots per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = (int64_t)blockIdx.x * 8 + warp;
+  if (u >= U) return;
+  const int e = lane % G;
+  float m = -INFINITY;
+  for (int s = 0; s < S; ++s) {
+    if (ids[u * S + s] < 0) continue;
+    m = fmaxf(m, lse_parts[(u * S + s) * G + e]);
+  }
+  float acc[R][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[r][x] = 0.f;
+  float total = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      if (ids[u * S + s] < 0) continue;
+      const float ls = lse_parts[(u * S + s) * G + e];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - m);
+      total += w;
+      const int64_t row = (u * S + s) * G + e;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int idx = lane + 32 * r;
+        if (idx < G * 16) {
+          const uint4 v = __ldcs(part_o + (int64_t)(idx / G) * part_rows + row);
+          acc[r][0] = fmaf(w, bf16_lo(v.x), acc[r][0]);
+          acc[r][1] = fmaf(w, bf16_hi(v.x), acc[r][1]);
+          acc[r][2] = fmaf(w, bf16_lo(v.y), acc[r][2]);
+          acc[r][3] = fmaf(w, bf16_hi(v.y), acc[r][3]);
+          acc[r][4] = fmaf(w, bf16_lo(v.z), acc[r][4]);
+          acc[r][5] = fmaf(w, bf16_hi(v.z), acc[r][5]);
+          acc[r][6] = fmaf(w, bf16_lo(v.w), acc[r][6]);
+          acc[r][7] = fmaf(w, bf16_hi(v.w), acc[r][7]);
+        }
+      }
+    }
+  }
+  const float inv = total > 0.f ? 1.0f / total : 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int idx = lane + 32 * r;
+    if (idx < G * 16) {
+      uint4 out;
+      out.x = pack_bf16x2(acc[r][0] * inv, acc[r][1] * inv);
+      out.y = pack_bf16x2(acc[r][2] * inv, acc[r][3] * inv);
+      out.z = pack_bf16x2(acc[r][4] * inv, acc[r][5] * inv);
+      out.w = pack_bf16x2(acc[r][6] * inv, acc[r][7] * inv);
+      *reinterpret_cast<uint4*>(o + (u * G + e) * 128 + (idx / G) * 8) = out;
+    }
+  }
+  if (lse && lane < G) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
+                                     const int32_t* ids, int64_t U, int32_t S, int32_t G,
+                                     uint16_t* o, float* lse, cudaStream_t stream) {
+  const unsigned grid = (unsigned)((U + 7) / 8);
+  const int64_t rows = U * S * G;
+  const uint4* po = reinterpret_cast<const uint4*>(part_o);
+  switch (G) {
+    case 1: lse_merge_chunked_kernel<1><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    case 2: lse_merge_chunked_kernel<2><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    case 4: lse_merge_chunked_kernel<4><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    case 8: lse_merge_chunked_kernel<8><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    case 16: lse_merge_chunked_kernel<16><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_page_table(const int32_t* block_ids, const int32_t* page_table,
                                    const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,

@@ -165,7 +165,7 @@ constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/3
 
 // shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
 // query tiles hides the latency of the scattered row gathers; P, S and O are double buffered
-constexpr int kQStages = 2;
+constexpr int kQStages = 3;
 constexpr uint32_t kOffQ = 0;                                  // Q[kQStages]
 constexpr uint32_t kOffP = kQStages * kTileBytes;              // P[2]
 constexpr uint32_t kOffK = (kQStages + 2) * kTileBytes;        // K block
@@ -187,7 +187,8 @@ struct PreKParams {
   const int32_t* tile_offsets;
   int32_t Hkv, G, topk, nblk, qpt;
   int64_t q_start;
-  uint16_t* part_o;
+  uint16_t* part_o;               // chunk-major [16][part_rows][8] bf16
+  int64_t part_rows;               // T*Hkv*topk*G
   float* part_lse;
 };
 
@@ -324,59 +325,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
+    // Event loop: issue O(oi) as soon as its P is ready, S(si) as soon as its queries and
+    // S buffer are ready, O first. A tile on a new K/V block waits until every O of the
+    // previous block is issued (its release is committed with the last one).
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
       const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
-      auto issue_o = [&](int k, bool release_kv) -> bool {
-        const int b = k & 1;
-        if (!wait_or_fail(&B.p_full[b], (k >> 1) & 1, fail)) return false;
-        if (k >= 2 && !wait_or_fail(&B.o_free[b], ((k - 2) >> 1) & 1, fail)) return false;
-        tmem_fence_after();
-        const uint32_t pa = sbase + kOffP + b * kTileBytes;
-        const uint32_t va = sbase + kOffV;
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-          umma_bf16(tmem + 256 + b * 128, ad, bd, idesc_o, kk > 0);
-        }
-        umma_commit(&B.o_full[b]);
-        if (release_kv) umma_commit(&B.kv_empty);
-        return true;
-      };
-      int kv_gj = -1, kv_loads = 0, pending = -1;
-      bool ok = true;
+      int si = 0, oi = 0, kv_gj = -1, kv_loads = 0;
+      int gj_ring[2] = {-1, -1};  // K/V list of the tiles whose S is issued and O is not
       int next_gj = load_desc(p, t0).x;
-      for (int i = 0; i < n && ok; ++i) {
-        const int b = i & 1;
-        const int gj = next_gj;
-        if (i + 1 < n) next_gj = load_desc(p, t0 + i + 1).x;
-        if (gj != kv_gj) {
-          if (pending >= 0) {
-            ok = issue_o(pending, true);
-            pending = -1;
-            if (!ok) break;
+      uint32_t idle = 0;
+      while (oi < n && !*fail) {
+        bool progress = false;
+        // ---- O(oi)
+        if (oi < si) {
+          const int b = oi & 1;
+          if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
+              (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
+            tmem_fence_after();
+            const uint32_t pa = sbase + kOffP + b * kTileBytes;
+            const uint32_t va = sbase + kOffV;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
+              umma_bf16(tmem + 256 + b * 128, ad, bd, idesc_o, kk > 0);
+            }
+            umma_commit(&B.o_full[b]);
+            const int gj_o = gj_ring[b];
+            const int gj_after = oi + 1 < si ? gj_ring[(oi + 1) & 1] : (oi + 1 < n ? next_gj : -2);
+            if (gj_after != gj_o) umma_commit(&B.kv_empty);  // last tile on this K/V block
+            ++oi;
+            progress = true;
           }
-          if (!wait_or_fail(&B.kv_full, kv_loads & 1, fail)) break;
-          ++kv_loads;
-          kv_gj = gj;
         }
-        const int qs = i % kQStages;
-        if (!wait_or_fail(&B.q_full[qs], (i / kQStages) & 1, fail)) break;
-        if (i >= 2 && !wait_or_fail(&B.s_free[b], ((i - 2) >> 1) & 1, fail)) break;
-        tmem_fence_after();
-        const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
-        const uint32_t ka = sbase + kOffK;
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          umma_bf16(tmem + b * 128, umma_desc_sw128(qa + off, 16, 1024),
-                    umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+        // ---- S(si)
+        if (si < n && si <= oi + 1) {
+          const int b = si & 1, qs = si % kQStages;
+          const int gj = next_gj;
+          bool kv_ok = gj == kv_gj;
+          if (!kv_ok && oi == si) {  // previous block fully consumed: switch to the new one
+            if (!wait_or_fail(&B.kv_full, kv_loads & 1, fail)) break;
+            ++kv_loads;
+            kv_gj = gj;
+            kv_ok = true;
+          }
+          if (kv_ok && mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
+              (si < 2 || mbar_test(&B.s_free[b], ((si - 2) >> 1) & 1))) {
+            tmem_fence_after();
+            const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
+            const uint32_t ka = sbase + kOffK;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+              umma_bf16(tmem + b * 128, umma_desc_sw128(qa + off, 16, 1024),
+                        umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+            }
+            umma_commit(&B.s_full[b]);
+            umma_commit(&B.q_empty[qs]);
+            gj_ring[b] = gj;
+            ++si;
+            if (si < n) next_gj = load_desc(p, t0 + si).x;
+            progress = true;
+          }
         }
-        umma_commit(&B.s_full[b]);
-        umma_commit(&B.q_empty[qs]);
-        if (pending >= 0) ok = issue_o(pending, false);
-        pending = i;
+        if (progress) {
+          idle = 0;
+        } else {
+          // back off: this thread shares its scheduler with two softmax warps
+          __nanosleep(64);
+          if (++idle > kWaitLimit) {
+            msa_record_error(kErrTimeout);
+            *fail = 1;
+          }
+        }
       }
-      if (ok && pending >= 0) issue_o(pending, true);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -407,80 +428,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- softmax of tile k
       if (!wait_or_fail(&B.s_full[wg], use & 1, fail)) break;
       tmem_fence_after();
-      float s[128];
+      float v[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, s + c * 32);
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, v + c * 32);
       tmem_wait_ld();
       tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.s_free[wg]);
       // causal mask: key j*128 + col is visible to the query iff it is <= the query position
       const int64_t qpos = ent >= 0 ? p.q_start + ent / p.topk : -1;
-      const int64_t lim = qpos - (int64_t)j * 128;  // last visible column
-      if (lim < 127) {
+      const int64_t lim64 = qpos - (int64_t)j * 128;  // last visible column
+      if (lim64 < 127) {
+        const int lim = lim64 < -1 ? -1 : (int)lim64;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) s[c] = -INFINITY;
+        for (int x = 0; x < 128; ++x)
+          if (x > lim) v[x] = -INFINITY;
       }
       float mx8[8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) mx8[r] = s[r];
+      for (int r = 0; r < 8; ++r) mx8[r] = v[r];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      for (int x = 8; x < 128; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], v[x]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float mref = mx == -INFINITY ? 0.f : mx;
-      const float mscaled = mref * kLog2e;
+      const float mscaled = (mx == -INFINITY ? 0.f : mx) * kLog2e;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = ex2(fmaf(s[c], kLog2e, -mscaled));
-        l8[c & 7] += s[c];
+      for (int x = 0; x < 128; ++x) {
+        v[x] = ex2(fmaf(v[x], kLog2e, -mscaled));
+        l8[x & 7] += v[x];
       }
-      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       // P row (bf16) into the swizzled K-major A-operand tile
 #pragma unroll
       for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int k0 = kh * 64 + c * 8;
-          uint4 v;
-          v.x = pack_bf16x2(s[k0 + 0], s[k0 + 1]);
-          v.y = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
-          v.z = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
-          v.w = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
-          *reinterpret_cast<uint4*>(prow + kh * kBox + sw128(row, c)) = v;
+          uint4 u;
+          u.x = pack_bf16x2(v[k0 + 0], v[k0 + 1]);
+          u.y = pack_bf16x2(v[k0 + 2], v[k0 + 3]);
+          u.z = pack_bf16x2(v[k0 + 4], v[k0 + 5]);
+          u.w = pack_bf16x2(v[k0 + 6], v[k0 + 7]);
+          *reinterpret_cast<uint4*>(prow + kh * kBox + sw128(row, c)) = u;
         }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[wg]);
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       // ---------------- epilogue of tile k: normalised bf16 partial + fp32 LSE
+      // Partials are stored chunk-major, part_o[c][row][8] with row = ((t*Hkv+g)*k+slot)*G+h:
+      // the G rows of one query are adjacent, so a warp store covers 128-byte segments.
       if (!wait_or_fail(&B.o_full[wg], use & 1, fail)) break;
       tmem_fence_after();
-      float o[128];
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(o_tmem + c * 32, o + c * 32);
+      for (int c = 0; c < 4; ++c) tmem_ld32(o_tmem + c * 32, v + c * 32);
       tmem_wait_ld();
       tmem_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.o_free[wg]);
       if (ent >= 0) {
         const int64_t t = ent / p.topk;
-        const int slot = ent % p.topk;
-        const int64_t pidx = ((t * p.Hkv + d.x / p.nblk) * p.topk + slot) * G + h;
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.part_o + pidx * 128);
+        const int64_t prow_idx = ((t * p.Hkv + d.x / p.nblk) * p.topk + ent % p.topk) * G + h;
+        p.part_lse[prow_idx] = l > 0.f ? mx + __logf(l) : -INFINITY;
+        uint4* dst = reinterpret_cast<uint4*>(p.part_o) + prow_idx;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          uint4 v;
-          v.x = pack_bf16x2(o[c * 8 + 0] * inv, o[c * 8 + 1] * inv);
-          v.y = pack_bf16x2(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv);
-          v.z = pack_bf16x2(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv);
-          v.w = pack_bf16x2(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv);
-          dst[c] = v;
+          uint4 u;
+          u.x = pack_bf16x2(v[c * 8 + 0] * inv, v[c * 8 + 1] * inv);
+          u.y = pack_bf16x2(v[c * 8 + 2] * inv, v[c * 8 + 3] * inv);
+          u.z = pack_bf16x2(v[c * 8 + 4] * inv, v[c * 8 + 5] * inv);
+          u.w = pack_bf16x2(v[c * 8 + 6] * inv, v[c * 8 + 7] * inv);
+          dst[(int64_t)c * p.part_rows] = u;
         }
-        p.part_lse[pidx] = l > 0.f ? mx + __logf(l) : -INFINITY;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.o_free[wg]);
     }
   }
   // ------------------------------------------------------------------ teardown
@@ -553,6 +574,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.qpt = qpt;
   p.q_start = a.S_kv - a.T;
   p.part_o = part_o;
+  p.part_rows = (int64_t)a.T * a.Hkv * a.topk * G;
   p.part_lse = part_lse;
   e = cudaFuncSetAttribute(prefill_block_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes);
@@ -560,8 +582,8 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   prefill_block_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_lse_merge(part_o, true, part_lse, a.block_ids, (int64_t)a.T * a.Hkv, a.topk, G,
-                          a.D, a.o, a.lse, stream);
+  return launch_lse_merge_chunked(part_o, part_lse, a.block_ids, (int64_t)a.T * a.Hkv, a.topk, G,
+                                  a.o, a.lse, stream);
 }
 
 }  // namespace msa
