@@ -282,3 +282,58 @@ def cfg4(device, seed: int = 4, B: int | None = None):
 
 
 CFG5 = dict(B=4, seq_len=1 << 20, Hq=64, Hkv=8, D=128, Di=128, topk=32, T_prefill=32768)
+
+
+def paged_layer_workload(seq_lens, Hq: int, Hkv: int, D: int, Di: int, seed: int, device,
+                         shuffle: bool = True):
+    """Decode-time layer state for B requests sharing one page table: paged K-index, K and V
+    caches [P, 128, Hkv, *] bf16 ~N(0,1), and one query row per request (q pre-scaled, q_idx)."""
+    gen = _gen(seed, device)
+    B = len(seq_lens)
+    page_table, num_pages = paged_layout(seq_lens, gen, device, shuffle)
+    q = randn_bf16((B, Hq, D), gen, device, scale=1.0 / math.sqrt(D))
+    q_idx = randn_bf16((B, Hkv, Di), gen, device)
+    k_idx = randn_bf16((num_pages, BLOCK, Hkv, Di), gen, device)
+    k_cache = randn_bf16((num_pages, BLOCK, Hkv, D), gen, device)
+    v_cache = randn_bf16((num_pages, BLOCK, Hkv, D), gen, device)
+    return {"q": q, "q_idx": q_idx, "k_idx_pages": k_idx, "k_cache": k_cache, "v_cache": v_cache,
+            "page_table": page_table, "num_pages": num_pages,
+            "seq_lens": torch.tensor([int(s) for s in seq_lens], dtype=torch.int32, device=device),
+            "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Di": Di}
+
+
+def chunk_prefill_workload(prefix: int, T: int, Hq: int, Hkv: int, D: int, Di: int, seed: int,
+                           device):
+    """A T-token prefill chunk after a `prefix`-token context of one sequence: contiguous K, V and
+    K-index for all S = prefix + T tokens (the K-index is also the paged cache with the identity
+    page table), queries q / q_idx for the chunk only."""
+    gen = _gen(seed, device)
+    S = prefix + T
+    P = (S + BLOCK - 1) // BLOCK
+    cap = P * BLOCK
+    q = randn_bf16((T, Hq, D), gen, device, scale=1.0 / math.sqrt(D))
+    q_idx = randn_bf16((T, Hkv, Di), gen, device)
+    k = randn_bf16((cap, Hkv, D), gen, device)
+    v = randn_bf16((cap, Hkv, D), gen, device)
+    k_idx = randn_bf16((cap, Hkv, Di), gen, device)
+    return {"q": q, "q_idx": q_idx, "k": k, "v": v, "k_idx": k_idx, "S": S, "T": T, "P": P,
+            "Hq": Hq, "Hkv": Hkv, "D": D, "Di": Di,
+            "page_table": torch.arange(P, dtype=torch.int32, device=device)[None, :]}
+
+
+def cfg5_decode(device, seed: int = 5, B: int | None = None, seq_len: int | None = None):
+    """1M-token decode: 4 requests x 1,048,576 tokens, Hq 64, Hkv 8, D 128, Di 128, k 32."""
+    c = CFG5
+    w = paged_layer_workload([seq_len or c["seq_len"]] * (B or c["B"]), c["Hq"], c["Hkv"], c["D"],
+                             c["Di"], seed, device)
+    w["topk"] = c["topk"]
+    return w
+
+
+def cfg5_prefill(device, seed: int = 6, T: int | None = None, prefix: int | None = None):
+    """32768-token prefill chunk after a 1,048,576-token prefix, Hq 64, Hkv 8, D 128, Di 128, k 32."""
+    c = CFG5
+    w = chunk_prefill_workload(prefix if prefix is not None else c["seq_len"], T or c["T_prefill"],
+                               c["Hq"], c["Hkv"], c["D"], c["Di"], seed, device)
+    w["topk"] = c["topk"]
+    return w
