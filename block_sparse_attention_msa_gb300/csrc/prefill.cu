@@ -164,19 +164,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/384
 
 // shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
-// query tiles hides the latency of the scattered row gathers; P, S and O are double buffered
+// query tiles hides the latency of the scattered row gathers; two K/V block buffers let the
+// next block load while the previous one is still in use. S and O live in tensor memory
+// (double buffered); P (bf16) is written over the first 64 columns of its S buffer.
 constexpr int kQStages = 3;
 constexpr uint32_t kOffQ = 0;                                  // Q[kQStages]
-constexpr uint32_t kOffP = kQStages * kTileBytes;              // P[2]
-constexpr uint32_t kOffK = (kQStages + 2) * kTileBytes;        // K block
-constexpr uint32_t kOffV = (kQStages + 3) * kTileBytes;        // V block
+constexpr uint32_t kOffKV = kQStages * kTileBytes;             // {K, V}[2]
 constexpr uint32_t kOffBar = (kQStages + 4) * kTileBytes;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
 
 struct Bars {
   uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2];
-  uint64_t kv_full, kv_empty;
+  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+  uint64_t kv_full[2], kv_empty[2];
   uint32_t tmem_base;
   int32_t fail;
 };
@@ -237,13 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B.s_full[b], 1);
-      mbar_init(&B.s_free[b], 4);
       mbar_init(&B.p_full[b], 4);
       mbar_init(&B.o_full[b], 1);
       mbar_init(&B.o_free[b], 4);
+      mbar_init(&B.kv_full[b], 1);
+      mbar_init(&B.kv_empty[b], 1);
     }
-    mbar_init(&B.kv_full, 1);
-    mbar_init(&B.kv_empty, 1);
     B.fail = 0;
     mbar_fence_init();
   }
@@ -309,14 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (d.x != loaded_gj) {
-        if (loaded_gj != -1 && !wait_or_fail(&B.kv_empty, (kv_loads - 1) & 1, fail)) break;
+        // K/V load number kv_loads goes to buffer kv_loads & 1, free once the last tile of
+        // load kv_loads - 2 has finished its O MMA
+        const int c = kv_loads & 1;
+        if (kv_loads >= 2 && !wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) break;
         if (lane == 0) {
-          mbar_expect_tx(&B.kv_full, 4 * kBox);
+          uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
+          mbar_expect_tx(&B.kv_full[c], 4 * kBox);
           const int tok = j * 128;
-          tma_load_3d(smem + kOffK, &kmap, &B.kv_full, 0, g, tok);
-          tma_load_3d(smem + kOffK + kBox, &kmap, &B.kv_full, 64, g, tok);
-          tma_load_3d(smem + kOffV, &vmap, &B.kv_full, 0, g, tok);
-          tma_load_3d(smem + kOffV + kBox, &vmap, &B.kv_full, 64, g, tok);
+          tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
+          tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
+          tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
+          tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
         }
         ++kv_loads;
         loaded_gj = d.x;
@@ -325,14 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    // Event loop: issue O(oi) as soon as its P is ready, S(si) as soon as its queries and
-    // S buffer are ready, O first. A tile on a new K/V block waits until every O of the
-    // previous block is issued (its release is committed with the last one).
+    // Event loop: issue O(oi) as soon as its P is in tensor memory, S(si) as soon as its
+    // queries and K/V block are loaded and O(si-2) (which reads P from S(si)'s columns) has
+    // completed; O first.
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
-      const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
+      const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
       int si = 0, oi = 0, kv_gj = -1, kv_loads = 0;
-      int gj_ring[2] = {-1, -1};  // K/V list of the tiles whose S is issued and O is not
+      int gj_ring[2] = {-1, -1}, kvb_ring[2] = {0, 0};  // tiles with S issued, O not yet
       int next_gj = load_desc(p, t0).x;
       uint32_t idle = 0;
       while (oi < n && !*fail) {
@@ -343,17 +346,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
               (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
             tmem_fence_after();
-            const uint32_t pa = sbase + kOffP + b * kTileBytes;
-            const uint32_t va = sbase + kOffV;
+            const int c = kvb_ring[b];
+            const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = umma_desc_sw128(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-              umma_bf16(tmem + 256 + b * 128, ad, bd, idesc_o, kk > 0);
+              umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
             }
             umma_commit(&B.o_full[b]);
             const int gj_o = gj_ring[b];
             const int gj_after = oi + 1 < si ? gj_ring[(oi + 1) & 1] : (oi + 1 < n ? next_gj : -2);
-            if (gj_after != gj_o) umma_commit(&B.kv_empty);  // last tile on this K/V block
+            if (gj_after != gj_o) umma_commit(&B.kv_empty[c]);  // last tile on this K/V load
             ++oi;
             progress = true;
           }
@@ -363,17 +365,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = si & 1, qs = si % kQStages;
           const int gj = next_gj;
           bool kv_ok = gj == kv_gj;
-          if (!kv_ok && oi == si) {  // previous block fully consumed: switch to the new one
-            if (!wait_or_fail(&B.kv_full, kv_loads & 1, fail)) break;
-            ++kv_loads;
+          if (!kv_ok && mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) {
+            ++kv_loads;  // the next K/V load (a new block) has landed
             kv_gj = gj;
             kv_ok = true;
           }
           if (kv_ok && mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
-              (si < 2 || mbar_test(&B.s_free[b], ((si - 2) >> 1) & 1))) {
+              (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
             tmem_fence_after();
+            const int c = (kv_loads - 1) & 1;
             const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
-            const uint32_t ka = sbase + kOffK;
+            const uint32_t ka = sbase + kOffKV + c * 2 * kTileBytes;
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
               umma_bf16(tmem + b * 128, umma_desc_sw128(qa + off, 16, 1024),
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&B.s_full[b]);
             umma_commit(&B.q_empty[qs]);
             gj_ring[b] = gj;
+            kvb_ring[b] = c;
             ++si;
             if (si < n) next_gj = load_desc(p, t0 + si).x;
             progress = true;
@@ -414,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t e_next = qi < d_next.z ? p.entries[d_next.y + qi] : -1;
     const uint32_t s_tmem = tmem + lane_addr + wg * 128;
     const uint32_t o_tmem = tmem + lane_addr + 256 + wg * 128;
-    uint8_t* prow = smem + kOffP + wg * kTileBytes;
     for (int k = wg; k < n; k += 2) {
       const int use = k >> 1;  // this warpgroup's use count of its buffers
       const int4 d = d_next;
@@ -432,9 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, v + c * 32);
       tmem_wait_ld();
-      tmem_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.s_free[wg]);
       // causal mask: key j*128 + col is visible to the query iff it is <= the query position
       const int64_t qpos = ent >= 0 ? p.q_start + ent / p.topk : -1;
       const int64_t lim64 = qpos - (int64_t)j * 128;  // last visible column
@@ -458,20 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[x] = ex2(fmaf(v[x], kLog2e, -mscaled));
         l8[x & 7] += v[x];
       }
-      // P row (bf16) into the swizzled K-major A-operand tile
+      // P row (bf16 pairs) into the first 64 columns of this tile's S buffer: the A operand
+      // of the O MMA
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh)
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int k0 = kh * 64 + c * 8;
-          uint4 u;
-          u.x = pack_bf16x2(v[k0 + 0], v[k0 + 1]);
-          u.y = pack_bf16x2(v[k0 + 2], v[k0 + 3]);
-          u.z = pack_bf16x2(v[k0 + 4], v[k0 + 5]);
-          u.w = pack_bf16x2(v[k0 + 6], v[k0 + 7]);
-          *reinterpret_cast<uint4*>(prow + kh * kBox + sw128(row, c)) = u;
-        }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(v[h2 * 64 + 2 * x], v[h2 * 64 + 2 * x + 1]);
+        tmem_st32(s_tmem + h2 * 32, pk);
+      }
+      tmem_wait_st();
+      tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[wg]);
       const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
