@@ -72,30 +72,38 @@ struct PrefillWorkspace {
   size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc, total;
 };
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+// Prefill work lists are per (group, query window, KV block): queries are cut into windows of
+// kPrefillWindow so that the tiles of one window -- whose query rows fit in L2 -- run together.
+constexpr int32_t kPrefillWindow = 2048;
+inline int32_t prefill_nwin(int64_t T) { return (int32_t)((T + kPrefillWindow - 1) / kPrefillWindow); }
 inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, int32_t nblk,
                                           int32_t G, bool attention) {
   PrefillWorkspace w{};
+  const size_t lists = (size_t)Hkv * (attention ? prefill_nwin(T) : 1) * nblk;
+  const size_t groups = lists / nblk;
   size_t off = 0;
-  w.counts = off;       off = ws_align(off + 4 * (size_t)Hkv * nblk);
-  w.group_base = off;   off = ws_align(off + 4 * (size_t)(Hkv + 1));
-  w.tile_offsets = off; off = ws_align(off + 4 * ((size_t)Hkv * nblk + 1));
+  w.counts = off;       off = ws_align(off + 4 * lists);
+  w.group_base = off;   off = ws_align(off + 4 * (groups + 1));
+  w.tile_offsets = off; off = ws_align(off + 4 * (groups * (nblk + 1) + groups + 1));
   if (attention) {
     const size_t sel = (size_t)T * Hkv * topk;
-    w.offsets = off;    off = ws_align(off + 4 * (size_t)Hkv * (nblk + 1));
+    w.offsets = off;    off = ws_align(off + 4 * groups * (nblk + 1));
     w.entries = off;    off = ws_align(off + 4 * sel);
     w.part_o = off;     off = ws_align(off + 2 * sel * G * 128);
     w.part_lse = off;   off = ws_align(off + 4 * sel * G);
     // one 16-byte descriptor per work tile of 128/G queries: at most sel/(128/G) + lists
-    w.tile_desc = off;  off = ws_align(off + 16 * (sel * G / 128 + (size_t)Hkv * nblk + 1));
+    w.tile_desc = off;  off = ws_align(off + 16 * (sel * G / 128 + lists + 1));
   }
   w.total = off;
   return w;
 }
 // (a) bucketing; tiles of `qpt` queries are laid out for the attention kernel.
+// List of selection (t, slot) of group g: ((g * nwin + t / win) * nblk + j); the per-list
+// offsets are relative to their (group, window) segment, segments in (g, w) order.
 cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
-                          int32_t nblk, int32_t qpt, int32_t* offsets, int32_t* entries,
-                          int32_t* counts, int32_t* group_base, int32_t* tile_offsets,
-                          cudaStream_t stream);
+                          int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,
+                          int32_t* entries, int32_t* counts, int32_t* group_base,
+                          int32_t* tile_offsets, cudaStream_t stream);
 struct PrefillArgs {
   const uint16_t* q;           // [T, Hq, D]
   const uint16_t* k;           // [S_kv, Hkv, D]

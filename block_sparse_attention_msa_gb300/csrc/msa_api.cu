@@ -266,7 +266,7 @@ int msa_prefill_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t
   const msa::PrefillWorkspace W = msa::prefill_ws_layout(0, Hkv, 1, nblk, 1, false);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return cuda_status(
-      msa::launch_bucket(block_ids, T, Hkv, topk, nblk, 128, offsets, entries,
+      msa::launch_bucket(block_ids, T, Hkv, topk, nblk, T > 0 ? T : 1, 128, offsets, entries,
                          reinterpret_cast<int32_t*>(ws + W.counts),
                          reinterpret_cast<int32_t*>(ws + W.group_base),
                          reinterpret_cast<int32_t*>(ws + W.tile_offsets), as_stream(stream)),

@@ -35,18 +35,31 @@ namespace msa {
 namespace {
 
 // ------------------------------------------------------------------------------ bucketing
-__global__ void bucket_count_kernel(const int32_t* __restrict__ block_ids, int64_t n, int32_t Hkv,
-                                    int32_t topk, int32_t nblk, int32_t* __restrict__ counts) {
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t j = block_ids[idx];
-    if (j < 0) continue;
-    if (j >= nblk) {
-      msa_record_error(kErrBadBlock);
-      continue;
+__device__ __forceinline__ int64_t list_of(int64_t idx, int32_t Hkv, int32_t topk, int32_t nblk,
+                                           int32_t win, int32_t nwin, int32_t j) {
+  const int64_t t = idx / ((int64_t)topk * Hkv);
+  const int g = (int)((idx / topk) % Hkv);
+  return ((int64_t)g * nwin + t / win) * nblk + j;
+}
+
+// One thread per (query, group) row: counts every valid selection into its list.
+__global__ void bucket_count_kernel(const int32_t* __restrict__ block_ids, int64_t rows,
+                                    int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
+                                    int32_t nwin, int32_t* __restrict__ counts) {
+  for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < rows;
+       row += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = row / Hkv;
+    const int g = (int)(row % Hkv);
+    const int64_t list0 = ((int64_t)g * nwin + t / win) * nblk;
+    for (int s = 0; s < topk; ++s) {
+      const int32_t j = block_ids[row * topk + s];
+      if (j < 0) continue;
+      if (j >= nblk) {
+        msa_record_error(kErrBadBlock);
+        continue;
+      }
+      atomicAdd(&counts[list0 + j], 1);
     }
-    const int g = (int)((idx / topk) % Hkv);
-    atomicAdd(&counts[(int64_t)g * nblk + j], 1);
   }
 }
 
@@ -79,46 +92,67 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return out;
 }
 
-// One CTA: per-group exclusive offsets of the lists, the group bases, the global tile
-// offsets (tiles of `qpt` queries per list), and counts reset to zero for the scatter.
+// One CTA per (group, window) segment: exclusive offsets of the segment's lists, the
+// segment-local tile prefix (tiles of `qpt` queries per list) with the segment totals at
+// index nblk, and counts reset to zero for the scatter.
 __global__ void __launch_bounds__(1024)
-    bucket_scan_kernel(int32_t* __restrict__ counts, int32_t Hkv, int32_t nblk, int32_t qpt,
-                       int32_t* __restrict__ offsets, int32_t* __restrict__ group_base,
-                       int32_t* __restrict__ tile_offsets) {
+    bucket_scan_kernel(int32_t* __restrict__ counts, int32_t nblk, int32_t qpt,
+                       int32_t* __restrict__ offsets, int32_t* __restrict__ tile_local) {
   __shared__ int warp_sums[33];
-  int tile_carry = 0, base = 0;
-  for (int g = 0; g < Hkv; ++g) {
-    int carry = 0;
-    for (int j0 = 0; j0 < nblk; j0 += blockDim.x) {
-      const int j = j0 + threadIdx.x;
-      const int c = j < nblk ? counts[(int64_t)g * nblk + j] : 0;
-      const int nt = (c + qpt - 1) / qpt;
-      int tot_c, tot_t;
-      const int ex_c = block_exclusive_scan(c, warp_sums, &tot_c);
-      const int ex_t = block_exclusive_scan(nt, warp_sums, &tot_t);
-      if (j < nblk) {
-        offsets[(int64_t)g * (nblk + 1) + j] = carry + ex_c;
-        tile_offsets[(int64_t)g * nblk + j] = tile_carry + ex_t;
-        counts[(int64_t)g * nblk + j] = 0;
-      }
-      carry += tot_c;
-      tile_carry += tot_t;
+  const int seg = blockIdx.x;
+  int carry = 0, tile_carry = 0;
+  for (int j0 = 0; j0 < nblk; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    const int c = j < nblk ? counts[(int64_t)seg * nblk + j] : 0;
+    const int nt = (c + qpt - 1) / qpt;
+    int tot_c, tot_t;
+    const int ex_c = block_exclusive_scan(c, warp_sums, &tot_c);
+    const int ex_t = block_exclusive_scan(nt, warp_sums, &tot_t);
+    if (j < nblk) {
+      offsets[(int64_t)seg * (nblk + 1) + j] = carry + ex_c;
+      tile_local[(int64_t)seg * (nblk + 1) + j] = tile_carry + ex_t;
+      counts[(int64_t)seg * nblk + j] = 0;
     }
-    if (threadIdx.x == 0) {
-      offsets[(int64_t)g * (nblk + 1) + nblk] = carry;
-      group_base[g] = base;
-    }
-    base += carry;
+    carry += tot_c;
+    tile_carry += tot_t;
   }
   if (threadIdx.x == 0) {
-    group_base[Hkv] = base;
-    tile_offsets[(int64_t)Hkv * nblk] = tile_carry;
+    offsets[(int64_t)seg * (nblk + 1) + nblk] = carry;
+    tile_local[(int64_t)seg * (nblk + 1) + nblk] = tile_carry;
+  }
+}
+
+// One CTA: exclusive scan of the segment totals -> entry base per segment (group_base) and
+// tile base per segment; the grand totals at index nseg.
+__global__ void __launch_bounds__(1024)
+    bucket_seg_scan_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_local,
+                           int32_t nseg, int32_t nblk, int32_t* __restrict__ group_base,
+                           int32_t* __restrict__ seg_tile_base) {
+  __shared__ int warp_sums[33];
+  int carry = 0, tile_carry = 0;
+  for (int s0 = 0; s0 < nseg; s0 += blockDim.x) {
+    const int sg = s0 + threadIdx.x;
+    const int c = sg < nseg ? offsets[(int64_t)sg * (nblk + 1) + nblk] : 0;
+    const int t = sg < nseg ? tile_local[(int64_t)sg * (nblk + 1) + nblk] : 0;
+    int tot_c, tot_t;
+    const int ex_c = block_exclusive_scan(c, warp_sums, &tot_c);
+    const int ex_t = block_exclusive_scan(t, warp_sums, &tot_t);
+    if (sg < nseg) {
+      group_base[sg] = carry + ex_c;
+      seg_tile_base[sg] = tile_carry + ex_t;
+    }
+    carry += tot_c;
+    tile_carry += tot_t;
+  }
+  if (threadIdx.x == 0) {
+    group_base[nseg] = carry;
+    seg_tile_base[nseg] = tile_carry;
   }
 }
 
 __global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int64_t n,
-                                      int32_t Hkv, int32_t topk, int32_t nblk,
-                                      const int32_t* __restrict__ offsets,
+                                      int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
+                                      int32_t nwin, const int32_t* __restrict__ offsets,
                                       const int32_t* __restrict__ group_base,
                                       int32_t* __restrict__ cursor, int32_t* __restrict__ entries) {
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
@@ -126,28 +160,30 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int
     const int32_t j = block_ids[idx];
     if (j < 0 || j >= nblk) continue;
     const int64_t t = idx / ((int64_t)topk * Hkv);
-    const int g = (int)((idx / topk) % Hkv);
     const int slot = (int)(idx % topk);
-    const int pos = group_base[g] + offsets[(int64_t)g * (nblk + 1) + j] +
-                    atomicAdd(&cursor[(int64_t)g * nblk + j], 1);
+    const int64_t list = list_of(idx, Hkv, topk, nblk, win, nwin, j);
+    const int64_t seg = list / nblk;  // (group, window) segment
+    const int pos = group_base[seg] + offsets[seg * (nblk + 1) + j] + atomicAdd(&cursor[list], 1);
     entries[pos] = (int32_t)(t * topk + slot);
   }
 }
 
-// Compact descriptor of every work tile: (list gj = g*nblk + j, first entry, valid queries).
-// One warp per list; lanes over the list's tiles.
+// Compact descriptor of every work tile: (list, first entry, valid queries). One warp per
+// list; lanes over the list's tiles. nseg = number of (group, window) segments.
 __global__ void __launch_bounds__(256)
     tile_desc_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ group_base,
-                     const int32_t* __restrict__ tile_offsets, int32_t Hkv, int32_t nblk,
+                     const int32_t* __restrict__ tile_local,
+                     const int32_t* __restrict__ seg_tile_base, int32_t nseg, int32_t nblk,
                      int32_t qpt, int4* __restrict__ desc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gj = blockIdx.x * 8 + warp;
-  if (gj >= Hkv * nblk) return;
-  const int g = gj / nblk, j = gj % nblk;
-  const int32_t* off = offsets + (int64_t)g * (nblk + 1) + j;
+  if (gj >= nseg * nblk) return;
+  const int seg = gj / nblk, j = gj % nblk;
+  const int32_t* off = offsets + (int64_t)seg * (nblk + 1) + j;
   const int lbeg = off[0], lcnt = off[1] - off[0];
-  const int first = group_base[g] + lbeg;
-  const int t0 = tile_offsets[gj], nt = tile_offsets[gj + 1] - t0;
+  const int first = group_base[seg] + lbeg;
+  const int32_t* tl = tile_local + (int64_t)seg * (nblk + 1) + j;
+  const int t0 = seg_tile_base[seg] + tl[0], nt = tl[1] - tl[0];
   for (int c = lane; c < nt; c += 32)
     desc[t0 + c] = make_int4(gj, first + c * qpt, min(qpt, lcnt - c * qpt), 0);
 }
@@ -162,6 +198,7 @@ constexpr uint32_t kBox = 128 * 64 * 2;          // 128 rows x 64 channels bf16 
 constexpr uint32_t kTileBytes = 2 * kBox;        // Q tile, P tile, K block or V block: 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/384
+constexpr int kChunk = 4;                        // consecutive tiles per CTA per round
 
 // shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
 // query tiles hides the latency of the scattered row gathers; two K/V block buffers let the
@@ -183,9 +220,9 @@ struct Bars {
 
 struct PreKParams {
   const int32_t* entries;
-  const int4* desc;                // per-tile (gj, first entry, valid queries)
+  const int4* desc;                // per-tile (list, first entry, valid queries)
   const int32_t* tile_offsets;
-  int32_t Hkv, G, topk, nblk, qpt;
+  int32_t Hkv, G, topk, nblk, qpt, nwin;
   int64_t q_start;
   uint16_t* part_o;               // chunk-major [16][part_rows][8] bf16
   int64_t part_rows;               // T*Hkv*topk*G
@@ -222,13 +259,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t* fail = &B.fail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int n_gj = p.Hkv * p.nblk;
-  const int64_t total = p.tile_offsets[n_gj];
-  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  const int64_t t0 = (int64_t)blockIdx.x * per;
-  const int64_t t1 = t0 + per < total ? t0 + per : total;
-  if (t0 >= t1) return;  // uniform for the CTA
-  const int n = (int)(t1 - t0);
+  // Tiles are dealt round-robin in chunks of kChunk: CTA c takes tiles
+  // (r * gridDim + c) * kChunk + q, so all CTAs sweep the (group, window)-ordered tile list
+  // together and the current window's query rows and K/V blocks stay in L2.
+  const int64_t nseg = (int64_t)p.Hkv * p.nwin;
+  const int64_t total = p.tile_offsets[nseg * (p.nblk + 1) + nseg];  // sum of segment tiles
+  const int64_t round_tiles = (int64_t)gridDim.x * kChunk;
+  const int64_t full_rounds = total / round_tiles;
+  const int64_t rem = total - full_rounds * round_tiles;
+  const int64_t mine_rem = rem - (int64_t)blockIdx.x * kChunk;
+  const int n = (int)(full_rounds * kChunk + (mine_rem <= 0 ? 0 : (mine_rem < kChunk ? mine_rem : kChunk)));
+  if (n == 0) return;  // uniform for the CTA
+  auto tile_of = [&](int i) -> int64_t {
+    return ((int64_t)(i / kChunk) * gridDim.x + blockIdx.x) * kChunk + (i % kChunk);
+  };
+  const int64_t lists_per_group = (int64_t)p.nwin * p.nblk;
 
   if (tid == 0) {
     for (int q = 0; q < kQStages; ++q) {
@@ -269,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&vmap);
     }
     constexpr int kMaxQPerLane = 4;  // qpt = 128/G <= 128
-    int4 d0 = load_desc(p, t0);
-    int4 d1 = n > 1 ? load_desc(p, t0 + 1) : d0;
+    int4 d0 = load_desc(p, tile_of(0));
+    int4 d1 = n > 1 ? load_desc(p, tile_of(1)) : d0;
     int32_t e0[kMaxQPerLane];
 #pragma unroll
     for (int r = 0; r < kMaxQPerLane; ++r) {
@@ -291,10 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           e0[r] = q < d1.z ? p.entries[d1.y + q] : -1;
         }
         d0 = d1;
-        if (i + 2 < n) d1 = load_desc(p, t0 + i + 2);
+        if (i + 2 < n) d1 = load_desc(p, tile_of(i + 2));
       }
       if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
-      const int g = d.x / p.nblk, j = d.x % p.nblk;
+      const int g = (int)(d.x / lists_per_group), j = d.x % p.nblk;
       uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
       if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
       __syncwarp();
@@ -336,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
       int si = 0, oi = 0, kv_gj = -1, kv_loads = 0;
       int gj_ring[2] = {-1, -1}, kvb_ring[2] = {0, 0};  // tiles with S issued, O not yet
-      int next_gj = load_desc(p, t0).x;
+      int next_gj = load_desc(p, tile_of(0)).x;
       uint32_t idle = 0;
       while (oi < n && !*fail) {
         bool progress = false;
@@ -386,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             gj_ring[b] = gj;
             kvb_ring[b] = c;
             ++si;
-            if (si < n) next_gj = load_desc(p, t0 + si).x;
+            if (si < n) next_gj = load_desc(p, tile_of(si)).x;
             progress = true;
           }
         }
@@ -412,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = p.G;
     const int qi = row / G, h = row % G;
     // software prefetch: descriptors two of this warpgroup's tiles ahead, entry one ahead
-    int4 d_next = wg < n ? load_desc(p, t0 + wg) : make_int4(0, 0, 0, 0);
-    int4 d_next2 = wg + 2 < n ? load_desc(p, t0 + wg + 2) : d_next;
+    int4 d_next = wg < n ? load_desc(p, tile_of(wg)) : make_int4(0, 0, 0, 0);
+    int4 d_next2 = wg + 2 < n ? load_desc(p, tile_of(wg + 2)) : d_next;
     int32_t e_next = qi < d_next.z ? p.entries[d_next.y + qi] : -1;
     const uint32_t s_tmem = tmem + lane_addr + wg * 128;
     const uint32_t o_tmem = tmem + lane_addr + 256 + wg * 128;
@@ -424,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k + 2 < n) {
         e_next = qi < d_next2.z ? p.entries[d_next2.y + qi] : -1;
         d_next = d_next2;
-        if (k + 4 < n) d_next2 = load_desc(p, t0 + k + 4);
+        if (k + 4 < n) d_next2 = load_desc(p, tile_of(k + 4));
       }
       const int j = d.x % p.nblk;
       // ---------------- softmax of tile k
@@ -483,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_fence_before();
       if (ent >= 0) {
         const int64_t t = ent / p.topk;
-        const int64_t prow_idx = ((t * p.Hkv + d.x / p.nblk) * p.topk + ent % p.topk) * G + h;
+        const int64_t prow_idx = ((t * p.Hkv + d.x / lists_per_group) * p.topk + ent % p.topk) * G + h;
         p.part_lse[prow_idx] = l > 0.f ? mx + __logf(l) : -INFINITY;
         uint4* dst = reinterpret_cast<uint4*>(p.part_o) + prow_idx;
 #pragma unroll
@@ -513,17 +558,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
-                          int32_t nblk, int32_t qpt, int32_t* offsets, int32_t* entries,
-                          int32_t* counts, int32_t* group_base, int32_t* tile_offsets,
-                          cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)Hkv * nblk, stream);
+                          int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,
+                          int32_t* entries, int32_t* counts, int32_t* group_base,
+                          int32_t* tile_offsets, cudaStream_t stream) {
+  const int32_t nwin = (T + win - 1) / win > 0 ? (T + win - 1) / win : 1;
+  const int32_t nseg = Hkv * nwin;  // (group, window) segments
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)nseg * nblk, stream);
   if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)T * Hkv * topk;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8));
-  bucket_count_kernel<<<grid, 256, 0, stream>>>(block_ids, n, Hkv, topk, nblk, counts);
-  bucket_scan_kernel<<<1, 1024, 0, stream>>>(counts, Hkv, nblk, qpt, offsets, group_base,
-                                             tile_offsets);
-  bucket_scatter_kernel<<<grid, 256, 0, stream>>>(block_ids, n, Hkv, topk, nblk, offsets,
+  const int64_t rows = (int64_t)T * Hkv;
+  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)sm_count() * 8));
+  bucket_count_kernel<<<rgrid, 256, 0, stream>>>(block_ids, rows, Hkv, topk, nblk, win, nwin,
+                                                 counts);
+  // tile_offsets holds the segment-local tile prefix [nseg][nblk+1], then the segment tile
+  // bases [nseg+1]
+  int32_t* tile_local = tile_offsets;
+  int32_t* seg_tile_base = tile_offsets + (size_t)nseg * (nblk + 1);
+  bucket_scan_kernel<<<nseg, 1024, 0, stream>>>(counts, nblk, qpt, offsets, tile_local);
+  bucket_seg_scan_kernel<<<1, 1024, 0, stream>>>(offsets, tile_local, nseg, nblk, group_base,
+                                                 seg_tile_base);
+  bucket_scatter_kernel<<<grid, 256, 0, stream>>>(block_ids, n, Hkv, topk, nblk, win, nwin, offsets,
                                                   group_base, counts, entries);
   return cudaGetLastError();
 }
@@ -540,8 +595,9 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   uint16_t* part_o = reinterpret_cast<uint16_t*>(a.workspace + W.part_o);
   float* part_lse = reinterpret_cast<float*>(a.workspace + W.part_lse);
   int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
-  cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, qpt, offsets, entries,
-                                counts, group_base, tile_offsets, stream);
+  const int32_t nwin = prefill_nwin(a.T);
+  cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, kPrefillWindow, qpt,
+                                offsets, entries, counts, group_base, tile_offsets, stream);
   if (e != cudaSuccess) return e;
 
   CUtensorMap qmap, kmap, vmap;
@@ -555,8 +611,10 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
       !encode_bf16_map(&kmap, a.k, 3, dims, strides, box, true) ||
       !encode_bf16_map(&vmap, a.v, 3, dims, strides, box, true))
     return cudaErrorInvalidValue;
-  tile_desc_kernel<<<(unsigned)((a.Hkv * a.nblk + 7) / 8), 256, 0, stream>>>(
-      offsets, group_base, tile_offsets, a.Hkv, a.nblk, qpt, tile_desc);
+  const int32_t nseg = a.Hkv * nwin;
+  tile_desc_kernel<<<(unsigned)((nseg * a.nblk + 7) / 8), 256, 0, stream>>>(
+      offsets, group_base, tile_offsets, tile_offsets + (size_t)nseg * (a.nblk + 1), nseg, a.nblk,
+      qpt, tile_desc);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   PreKParams p;
@@ -568,6 +626,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.topk = a.topk;
   p.nblk = a.nblk;
   p.qpt = qpt;
+  p.nwin = nwin;
   p.q_start = a.S_kv - a.T;
   p.part_o = part_o;
   p.part_rows = (int64_t)a.T * a.Hkv * a.topk * G;
