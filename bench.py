@@ -297,13 +297,17 @@ def run_ours(args, ws, rank, local):
                                "block-major sparse prefill (32768 tokens)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
+        # kernels of this library per step: scorer (1); page table, decode, merge (3); bucket
+        # count, two scans, scatter, tile descriptors, attention, merge (7). Memsets not counted.
         "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
-                                      + ("prefill" in run) * 5),
+                                      + ("prefill" in run) * 7),
         "clocks": clk.summary(), "device_error_word": err,
     }
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
         if key not in run:
             stages[name] = None
+    if args.cfg5:
+        line["cfg5"] = run_cfg5(args, local)
     if args.small or run != {"score", "decode", "prefill"}:
         line["config"]["partial_run"] = f"stages={sorted(run)} small={args.small} (profiling only)"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and "score" in run:
@@ -409,6 +413,72 @@ def cpu_baseline(c2, seconds: float):
             "sample": f"{n} full passes of all {B} requests (scores + top-k) in {dt:.1f} s"}
 
 
+def run_cfg5(args, local):
+    """1M-token layer, reported per stage (not part of the headline step): 4 x 1,048,576-token
+    decode (score + top-k, sparse page table, paged decode, k 32) and a 32768-token prefill chunk
+    on a 1,048,576-token prefix (score + top-k over every chunk row, then block-major attention)."""
+    import block_sparse_attention_msa_gb300 as msa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    msa.load(build_if_missing=True)
+    pk = peaks()
+    out = {}
+    w = workloads.cfg5_decode(dev, seed=5)
+    ws_ = msa.Workspace()
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    B, Hkv, Di, k = w["B"], w["Hkv"], w["Di"], w["topk"]
+    ids, _ = msa.index_score_topk(w["q_idx"], w["k_idx_pages"], w["page_table"], w["seq_lens"], 1, k,
+                                  workspace=ws_)
+    fpt, lens = msa.build_sparse_page_table(ids, w["page_table"], w["seq_lens"], 1, w["num_pages"])
+    ms_s = timed(lambda: msa.index_score_topk(w["q_idx"], w["k_idx_pages"], w["page_table"],
+                                              w["seq_lens"], 1, k, workspace=ws_), max(3, args.steps))
+    ms_pt = timed(lambda: msa.build_sparse_page_table(ids, w["page_table"], w["seq_lens"], 1,
+                                                      w["num_pages"]), max(3, args.steps))
+    ms_d = timed(lambda: msa.paged_sparse_decode(w["q"], w["k_cache"], w["v_cache"], fpt, lens,
+                                                 workspace=ws_), max(3, args.steps))
+    kidx_bytes = int(w["seq_lens"].to(torch.int64).sum()) * Hkv * Di * 2
+    kv_bytes = int(lens.to(torch.int64).sum()) * w["D"] * 2 * 2
+    out["decode_score_topk"] = {"ms": round(ms_s, 4), "GB/s": round(kidx_bytes / ms_s / 1e6, 1),
+                                "frac_hbm": round(kidx_bytes / ms_s / 1e6 / pk["hbm_gbs"], 4)}
+    out["decode_page_table_ms"] = round(ms_pt, 4)
+    out["decode_attention"] = {"ms": round(ms_d, 4), "GB/s": round(kv_bytes / ms_d / 1e6, 1),
+                               "frac_hbm": round(kv_bytes / ms_d / 1e6 / pk["hbm_gbs"], 4)}
+    del w, ids, fpt, lens
+    torch.cuda.empty_cache()
+    w = workloads.cfg5_prefill(dev, seed=6)
+    T, S, P = w["T"], w["S"], w["P"]
+    kidx_pages = w["k_idx"].view(P, 128, Hkv, Di)
+    sl = torch.tensor([S], dtype=torch.int32, device=dev)
+    ws2 = msa.Workspace()
+    ids, _ = msa.index_score_topk(w["q_idx"], kidx_pages, w["page_table"], sl, T, k, workspace=ws2)
+    ms_ps = timed(lambda: msa.index_score_topk(w["q_idx"], kidx_pages, w["page_table"], sl, T, k,
+                                               workspace=ws2), 2)
+    kk, vv = w["k"][:S], w["v"][:S]
+    ms_pa = timed(lambda: msa.sparse_prefill(w["q"], kk, vv, ids, workspace=ws2), 3)
+    q_pos = torch.arange(S - T, S, device=dev, dtype=torch.int64)
+    score_flops = 2 * Di * Hkv * int((q_pos + 1).sum())  # every causal key of every row
+    attn_flops = 4 * w["D"] * (w["Hq"] // Hkv) * int(visible_keys(ids, q_pos).sum())
+    out["prefill_score_topk"] = {"ms": round(ms_ps, 3), "TFLOP/s": round(score_flops / ms_ps / 1e9, 1),
+                                 "flops": score_flops}
+    out["prefill_attention"] = {"ms": round(ms_pa, 3), "TFLOP/s": round(attn_flops / ms_pa / 1e9, 1),
+                                "frac_bf16": round(attn_flops / ms_pa / 1e9 / pk["bf16_tflops_sustained"], 4),
+                                "flops": attn_flops}
+    return out
+
+
 def run_reference(args, ws, rank, local):
     if rank != 0:
         return
@@ -452,6 +522,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--stages", default="score,decode,prefill",
                     help="comma list of stages to run (profiling captures)")
+    ap.add_argument("--cfg5", action="store_true",
+                    help="also report the 1M-token layer's stages (takes about a minute)")
     ap.add_argument("--small", action="store_true",
                     help="smaller decode/prefill workloads (profiling captures only)")
     args = ap.parse_args()

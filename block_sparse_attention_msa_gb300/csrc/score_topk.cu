@@ -20,8 +20,9 @@
 //  * the top-k is fused: the CTA that completes a request's last page (an atomic ticket
 //    per request, no spinning) selects the blocks of every (query row, group) of that
 //    request with a warp-level radix select.
-// Long query chunks (prefill, N > 8) use a tiled CUDA-core scorer writing every block
-// score, then the same warp top-k in a separate launch.
+// Long query chunks (prefill, N > 8) are a dense contraction and run on the tensor cores
+// (tcgen05, accumulators in tensor memory), writing every visible block score; the same warp
+// top-k follows in a separate launch.
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
@@ -444,83 +445,268 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------
-// Generic scorer: CTA = (request, 32 query rows, group, chunk of 16 blocks).
-constexpr int kRowTile = 32;
-constexpr int kBlkChunk = 16;
+// Multi-row scorer (N > 8: a prefill chunk, or many draft rows) on the tensor cores.
+//
+// The scores of one (request, group) are the product of the request's query-index rows
+// (N x Di) with the transposed key-index rows of every visible block, reduced by a max over
+// each block's 128 keys: a dense contraction, so it runs as tcgen05 MMAs with the accumulator
+// in tensor memory. A work item is (request, group, chunk of kScoreChunk = 4 consecutive
+// blocks). Its 4 key blocks (512 keys) stay in shared memory while the query rows that can see
+// them stream through in 128-row tiles; one tile is two M=128, N=256 MMA groups into the two
+// halves of tensor memory. Each key-index row is read from HBM once; the query rows of a
+// (request, group) are re-read from L2 by every chunk (all CTAs sweep the same request and
+// group at the same time).
+//
+// Warp 0 issues the TMA copies, warp 1 the MMAs, and warps 2..9 form two epilogue
+// warpgroups: warpgroup h drains accumulator half h (blocks 2h and 2h+1 of the chunk), one
+// query row per thread, applies the causal mask on the row's own (local) block and writes one
+// max per block. While one half is drained the MMAs of the other half run.
+constexpr int kScoreChunk = 4;                            // key blocks per work item
+constexpr int kScThreads = 320;
+constexpr int kScQStages = 3;
 
 template <int DI>
-__global__ void __launch_bounds__(256) score_rows_kernel(const ScoreArgs a, int tiles_per_req) {
-  __shared__ __align__(16) float sq[kRowTile][DI + 4];
-  __shared__ __align__(16) uint16_t sk[128][DI + 8];
-  const int tid = threadIdx.x;
-  const int b = blockIdx.x / tiles_per_req;
-  const int i0 = (blockIdx.x % tiles_per_req) * kRowTile;
-  const int g = blockIdx.y;
-  const int j_begin = blockIdx.z * kBlkChunk;
-  const int j_end = min(a.max_blocks, j_begin + kBlkChunk);
-  bool bad = false;
-  const int seq = clamp_seq(a.seq_lens, b, a.N, a.max_blocks, bad);
-  if (bad && threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) msa_record_error(kErrBadBlock);
-  const int nrows = min(kRowTile, a.N - i0);
-  for (int e = tid; e < kRowTile * DI; e += 256) {
-    const int rr = e / DI, d = e % DI;
-    float v = 0.0f;
-    if (rr < nrows) {
-      const int64_t r = (int64_t)b * a.N + i0 + rr;
-      v = __uint_as_float((uint32_t)a.q_idx[(r * a.Hkv + g) * DI + d] << 16);
+struct ScoreTcLayout {
+  static constexpr uint32_t kBox = 128 * 64 * 2;           // 128 rows x 64 channels = 16 KB
+  static constexpr int kBoxes = DI / 64;
+  static constexpr uint32_t kQTile = kBoxes * kBox;
+  static constexpr uint32_t kKHalfBox = kScoreChunk * kBox;  // one 64-channel box of 4 blocks
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffQ = kBoxes * kKHalfBox;
+  static constexpr uint32_t kOffBar = kOffQ + kScQStages * kQTile;
+  static constexpr size_t kSmem = 1024 + kOffBar + 256;
+};
+
+struct ScoreTcBars {
+  uint64_t k_full, k_empty;
+  uint64_t q_full[kScQStages], q_empty[kScQStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  int32_t fail;
+};
+
+struct ScoreTcParams {
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t B, N, Hkv, max_blocks, max_chunks;
+  int64_t num_pages;
+  float* scores;
+};
+
+// Query-row tiles of work item (b, c): rows whose position can see a key of blocks
+// 4c..4c+3, in 128-row tiles counted from the request's first row. Returns the tile count.
+__device__ __forceinline__ int item_tiles(const ScoreTcParams& p, int b, int c, int seq, int& t_lo) {
+  const int nblk = (seq + 127) / 128;
+  if (c * kScoreChunk >= nblk) return 0;
+  const int first_row = c * kScoreChunk * 128 - (seq - p.N);  // first row seeing the chunk
+  t_lo = first_row <= 0 ? 0 : first_row / 128;
+  const int t_end = (p.N + 127) / 128;
+  return t_end - t_lo;
+}
+
+__device__ __forceinline__ bool sc_wait(uint64_t* bar, uint32_t parity, volatile int32_t* fail) {
+  if (*fail) return false;
+  if (mbar_wait(bar, parity)) return true;
+  msa_record_error(kErrTimeout);
+  *fail = 1;
+  return false;
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kScThreads, 1)
+    score_rows_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                         const __grid_constant__ CUtensorMap kmap, const ScoreTcParams p) {
+  using L = ScoreTcLayout<DI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  ScoreTcBars& Bz = *reinterpret_cast<ScoreTcBars*>(smem + L::kOffBar);
+  volatile int32_t* fail = &Bz.fail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t n_items = (int64_t)p.B * p.Hkv * p.max_chunks;
+
+  if (tid == 0) {
+    mbar_init(&Bz.k_full, 1);
+    mbar_init(&Bz.k_empty, 1);
+    for (int q = 0; q < kScQStages; ++q) {
+      mbar_init(&Bz.q_full[q], 1);
+      mbar_init(&Bz.q_empty[q], 1);
     }
-    sq[rr][d] = v;
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&Bz.acc_full[h], 1);
+      mbar_init(&Bz.acc_empty[h], 4);
+    }
+    Bz.fail = 0;
+    mbar_fence_init();
   }
-  const int rr = tid >> 3, sub = tid & 7;
-  const int qp = seq - a.N + i0 + rr;                  // this thread's query position
-  const int tile_local = (seq - a.N + i0 + nrows - 1) / 128;
-  for (int j = j_begin; j < j_end; ++j) {
-    float best = -INFINITY;
-    if (j <= tile_local) {
-      int32_t page = a.page_table[(int64_t)b * a.max_blocks + j];
-      if (page < 0 || page >= a.num_pages) {
-        msa_record_error(kErrBadPage);
-        page = 0;
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&Bz.tmem_base)), "n"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = Bz.tmem_base;
+  const uint32_t sbase = smem_u32(smem);
+
+  // Items in (request, group, chunk) order, dealt round-robin: all CTAs work on the chunks of
+  // one (request, group) at a time, so its query rows stay in L2.
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      int items_done = 0, tiles_done = 0;
+      for (int64_t it = blockIdx.x; it < n_items && !*fail; it += gridDim.x) {
+        const int c = (int)(it % p.max_chunks);
+        const int g = (int)((it / p.max_chunks) % p.Hkv);
+        const int b = (int)(it / ((int64_t)p.max_chunks * p.Hkv));
+        bool bad = false;
+        const int seq = clamp_seq(p.seq_lens, b, p.N, p.max_blocks, bad);
+        if (bad && g == 0 && c == 0) msa_record_error(kErrBadBlock);
+        int t_lo = 0;
+        const int nt = item_tiles(p, b, c, seq, t_lo);
+        if (nt <= 0) continue;
+        if (items_done > 0 && !sc_wait(&Bz.k_empty, (items_done - 1) & 1, fail)) break;
+        const int nblk = (seq + 127) / 128;
+        const int j0 = c * kScoreChunk;
+        const int nvalid = min(kScoreChunk, nblk - j0);
+        mbar_expect_tx(&Bz.k_full, (uint32_t)(nvalid * L::kBoxes) * L::kBox);
+        for (int s = 0; s < nvalid; ++s) {
+          int32_t page = p.page_table[(int64_t)b * p.max_blocks + j0 + s];
+          if (page < 0 || page >= p.num_pages) {
+            msa_record_error(kErrBadPage);
+            page = 0;
+          }
+          for (int h = 0; h < L::kBoxes; ++h)
+            tma_load_3d(smem + L::kOffK + h * L::kKHalfBox + s * L::kBox, &kmap, &Bz.k_full,
+                        h * 64, g, page * 128);
+        }
+        for (int t = 0; t < nt; ++t, ++tiles_done) {
+          const int qs = tiles_done % kScQStages;
+          if (tiles_done >= kScQStages &&
+              !sc_wait(&Bz.q_empty[qs], (tiles_done / kScQStages - 1) & 1, fail))
+            break;
+          mbar_expect_tx(&Bz.q_full[qs], L::kQTile);
+          const int row = b * p.N + (t_lo + t) * 128;
+          for (int h = 0; h < L::kBoxes; ++h)
+            tma_load_3d(smem + L::kOffQ + qs * L::kQTile + h * L::kBox, &qmap, &Bz.q_full[qs],
+                        h * 64, g, row);
+        }
+        ++items_done;
       }
-      __syncthreads();
-      for (int e = tid; e < 128 * (DI / 8); e += 256) {
-        const int tok = e / (DI / 8), c = e % (DI / 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(
-            a.k_idx + (((int64_t)page * 128 + tok) * a.Hkv + g) * DI + c * 8);
-        *reinterpret_cast<uint4*>(&sk[tok][c * 8]) = v;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(128, 256, 0, 0);  // Q (K-major) x K (K-major)
+      int items_done = 0, tiles_done = 0;
+      for (int64_t it = blockIdx.x; it < n_items && !*fail; it += gridDim.x) {
+        const int c = (int)(it % p.max_chunks);
+        const int b = (int)(it / ((int64_t)p.max_chunks * p.Hkv));
+        bool bad = false;
+        const int seq = clamp_seq(p.seq_lens, b, p.N, p.max_blocks, bad);
+        int t_lo = 0;
+        const int nt = item_tiles(p, b, c, seq, t_lo);
+        if (nt <= 0) continue;
+        if (!sc_wait(&Bz.k_full, items_done & 1, fail)) break;
+        for (int t = 0; t < nt; ++t, ++tiles_done) {
+          const int qs = tiles_done % kScQStages;
+          if (!sc_wait(&Bz.q_full[qs], (tiles_done / kScQStages) & 1, fail)) break;
+          const uint32_t qa = sbase + L::kOffQ + qs * L::kQTile;
+          for (int h = 0; h < 2; ++h) {
+            if (tiles_done > 0 && !sc_wait(&Bz.acc_empty[h], (tiles_done - 1) & 1, fail)) break;
+            tmem_fence_after();
+            const uint32_t ka = sbase + L::kOffK + h * 2 * L::kBox;  // blocks 2h, 2h+1
+#pragma unroll
+            for (int kk = 0; kk < DI / 16; ++kk) {
+              const uint32_t a_off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+              const uint32_t b_off = (kk >> 2) * L::kKHalfBox + (kk & 3) * 32;
+              umma_bf16(tmem + h * 256, umma_desc_sw128(qa + a_off, 16, 1024),
+                        umma_desc_sw128(ka + b_off, 16, 1024), idesc, kk > 0);
+            }
+            umma_commit(&Bz.acc_full[h]);
+          }
+          if (*fail) break;
+          umma_commit(&Bz.q_empty[qs]);
+        }
+        if (*fail) break;
+        umma_commit(&Bz.k_empty);
+        ++items_done;
       }
-      __syncthreads();
-      float acc[16];
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue (warps 2..9)
+    const int h = (warp - 2) >> 2;                    // accumulator half = warpgroup
+    const int row = 32 * (warp & 3) + lane;           // tile row = TMEM lane
+    const uint32_t acc = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + h * 256;
+    int tiles_done = 0;
+    for (int64_t it = blockIdx.x; it < n_items && !*fail; it += gridDim.x) {
+      const int c = (int)(it % p.max_chunks);
+      const int g = (int)((it / p.max_chunks) % p.Hkv);
+      const int b = (int)(it / ((int64_t)p.max_chunks * p.Hkv));
+      bool bad = false;
+      const int seq = clamp_seq(p.seq_lens, b, p.N, p.max_blocks, bad);
+      int t_lo = 0;
+      const int nt = item_tiles(p, b, c, seq, t_lo);
+      if (nt <= 0) continue;
+      const int nblk = (seq + 127) / 128;
+      for (int t = 0; t < nt; ++t, ++tiles_done) {
+        if (!sc_wait(&Bz.acc_full[h], tiles_done & 1, fail)) break;
+        tmem_fence_after();
+        const int i = (t_lo + t) * 128 + row;          // row within the request
+        const int qp = seq - p.N + i;                  // its query position
+        float best[2];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
-#pragma unroll 4
-      for (int c = 0; c < DI / 8; ++c) {
-        const float4 qa = *reinterpret_cast<const float4*>(&sq[rr][c * 8]);
-        const float4 qb = *reinterpret_cast<const float4*>(&sq[rr][c * 8 + 4]);
+        for (int s = 0; s < 2; ++s) {
+          float v[128];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(&sk[sub + 8 * m][c * 8]);
-          acc[m] = fmaf(qa.x, bf16_lo(kv.x), acc[m]);
-          acc[m] = fmaf(qa.y, bf16_hi(kv.x), acc[m]);
-          acc[m] = fmaf(qa.z, bf16_lo(kv.y), acc[m]);
-          acc[m] = fmaf(qa.w, bf16_hi(kv.y), acc[m]);
-          acc[m] = fmaf(qb.x, bf16_lo(kv.z), acc[m]);
-          acc[m] = fmaf(qb.y, bf16_hi(kv.z), acc[m]);
-          acc[m] = fmaf(qb.z, bf16_lo(kv.w), acc[m]);
-          acc[m] = fmaf(qb.w, bf16_hi(kv.w), acc[m]);
+          for (int x = 0; x < 4; ++x) tmem_ld32(acc + s * 128 + x * 32, v + x * 32);
+          tmem_wait_ld();
+          if (s == 1) {  // both blocks are in registers: hand the accumulator half back
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&Bz.acc_empty[h]);
+          }
+          const int j = c * kScoreChunk + 2 * h + s;
+          // causal mask: only the row's own block holds keys after the query
+          const int lim = qp - j * 128;                // last visible column
+          if (lim < 127) {
+#pragma unroll
+            for (int x = 0; x < 128; ++x)
+              if (x > lim) v[x] = -INFINITY;
+          }
+          float m8[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) m8[r] = v[r];
+#pragma unroll
+          for (int x = 8; x < 128; ++x) m8[x & 7] = fmaxf(m8[x & 7], v[x]);
+          best[s] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        }
+        if (i < p.N) {
+          const int64_t r = (int64_t)b * p.N + i;
+          float* dst = p.scores + (r * p.Hkv + g) * p.max_blocks;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const int j = c * kScoreChunk + 2 * h + s;
+            if (j < nblk && j * 128 <= qp) dst[j] = best[s];
+          }
         }
       }
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        if (j * 128 + sub + 8 * m <= qp) best = fmaxf(best, acc[m]);
     }
-    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
-    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
-    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 4));
-    if (sub == 0 && rr < nrows) {
-      const int64_t r = (int64_t)b * a.N + i0 + rr;
-      a.scores[(r * a.Hkv + g) * a.max_blocks + j] = best;
-    }
+  }
+  // ------------------------------------------------------------------ teardown
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(512)
+                 : "memory");
   }
 }
 
@@ -599,14 +785,34 @@ cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_score_rows(const ScoreArgs& a, cudaStream_t stream) {
-  const int tiles = (a.N + kRowTile - 1) / kRowTile;
-  dim3 grid((unsigned)(a.B * tiles), (unsigned)a.Hkv,
-            (unsigned)((a.max_blocks + kBlkChunk - 1) / kBlkChunk));
-  if (a.Di == 128)
-    score_rows_kernel<128><<<grid, 256, 0, stream>>>(a, tiles);
-  else
-    score_rows_kernel<64><<<grid, 256, 0, stream>>>(a, tiles);
-  return cudaGetLastError();
+  CUtensorMap qmap, kmap;
+  const uint64_t qdims[3] = {(uint64_t)a.Di, (uint64_t)a.Hkv, (uint64_t)a.B * a.N};
+  const uint64_t kdims[3] = {(uint64_t)a.Di, (uint64_t)a.Hkv, (uint64_t)a.num_pages * 128};
+  const uint64_t strides[2] = {(uint64_t)a.Di * 2, (uint64_t)a.Hkv * a.Di * 2};
+  const uint32_t box[3] = {64, 1, 128};
+  if (!encode_bf16_map(&qmap, a.q_idx, 3, qdims, strides, box, true) ||
+      !encode_bf16_map(&kmap, a.k_idx, 3, kdims, strides, box, true))
+    return cudaErrorInvalidValue;
+  ScoreTcParams p;
+  p.page_table = a.page_table;
+  p.seq_lens = a.seq_lens;
+  p.B = a.B;
+  p.N = a.N;
+  p.Hkv = a.Hkv;
+  p.max_blocks = a.max_blocks;
+  p.max_chunks = (a.max_blocks + kScoreChunk - 1) / kScoreChunk;
+  p.num_pages = a.num_pages;
+  p.scores = a.scores;
+  const int64_t items = (int64_t)a.B * a.Hkv * p.max_chunks;
+  const int grid = (int)(items < sm_count() ? items : sm_count());
+  auto launch = [&](auto kern, size_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kScThreads, smem, stream>>>(qmap, kmap, p);
+    return cudaGetLastError();
+  };
+  return a.Di == 128 ? launch(score_rows_tc_kernel<128>, ScoreTcLayout<128>::kSmem)
+                     : launch(score_rows_tc_kernel<64>, ScoreTcLayout<64>::kSmem);
 }
 
 cudaError_t launch_topk_rows(const ScoreArgs& a, cudaStream_t stream) {

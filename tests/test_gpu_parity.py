@@ -58,6 +58,9 @@ def test_score_topk_streaming_path(seq_lens, N, Hkv, Di, topk):
 @pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
     ([700], 300, 2, 64, 4),                         # prefill chunk, ragged row tile
     ([2048, 1500], 33, 4, 128, 5),                  # two requests, N just above the streaming cap
+    ([5000, 3000], 600, 2, 128, 8),                 # chunks after a prefix, several row tiles
+    ([1300], 1300, 4, 128, 16),                     # whole sequence is the chunk, ragged tiles
+    ([9000, 129, 4000], 129, 2, 64, 6),             # one request with seq == N, 4-block chunks
 ])
 def test_score_topk_row_path(seq_lens, N, Hkv, Di, topk):
     _score_case(seq_lens, N, Hkv, Di, topk, seed=7)
