@@ -423,7 +423,9 @@ def run_cfg5(args, local):
     msa.load(build_if_missing=True)
     pk = peaks()
     out = {}
-    w = workloads.cfg5_decode(dev, seed=5)
+    # --small (profiling captures only): one 131072-token request, an 8192-token chunk on a
+    # 131072-token prefix
+    w = workloads.cfg5_decode(dev, seed=5, **(dict(B=1, seq_len=131072) if args.small else {}))
     ws_ = msa.Workspace()
 
     def timed(fn, reps):
@@ -458,7 +460,7 @@ def run_cfg5(args, local):
                                "frac_hbm": round(kv_bytes / ms_d / 1e6 / pk["hbm_gbs"], 4)}
     del w, ids, fpt, lens
     torch.cuda.empty_cache()
-    w = workloads.cfg5_prefill(dev, seed=6)
+    w = workloads.cfg5_prefill(dev, seed=6, **(dict(T=8192, prefix=131072) if args.small else {}))
     T, S, P = w["T"], w["S"], w["P"]
     kidx_pages = w["k_idx"].view(P, 128, Hkv, Di)
     sl = torch.tensor([S], dtype=torch.int32, device=dev)

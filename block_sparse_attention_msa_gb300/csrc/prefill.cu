@@ -189,9 +189,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------------------ attention
-// One CTA per SM (tcgen05 path). Warp 0 produces (TMA), warp 1 owns tensor memory and issues
-// the MMAs, two softmax warpgroups (warps 4-7: even tiles, warps 8-11: odd tiles; one row per
-// thread) run softmax and the epilogue.
+// One CTA per SM (tcgen05 path). Warp 0 gathers the query rows (TMA), warp 2 loads the K/V
+// blocks (TMA), warp 1 owns tensor memory and issues the MMAs, two softmax warpgroups (warps
+// 4-7: even tiles, warps 8-11: odd tiles; one row per thread) run softmax and the epilogue.
 constexpr int kThreads = 384;
 constexpr int kRows = 128;                       // query-head rows per tile (MMA M)
 constexpr uint32_t kBox = 128 * 64 * 2;          // 128 rows x 64 channels bf16 = 16 KB
@@ -199,6 +199,7 @@ constexpr uint32_t kTileBytes = 2 * kBox;        // Q tile, P tile, K block or V
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/384
 constexpr int kChunk = 4;                        // consecutive tiles per CTA per round
+constexpr uint32_t kIssuerNap = 100;             // ns an idle MMA issuer blocks on a barrier
 
 // shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
 // query tiles hides the latency of the scattered row gathers; two K/V block buffers let the
@@ -223,6 +224,10 @@ struct PreKParams {
   const int4* desc;                // per-tile (list, first entry, valid queries)
   const int32_t* tile_offsets;
   int32_t Hkv, G, topk, nblk, qpt, nwin;
+  // 1: the query map is 5-D {64 channels, 8 heads, 2 channel halves, G/8, query-group} and one
+  // copy brings a query's G head rows as whole 8-row swizzle atoms (both channel halves, 2 KB
+  // per 8 heads); 0: two 3-D copies per query, one per channel half.
+  int32_t q_atoms;
   int64_t q_start;
   uint16_t* part_o;               // chunk-major [16][part_rows][8] bf16
   int64_t part_rows;               // T*Hkv*topk*G
@@ -233,6 +238,31 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Packed fp32 pair arithmetic (one instruction for two lanes of data) and a three-input max.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 ra, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
+      " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float b0, float b1) {
+  asm("{\n .reg .b64 rb, rd;\n mov.b64 rb, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
+      " mul.rn.f32x2 rd, rd, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(b0), "f"(b1));
 }
 
 // Tile descriptor: list gj = g*nblk + j, first entry of the tile, valid query slots.
@@ -322,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q = lane + 32 * r;
       e0[r] = q < d0.z ? p.entries[d0.y + q] : -1;
     }
-    int loaded_gj = -1, kv_loads = 0;
     for (int i = 0; i < n; ++i) {
       const int qs = i % kQStages;
       const int4 d = d0;
@@ -339,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i + 2 < n) d1 = load_desc(p, tile_of(i + 2));
       }
       if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
-      const int g = (int)(d.x / lists_per_group), j = d.x % p.nblk;
+      const int g = (int)(d.x / lists_per_group);
       uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
       if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
       __syncwarp();
@@ -348,102 +377,139 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = lane + 32 * r;
         if (q < d.z) {
           const int t = e[r] / p.topk;
-          tma_load_3d(qdst + q * p.G * 128, &qmap, &B.q_full[qs], 0, g * p.G, t);
-          tma_load_3d(qdst + kBox + q * p.G * 128, &qmap, &B.q_full[qs], 64, g * p.G, t);
+          if (p.q_atoms) {
+            tma_load_5d(qdst + q * p.G * 256, &qmap, &B.q_full[qs], 0, 0, 0, 0, t * p.Hkv + g);
+          } else {
+            tma_load_3d(qdst + q * p.G * 128, &qmap, &B.q_full[qs], 0, g * p.G, t);
+            tma_load_3d(qdst + kBox + q * p.G * 128, &qmap, &B.q_full[qs], 64, g * p.G, t);
+          }
         }
       }
-      if (d.x != loaded_gj) {
-        // K/V load number kv_loads goes to buffer kv_loads & 1, free once the last tile of
-        // load kv_loads - 2 has finished its O MMA
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ================================================================ K/V producer
+    // Walks the same tile sequence and loads the K and V block of every new list into the
+    // next of the two K/V buffers, as soon as that buffer's previous list has finished its
+    // last O MMA. Kept apart from the query gathers so that waiting for a buffer never
+    // delays the query rows of the tiles in between. Descriptors are read 32 at a time.
+    int loaded_gj = -1, kv_loads = 0;
+    for (int base = 0; base < n && !*fail; base += 32) {
+      const int mine = base + lane;
+      const int gj_l = mine < n ? load_desc(p, tile_of(mine)).x : -1;
+      const int cnt = n - base < 32 ? n - base : 32;
+      for (int t = 0; t < cnt; ++t) {
+        const int gj = __shfl_sync(0xffffffffu, gj_l, t);
+        if (gj == loaded_gj) continue;
         const int c = kv_loads & 1;
-        if (kv_loads >= 2 && !wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) break;
         if (lane == 0) {
-          uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
-          mbar_expect_tx(&B.kv_full[c], 4 * kBox);
-          const int tok = j * 128;
-          tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
-          tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
-          tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
-          tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
+          // load kv_loads goes to buffer kv_loads & 1, free once the last tile of load
+          // kv_loads - 2 has finished its O MMA
+          if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
+            const int g = (int)(gj / lists_per_group), j = gj % p.nblk;
+            uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
+            mbar_expect_tx(&B.kv_full[c], 4 * kBox);
+            const int tok = j * 128;
+            tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
+            tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
+            tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
+            tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
+          }
         }
+        if (__shfl_sync(0xffffffffu, (int)*fail, 0)) break;
         ++kv_loads;
-        loaded_gj = d.x;
+        loaded_gj = gj;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    // Event loop: issue O(oi) as soon as its P is in tensor memory, S(si) as soon as its
-    // queries and K/V block are loaded and O(si-2) (which reads P from S(si)'s columns) has
-    // completed; O first.
+    // Preferred order S(0), S(1), then O(k), S(k+2) for k = 0, 1, ...: S(k+2) writes the tensor
+    // memory that P(k) occupies, so it follows O(k). When the next S is waiting for its data
+    // while P of the next O is ready, the O goes first. An idle issuer blocks in hardware on
+    // the next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
+    // within a few hundred cycles. All state stays in registers.
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
       const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
-      int si = 0, oi = 0, kv_gj = -1, kv_loads = 0;
-      int gj_ring[2] = {-1, -1}, kvb_ring[2] = {0, 0};  // tiles with S issued, O not yet
+      int kv_gj = -1, kv_loads = 0;
+      // list and K/V buffer of the tile whose S is in tensor-memory buffer 0 / 1
+      int gj0 = -1, gj1 = -1, kvb0 = 0, kvb1 = 0;
       int next_gj = load_desc(p, tile_of(0)).x;
+      int after_gj = n > 1 ? load_desc(p, tile_of(1)).x : -2;
+      int si = 0, oi = 0;
       uint32_t idle = 0;
       while (oi < n && !*fail) {
-        bool progress = false;
-        // ---- O(oi)
+        // ---- S(si): needs O(si-2) issued and completed, its queries and its K/V block
+        if (si < n && oi >= si - 1) {
+          const int b = si & 1, qs = si % kQStages;
+          const bool kv_new = next_gj != kv_gj;
+          if ((!kv_new || mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
+              mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
+              (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
+            tmem_fence_after();
+            if (kv_new) {
+              ++kv_loads;
+              kv_gj = next_gj;
+            }
+            const int c = (kv_loads - 1) & 1;
+            const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
+            const uint32_t ka = sbase + kOffKV + c * 2 * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // query tile: per channel half, 8-row atoms 1 KB apart (two copies per query) or
+              // 2 KB apart with the halves interleaved (one copy per query)
+              const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
+                                              : (kk >> 2) * kBox + (kk & 3) * 32;
+              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+              umma_bf16(tmem + b * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
+                        umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+            }
+            umma_commit(&B.s_full[b]);
+            umma_commit(&B.q_empty[qs]);
+            if (b) {
+              gj1 = next_gj;
+              kvb1 = c;
+            } else {
+              gj0 = next_gj;
+              kvb0 = c;
+            }
+            ++si;
+            next_gj = after_gj;  // descriptors are read two tiles ahead
+            if (si + 1 < n) after_gj = load_desc(p, tile_of(si + 1)).x;
+            idle = 0;
+            continue;
+          }
+        }
+        // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
         if (oi < si) {
           const int b = oi & 1;
           if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
               (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
             tmem_fence_after();
-            const int c = kvb_ring[b];
+            const int c = b ? kvb1 : kvb0;
             const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
               umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
             }
             umma_commit(&B.o_full[b]);
-            const int gj_o = gj_ring[b];
-            const int gj_after = oi + 1 < si ? gj_ring[(oi + 1) & 1] : (oi + 1 < n ? next_gj : -2);
-            if (gj_after != gj_o) umma_commit(&B.kv_empty[c]);  // last tile on this K/V load
+            // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
+            // oi is the last one on this K/V load
+            const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
+            if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
             ++oi;
-            progress = true;
+            idle = 0;
+            continue;
           }
-        }
-        // ---- S(si)
-        if (si < n && si <= oi + 1) {
-          const int b = si & 1, qs = si % kQStages;
-          const int gj = next_gj;
-          bool kv_ok = gj == kv_gj;
-          if (!kv_ok && mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) {
-            ++kv_loads;  // the next K/V load (a new block) has landed
-            kv_gj = gj;
-            kv_ok = true;
-          }
-          if (kv_ok && mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
-              (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
-            tmem_fence_after();
-            const int c = (kv_loads - 1) & 1;
-            const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
-            const uint32_t ka = sbase + kOffKV + c * 2 * kTileBytes;
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-              umma_bf16(tmem + b * 128, umma_desc_sw128(qa + off, 16, 1024),
-                        umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
-            }
-            umma_commit(&B.s_full[b]);
-            umma_commit(&B.q_empty[qs]);
-            gj_ring[b] = gj;
-            kvb_ring[b] = c;
-            ++si;
-            if (si < n) next_gj = load_desc(p, tile_of(si)).x;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
+          mbar_try_wait_hint(&B.p_full[b], (oi >> 1) & 1, kIssuerNap);
         } else {
-          // back off: this thread shares its scheduler with two softmax warps
-          __nanosleep(64);
-          if (++idle > kWaitLimit) {
-            msa_record_error(kErrTimeout);
-            *fail = 1;
-          }
+          __nanosleep(32);
+        }
+        if (++idle > kWaitLimit) {
+          msa_record_error(kErrTimeout);
+          *fail = 1;
         }
       }
     }
@@ -488,19 +554,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 128; ++x)
           if (x > lim) v[x] = -INFINITY;
       }
-      float mx8[8];
+      // row max: three-input max over column pairs, four independent chains
+      float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int r = 0; r < 8; ++r) mx8[r] = v[r];
-#pragma unroll
-      for (int x = 8; x < 128; ++x) mx8[x & 7] = fmaxf(mx8[x & 7], v[x]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int x = 4; x < 128; x += 2) m4[(x >> 1) & 3] = max3(m4[(x >> 1) & 3], v[x], v[x + 1]);
+      const float mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
       const float mscaled = (mx == -INFINITY ? 0.f : mx) * kLog2e;
+      // p = 2^(s*log2e - max*log2e): the scaling in packed pairs, the exponent on the SFU
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int x = 0; x < 128; ++x) {
-        v[x] = ex2(fmaf(v[x], kLog2e, -mscaled));
-        l8[x & 7] += v[x];
+      for (int x = 0; x < 128; x += 2) {
+        fma2(v[x], v[x + 1], v[x], v[x + 1], kLog2e, kLog2e, -mscaled, -mscaled);
+        v[x] = ex2(v[x]);
+        v[x + 1] = ex2(v[x + 1]);
+        add2(l8[(x >> 1) & 3], l8[4 + ((x >> 1) & 3)], v[x], v[x + 1]);
       }
       // P row (bf16 pairs) into the first 64 columns of this tile's S buffer: the A operand
       // of the O MMA
@@ -534,10 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           uint4 u;
-          u.x = pack_bf16x2(v[c * 8 + 0] * inv, v[c * 8 + 1] * inv);
-          u.y = pack_bf16x2(v[c * 8 + 2] * inv, v[c * 8 + 3] * inv);
-          u.z = pack_bf16x2(v[c * 8 + 4] * inv, v[c * 8 + 5] * inv);
-          u.w = pack_bf16x2(v[c * 8 + 6] * inv, v[c * 8 + 7] * inv);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) mul2(v[c * 8 + e], v[c * 8 + e + 1], inv, inv);
+          u.x = pack_bf16x2(v[c * 8 + 0], v[c * 8 + 1]);
+          u.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
+          u.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
+          u.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
           dst[(int64_t)c * p.part_rows] = u;
         }
       }
@@ -601,13 +670,24 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
 
   CUtensorMap qmap, kmap, vmap;
+  // Query rows, preferably as one copy per query: dims {channel in half, head mod 8, half,
+  // head / 8, t*Hkv + g} (the half's stride is below the head's, so the box lands as
+  // [G/8][half][8 heads][64 channels]); otherwise two 3-D copies per query.
+  int32_t q_atoms = 0;
+  if (G % 8 == 0) {
+    const uint64_t q5dims[5] = {64, 8, 2, (uint64_t)G / 8, (uint64_t)a.T * a.Hkv};
+    const uint64_t q5strides[4] = {(uint64_t)a.D * 2, 128, (uint64_t)8 * a.D * 2,
+                                   (uint64_t)G * a.D * 2};
+    const uint32_t q5box[5] = {64, 8, 2, (uint32_t)G / 8, 1};
+    q_atoms = encode_bf16_map(&qmap, a.q, 5, q5dims, q5strides, q5box, true) ? 1 : 0;
+  }
   const uint64_t qdims[3] = {(uint64_t)a.D, (uint64_t)a.Hq, (uint64_t)a.T};
   const uint64_t qstrides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hq * a.D * 2};
   const uint32_t qbox[3] = {64, (uint32_t)G, 1};
   const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.Hkv, (uint64_t)a.S_kv};
   const uint64_t strides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hkv * a.D * 2};
   const uint32_t box[3] = {64, 1, 128};
-  if (!encode_bf16_map(&qmap, a.q, 3, qdims, qstrides, qbox, true) ||
+  if ((!q_atoms && !encode_bf16_map(&qmap, a.q, 3, qdims, qstrides, qbox, true)) ||
       !encode_bf16_map(&kmap, a.k, 3, dims, strides, box, true) ||
       !encode_bf16_map(&vmap, a.v, 3, dims, strides, box, true))
     return cudaErrorInvalidValue;
@@ -627,6 +707,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.nblk = a.nblk;
   p.qpt = qpt;
   p.nwin = nwin;
+  p.q_atoms = q_atoms;
   p.q_start = a.S_kv - a.T;
   p.part_o = part_o;
   p.part_rows = (int64_t)a.T * a.Hkv * a.topk * G;
