@@ -200,6 +200,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;              // S[2] at 0/128, O[2] at 256/384
 constexpr int kChunk = 4;                        // consecutive tiles per CTA per round
 constexpr uint32_t kIssuerNap = 100;             // ns an idle MMA issuer blocks on a barrier
+constexpr int kLaunchRegs = 168;                 // registers per thread at launch (384 threads)
+constexpr int kRegsLow = 88;                     // warps 0-3 after the split
+constexpr int kRegsHigh = 208;                   // softmax warpgroups after the split
 
 // shared-memory carve-up (offsets from a 1024-aligned base): a 3-deep ring of gathered
 // query tiles hides the latency of the scattered row gathers; two K/V block buffers let the
@@ -333,188 +336,196 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = B.tmem_base;
   const uint32_t sbase = smem_u32(smem);
 
-  if (warp == 0) {
-    // ================================================================ producer (whole warp)
-    // Each lane gathers the query rows of up to kMaxQPerLane query slots of the tile (lane,
-    // lane+32, ...). Descriptors are prefetched two tiles ahead and entries one tile ahead so
-    // that no global-memory latency sits between two tiles' copies.
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
-    constexpr int kMaxQPerLane = 4;  // qpt = 128/G <= 128
-    int4 d0 = load_desc(p, tile_of(0));
-    int4 d1 = n > 1 ? load_desc(p, tile_of(1)) : d0;
-    int32_t e0[kMaxQPerLane];
-#pragma unroll
-    for (int r = 0; r < kMaxQPerLane; ++r) {
-      const int q = lane + 32 * r;
-      e0[r] = q < d0.z ? p.entries[d0.y + q] : -1;
-    }
-    for (int i = 0; i < n; ++i) {
-      const int qs = i % kQStages;
-      const int4 d = d0;
-      int32_t e[kMaxQPerLane];
-#pragma unroll
-      for (int r = 0; r < kMaxQPerLane; ++r) e[r] = e0[r];
-      if (i + 1 < n) {  // prefetch: entries of tile i+1, descriptor of tile i+2
-#pragma unroll
-        for (int r = 0; r < kMaxQPerLane; ++r) {
-          const int q = lane + 32 * r;
-          e0[r] = q < d1.z ? p.entries[d1.y + q] : -1;
-        }
-        d0 = d1;
-        if (i + 2 < n) d1 = load_desc(p, tile_of(i + 2));
+  // Register split: the producer / issuer warpgroup needs few registers, each softmax thread
+  // holds a 128-column row. The launcher checks that the kernel was built with kLaunchRegs
+  // registers per thread, so the split adds up to exactly what the launch allocated.
+  static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+      // ================================================================ producer (whole warp)
+      // Each lane gathers the query rows of up to kMaxQPerLane query slots of the tile (lane,
+      // lane+32, ...). Descriptors are prefetched two tiles ahead and entries one tile ahead so
+      // that no global-memory latency sits between two tiles' copies.
+      if (lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
       }
-      if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
-      const int g = (int)(d.x / lists_per_group);
-      uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
-      if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
-      __syncwarp();
-#pragma unroll
+      constexpr int kMaxQPerLane = 4;  // qpt = 128/G <= 128
+      int4 d0 = load_desc(p, tile_of(0));
+      int4 d1 = n > 1 ? load_desc(p, tile_of(1)) : d0;
+      int32_t e0[kMaxQPerLane];
+  #pragma unroll
       for (int r = 0; r < kMaxQPerLane; ++r) {
         const int q = lane + 32 * r;
-        if (q < d.z) {
-          const int t = e[r] / p.topk;
-          if (p.q_atoms) {
-            tma_load_5d(qdst + q * p.G * 256, &qmap, &B.q_full[qs], 0, 0, 0, 0, t * p.Hkv + g);
-          } else {
-            tma_load_3d(qdst + q * p.G * 128, &qmap, &B.q_full[qs], 0, g * p.G, t);
-            tma_load_3d(qdst + kBox + q * p.G * 128, &qmap, &B.q_full[qs], 64, g * p.G, t);
-          }
-        }
+        e0[r] = q < d0.z ? p.entries[d0.y + q] : -1;
       }
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ================================================================ K/V producer
-    // Walks the same tile sequence and loads the K and V block of every new list into the
-    // next of the two K/V buffers, as soon as that buffer's previous list has finished its
-    // last O MMA. Kept apart from the query gathers so that waiting for a buffer never
-    // delays the query rows of the tiles in between. Descriptors are read 32 at a time.
-    int loaded_gj = -1, kv_loads = 0;
-    for (int base = 0; base < n && !*fail; base += 32) {
-      const int mine = base + lane;
-      const int gj_l = mine < n ? load_desc(p, tile_of(mine)).x : -1;
-      const int cnt = n - base < 32 ? n - base : 32;
-      for (int t = 0; t < cnt; ++t) {
-        const int gj = __shfl_sync(0xffffffffu, gj_l, t);
-        if (gj == loaded_gj) continue;
-        const int c = kv_loads & 1;
-        if (lane == 0) {
-          // load kv_loads goes to buffer kv_loads & 1, free once the last tile of load
-          // kv_loads - 2 has finished its O MMA
-          if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
-            const int g = (int)(gj / lists_per_group), j = gj % p.nblk;
-            uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
-            mbar_expect_tx(&B.kv_full[c], 4 * kBox);
-            const int tok = j * 128;
-            tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
-            tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
-            tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
-            tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
+      for (int i = 0; i < n; ++i) {
+        const int qs = i % kQStages;
+        const int4 d = d0;
+        int32_t e[kMaxQPerLane];
+  #pragma unroll
+        for (int r = 0; r < kMaxQPerLane; ++r) e[r] = e0[r];
+        if (i + 1 < n) {  // prefetch: entries of tile i+1, descriptor of tile i+2
+  #pragma unroll
+          for (int r = 0; r < kMaxQPerLane; ++r) {
+            const int q = lane + 32 * r;
+            e0[r] = q < d1.z ? p.entries[d1.y + q] : -1;
           }
+          d0 = d1;
+          if (i + 2 < n) d1 = load_desc(p, tile_of(i + 2));
         }
-        if (__shfl_sync(0xffffffffu, (int)*fail, 0)) break;
-        ++kv_loads;
-        loaded_gj = gj;
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    // Preferred order S(0), S(1), then O(k), S(k+2) for k = 0, 1, ...: S(k+2) writes the tensor
-    // memory that P(k) occupies, so it follows O(k). When the next S is waiting for its data
-    // while P of the next O is ready, the O goes first. An idle issuer blocks in hardware on
-    // the next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
-    // within a few hundred cycles. All state stays in registers.
-    if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
-      const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
-      int kv_gj = -1, kv_loads = 0;
-      // list and K/V buffer of the tile whose S is in tensor-memory buffer 0 / 1
-      int gj0 = -1, gj1 = -1, kvb0 = 0, kvb1 = 0;
-      int next_gj = load_desc(p, tile_of(0)).x;
-      int after_gj = n > 1 ? load_desc(p, tile_of(1)).x : -2;
-      int si = 0, oi = 0;
-      uint32_t idle = 0;
-      while (oi < n && !*fail) {
-        // ---- S(si): needs O(si-2) issued and completed, its queries and its K/V block
-        if (si < n && oi >= si - 1) {
-          const int b = si & 1, qs = si % kQStages;
-          const bool kv_new = next_gj != kv_gj;
-          if ((!kv_new || mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
-              mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
-              (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
-            tmem_fence_after();
-            if (kv_new) {
-              ++kv_loads;
-              kv_gj = next_gj;
-            }
-            const int c = (kv_loads - 1) & 1;
-            const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
-            const uint32_t ka = sbase + kOffKV + c * 2 * kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              // query tile: per channel half, 8-row atoms 1 KB apart (two copies per query) or
-              // 2 KB apart with the halves interleaved (one copy per query)
-              const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
-                                              : (kk >> 2) * kBox + (kk & 3) * 32;
-              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-              umma_bf16(tmem + b * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
-                        umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
-            }
-            umma_commit(&B.s_full[b]);
-            umma_commit(&B.q_empty[qs]);
-            if (b) {
-              gj1 = next_gj;
-              kvb1 = c;
+        if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
+        const int g = (int)(d.x / lists_per_group);
+        uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
+        if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
+        __syncwarp();
+  #pragma unroll
+        for (int r = 0; r < kMaxQPerLane; ++r) {
+          const int q = lane + 32 * r;
+          if (q < d.z) {
+            const int t = e[r] / p.topk;
+            if (p.q_atoms) {
+              tma_load_5d(qdst + q * p.G * 256, &qmap, &B.q_full[qs], 0, 0, 0, 0, t * p.Hkv + g);
             } else {
-              gj0 = next_gj;
-              kvb0 = c;
+              tma_load_3d(qdst + q * p.G * 128, &qmap, &B.q_full[qs], 0, g * p.G, t);
+              tma_load_3d(qdst + kBox + q * p.G * 128, &qmap, &B.q_full[qs], 64, g * p.G, t);
             }
-            ++si;
-            next_gj = after_gj;  // descriptors are read two tiles ahead
-            if (si + 1 < n) after_gj = load_desc(p, tile_of(si + 1)).x;
-            idle = 0;
-            continue;
           }
-        }
-        // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
-        if (oi < si) {
-          const int b = oi & 1;
-          if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
-              (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
-            tmem_fence_after();
-            const int c = b ? kvb1 : kvb0;
-            const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-              umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
-            }
-            umma_commit(&B.o_full[b]);
-            // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
-            // oi is the last one on this K/V load
-            const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
-            if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
-            ++oi;
-            idle = 0;
-            continue;
-          }
-          mbar_try_wait_hint(&B.p_full[b], (oi >> 1) & 1, kIssuerNap);
-        } else {
-          __nanosleep(32);
-        }
-        if (++idle > kWaitLimit) {
-          msa_record_error(kErrTimeout);
-          *fail = 1;
         }
       }
+      __syncwarp();
+    } else if (warp == 2) {
+      // ================================================================ K/V producer
+      // Walks the same tile sequence and loads the K and V block of every new list into the
+      // next of the two K/V buffers, as soon as that buffer's previous list has finished its
+      // last O MMA. Kept apart from the query gathers so that waiting for a buffer never
+      // delays the query rows of the tiles in between. Descriptors are read 32 at a time.
+      int loaded_gj = -1, kv_loads = 0;
+      for (int base = 0; base < n && !*fail; base += 32) {
+        const int mine = base + lane;
+        const int gj_l = mine < n ? load_desc(p, tile_of(mine)).x : -1;
+        const int cnt = n - base < 32 ? n - base : 32;
+        for (int t = 0; t < cnt; ++t) {
+          const int gj = __shfl_sync(0xffffffffu, gj_l, t);
+          if (gj == loaded_gj) continue;
+          const int c = kv_loads & 1;
+          if (lane == 0) {
+            // load kv_loads goes to buffer kv_loads & 1, free once the last tile of load
+            // kv_loads - 2 has finished its O MMA
+            if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
+              const int g = (int)(gj / lists_per_group), j = gj % p.nblk;
+              uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
+              mbar_expect_tx(&B.kv_full[c], 4 * kBox);
+              const int tok = j * 128;
+              tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
+              tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
+              tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
+              tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
+            }
+          }
+          if (__shfl_sync(0xffffffffu, (int)*fail, 0)) break;
+          ++kv_loads;
+          loaded_gj = gj;
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ================================================================ MMA issuer
+      // Preferred order S(0), S(1), then O(k), S(k+2) for k = 0, 1, ...: S(k+2) writes the tensor
+      // memory that P(k) occupies, so it follows O(k). When the next S is waiting for its data
+      // while P of the next O is ready, the O goes first. An idle issuer blocks in hardware on
+      // the next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
+      // within a few hundred cycles. All state stays in registers.
+      if (lane == 0) {
+        const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
+        const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
+        int kv_gj = -1, kv_loads = 0;
+        // list and K/V buffer of the tile whose S is in tensor-memory buffer 0 / 1
+        int gj0 = -1, gj1 = -1, kvb0 = 0, kvb1 = 0;
+        int next_gj = load_desc(p, tile_of(0)).x;
+        int after_gj = n > 1 ? load_desc(p, tile_of(1)).x : -2;
+        int si = 0, oi = 0;
+        uint32_t idle = 0;
+        while (oi < n && !*fail) {
+          // ---- S(si): needs O(si-2) issued and completed, its queries and its K/V block
+          if (si < n && oi >= si - 1) {
+            const int b = si & 1, qs = si % kQStages;
+            const bool kv_new = next_gj != kv_gj;
+            if ((!kv_new || mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
+                mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
+                (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
+              tmem_fence_after();
+              if (kv_new) {
+                ++kv_loads;
+                kv_gj = next_gj;
+              }
+              const int c = (kv_loads - 1) & 1;
+              const uint32_t qa = sbase + kOffQ + qs * kTileBytes;
+              const uint32_t ka = sbase + kOffKV + c * 2 * kTileBytes;
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                // query tile: per channel half, 8-row atoms 1 KB apart (two copies per query) or
+                // 2 KB apart with the halves interleaved (one copy per query)
+                const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
+                                                : (kk >> 2) * kBox + (kk & 3) * 32;
+                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                umma_bf16(tmem + b * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
+                          umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+              }
+              umma_commit(&B.s_full[b]);
+              umma_commit(&B.q_empty[qs]);
+              if (b) {
+                gj1 = next_gj;
+                kvb1 = c;
+              } else {
+                gj0 = next_gj;
+                kvb0 = c;
+              }
+              ++si;
+              next_gj = after_gj;  // descriptors are read two tiles ahead
+              if (si + 1 < n) after_gj = load_desc(p, tile_of(si + 1)).x;
+              idle = 0;
+              continue;
+            }
+          }
+          // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
+          if (oi < si) {
+            const int b = oi & 1;
+            if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
+                (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
+              tmem_fence_after();
+              const int c = b ? kvb1 : kvb0;
+              const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
+                umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
+              }
+              umma_commit(&B.o_full[b]);
+              // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
+              // oi is the last one on this K/V load
+              const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
+              if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
+              ++oi;
+              idle = 0;
+              continue;
+            }
+            mbar_try_wait_hint(&B.p_full[b], (oi >> 1) & 1, kIssuerNap);
+          } else {
+            __nanosleep(32);
+          }
+          if (++idle > kWaitLimit) {
+            msa_record_error(kErrTimeout);
+            *fail = 1;
+          }
+        }
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ================================================================ softmax + epilogue
     // Warpgroup wg handles tiles k = wg, wg+2, ... with S[wg], P[wg], O[wg].
     const int wg = (warp - 4) >> 2;
@@ -715,6 +726,11 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   e = cudaFuncSetAttribute(prefill_block_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes);
   if (e != cudaSuccess) return e;
+  // the in-kernel register split assumes exactly kLaunchRegs registers per thread at launch
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_block_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   prefill_block_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
