@@ -675,8 +675,9 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   uint16_t* part_o = reinterpret_cast<uint16_t*>(a.workspace + W.part_o);
   float* part_lse = reinterpret_cast<float*>(a.workspace + W.part_lse);
   int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
-  const int32_t nwin = prefill_nwin(a.T);
-  cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, kPrefillWindow, qpt,
+  const int32_t win = prefill_window(a.T, a.nblk, a.topk);
+  const int32_t nwin = prefill_nwin(a.T, a.nblk, a.topk);
+  cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, win, qpt,
                                 offsets, entries, counts, group_base, tile_offsets, stream);
   if (e != cudaSuccess) return e;
 
