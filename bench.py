@@ -25,6 +25,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -62,7 +63,9 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms; only the lines that arrive
+    between entering and leaving the `with` block (the timed region) are kept. Entering waits
+    for nvidia-smi's first line so that sampling is running when the region starts."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -71,26 +74,43 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
+        self.out = ""
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        t0 = time.monotonic()
+        while not self.lines and time.monotonic() - t0 < 5.0:
+            time.sleep(0.01)
+        self.t_start = time.monotonic()
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                self.out, _ = self.proc.communicate()
+        t_end = time.monotonic()
+        if self.proc is None:
+            return
+        time.sleep(0.15)  # a sample taken just before the end may still be in flight
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.thread.join(timeout=5)
+        self.out = "".join(l for t, l in list(self.lines) if self.t_start <= t <= t_end + 0.1)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -146,6 +166,9 @@ def build_workloads(dev, seed_offset: int, small: bool = False):
     keys3 = visible_keys(c3["block_ids"], q_pos3)                 # [T, Hkv]
     G3 = c3["Hq"] // c3["Hkv"]
     c3["flops"] = 4 * c3["D"] * G3 * int(keys3.sum().item())
+    # bf16 partial rows (G per selection, D channels) written once and read once, + fp32 LSE
+    nsel3 = int((c3["block_ids"] >= 0).sum().item())
+    c3["partial_bytes"] = nsel3 * G3 * (2 * c3["D"] * 2 + 4 * 2)
     del G4
     return c2, c4, c3
 
@@ -285,7 +308,12 @@ def run_ours(args, ws, rank, local):
                            "attention_merge_frac_bf16": round(attn_tflops / pk["bf16_tflops_sustained"], 4),
                            "bucket_ms": round(sub["bucket_ms"], 4),
                            "flops": c3["flops"],
-                           "traffic": recorded_traffic("prefill_partials_kernel", src_hash("prefill.cu"))},
+                           # block-major design: every (query, block) selection writes a bf16
+                           # partial of G rows that the merge reads back; that traffic alone
+                           # takes partials_floor_ms at the measured HBM bandwidth
+                           "partials_bytes": c3["partial_bytes"],
+                           "partials_floor_ms": round(c3["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
+                           "traffic": recorded_traffic("prefill_block_tc_kernel", src_hash("prefill.cu"))},
     }
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
@@ -517,7 +545,7 @@ def run_reference(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
