@@ -325,10 +325,11 @@ def run_ours(args, ws, rank, local):
                                "block-major sparse prefill (32768 tokens)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
-        # kernels of this library per step: scorer (1); page table, decode, merge (3); bucket
-        # count, two scans, scatter, tile descriptors, attention, merge (7). Memsets not counted.
+        # kernels of this library per step: scorer (1); page table, decode, merge (3); dense
+        # selection, bucket count, two scans, scatter, tile descriptors, block-major attention,
+        # query-major attention, merge (9). Memsets not counted.
         "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
-                                      + ("prefill" in run) * 7),
+                                      + ("prefill" in run) * 9),
         "clocks": clk.summary(), "device_error_word": err,
     }
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):

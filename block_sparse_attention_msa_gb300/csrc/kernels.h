@@ -60,16 +60,27 @@ cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* 
                              uint16_t* o, float* lse, cudaStream_t stream);
 
 // Prefill merge of chunk-major partials part_o[16][U*S*G][8] bf16 (row = (u*S+s)*G+e); a
-// partial s of unit u is skipped when ids[u*S+s] < 0 (never written). G in {1,2,4,8,16}.
+// partial s of unit u is skipped when ids[u*S+s] < 0 (never written). Optionally one more
+// partial per (unit, head): dense_o chunk-major [16][U*G][8], dense_lse [U*G] (-inf = none).
+// G in {1,2,4,8,16}.
 cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
-                                     const int32_t* ids, int64_t U, int32_t S, int32_t G,
+                                     const int32_t* ids, const void* dense_o,
+                                     const float* dense_lse, int64_t U, int32_t S, int32_t G,
                                      uint16_t* o, float* lse, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill
 // Workspace carve-up shared by the C ABI (size query) and the launcher. Offsets in bytes,
 // each 256-byte aligned.
+// Query-major part (G in {8, 16}): pairs of 128/G-query tiles, at most kMaxDense shared blocks each.
+constexpr int kMaxDense = 64;
+inline bool prefill_hybrid(int32_t G) { return G == 8 || G == 16; }
+inline int64_t prefill_pairs(int64_t T, int32_t Hkv, int32_t G) {
+  const int64_t q2 = 2 * (128 / G);
+  return (int64_t)Hkv * ((T + q2 - 1) / q2);
+}
 struct PrefillWorkspace {
-  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc, total;
+  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc;
+  size_t residual, dcnt, dblk, dmask, dense_o, dense_lse, total;  // query-major part (G 8, 16)
 };
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 // Prefill work lists are per (group, query window, KV block): queries are cut into windows so
@@ -104,10 +115,38 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
     w.part_lse = off;   off = ws_align(off + 4 * sel * G);
     // one 16-byte descriptor per work tile of 128/G queries: at most sel/(128/G) + lists
     w.tile_desc = off;  off = ws_align(off + 16 * (sel * G / 128 + lists + 1));
+    if (prefill_hybrid(G)) {
+      const size_t pairs = (size_t)prefill_pairs(T, Hkv, G);
+      const size_t rows = (size_t)T * Hkv * G;
+      w.residual = off;   off = ws_align(off + 4 * sel);
+      w.dcnt = off;       off = ws_align(off + 4 * pairs);
+      w.dblk = off;       off = ws_align(off + 4 * pairs * kMaxDense);
+      w.dmask = off;      off = ws_align(off + 4 * pairs * kMaxDense);
+      w.dense_o = off;    off = ws_align(off + 2 * rows * 128);
+      w.dense_lse = off;  off = ws_align(off + 4 * rows);
+    }
   }
   w.total = off;
   return w;
 }
+// Query-major part of the prefill (G in {8, 16}): per pair of 128/G-query tiles, the blocks
+// chosen by at least 3/8 of the pair's queries (ascending, at most kMaxDense) with a bit mask of
+// the queries that chose each; the residual selections go to the block-major pass.
+struct DenseWorkspace {
+  int32_t* residual;   // [T, Hkv, k]
+  int32_t* dcnt;       // [pairs]
+  int32_t* dblk;       // [pairs, kMaxDense]
+  uint32_t* dmask;     // [pairs, kMaxDense]
+  uint16_t* part_o;    // chunk-major [16][T*Hkv*G][8] bf16
+  float* part_lse;     // [T*Hkv*G]
+};
+cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t G,
+                                int32_t topk, const DenseWorkspace& w, cudaStream_t stream);
+cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
+                                   int64_t S_kv, int32_t Hkv, int32_t G, const DenseWorkspace& w,
+                                   cudaStream_t stream);
+
 // (a) bucketing; tiles of `qpt` queries are laid out for the attention kernel.
 // List of selection (t, slot) of group g: ((g * nwin + t / win) * nblk + j); the per-list
 // offsets are relative to their (group, window) segment, segments in (g, w) order.

@@ -17,6 +17,7 @@ cudaError_t msa_read_error_score(uint32_t* w);
 cudaError_t msa_read_error_ptm(uint32_t* w);
 cudaError_t msa_read_error_dec(uint32_t* w);
 cudaError_t msa_read_error_pre(uint32_t* w);
+cudaError_t msa_read_error_dense(uint32_t* w);
 
 namespace {
 
@@ -350,7 +351,8 @@ int msa_device_error(uint32_t* word) {
   if (e != cudaSuccess) return cuda_status(e, "msa_device_error");
   uint32_t all = 0, w = 0;
   cudaError_t (*readers[])(uint32_t*) = {msa_read_error_score, msa_read_error_ptm,
-                                         msa_read_error_dec, msa_read_error_pre};
+                                         msa_read_error_dec, msa_read_error_pre,
+                                         msa_read_error_dense};
   for (auto rd : readers) {
     w = 0;
     e = rd(&w);

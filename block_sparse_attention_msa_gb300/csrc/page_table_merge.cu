@@ -162,6 +162,7 @@ template <int G>
 __global__ void __launch_bounds__(256)
     lse_merge_chunked_kernel(const uint4* __restrict__ part_o, int64_t part_rows,
                              const float* __restrict__ lse_parts, const int32_t* __restrict__ ids,
+                             const uint4* __restrict__ dense_o, const float* __restrict__ dense_lse,
                              int64_t U, int32_t S, uint16_t* __restrict__ o, float* __restrict__ lse) {
   constexpr int R = (G * 16 + 31) / 32;  // chunk slots per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -173,6 +174,9 @@ __global__ void __launch_bounds__(256)
     if (ids[u * S + s] < 0) continue;
     m = fmaxf(m, lse_parts[(u * S + s) * G + e]);
   }
+  // the query-major partial (one per unit and head), when the prefill has one
+  const float ld = dense_lse ? dense_lse[u * G + e] : -INFINITY;
+  m = fmaxf(m, ld);
   float acc[R][8];
 #pragma unroll
   for (int r = 0; r < R; ++r)
@@ -204,6 +208,26 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
+  if (m != -INFINITY && ld != -INFINITY) {
+    const float w = __expf(ld - m);
+    total += w;
+    const int64_t drows = U * G;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int idx = lane + 32 * r;
+      if (idx < G * 16) {
+        const uint4 v = __ldcs(dense_o + (int64_t)(idx / G) * drows + u * G + e);
+        acc[r][0] = fmaf(w, bf16_lo(v.x), acc[r][0]);
+        acc[r][1] = fmaf(w, bf16_hi(v.x), acc[r][1]);
+        acc[r][2] = fmaf(w, bf16_lo(v.y), acc[r][2]);
+        acc[r][3] = fmaf(w, bf16_hi(v.y), acc[r][3]);
+        acc[r][4] = fmaf(w, bf16_lo(v.z), acc[r][4]);
+        acc[r][5] = fmaf(w, bf16_hi(v.z), acc[r][5]);
+        acc[r][6] = fmaf(w, bf16_lo(v.w), acc[r][6]);
+        acc[r][7] = fmaf(w, bf16_hi(v.w), acc[r][7]);
+      }
+    }
+  }
   const float inv = total > 0.f ? 1.0f / total : 0.f;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -223,17 +247,19 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
-                                     const int32_t* ids, int64_t U, int32_t S, int32_t G,
+                                     const int32_t* ids, const void* dense_o,
+                                     const float* dense_lse, int64_t U, int32_t S, int32_t G,
                                      uint16_t* o, float* lse, cudaStream_t stream) {
   const unsigned grid = (unsigned)((U + 7) / 8);
   const int64_t rows = U * S * G;
   const uint4* po = reinterpret_cast<const uint4*>(part_o);
+  const uint4* pd = reinterpret_cast<const uint4*>(dense_o);
   switch (G) {
-    case 1: lse_merge_chunked_kernel<1><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
-    case 2: lse_merge_chunked_kernel<2><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
-    case 4: lse_merge_chunked_kernel<4><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
-    case 8: lse_merge_chunked_kernel<8><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
-    case 16: lse_merge_chunked_kernel<16><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, U, S, o, lse); break;
+    case 1: lse_merge_chunked_kernel<1><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 2: lse_merge_chunked_kernel<2><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 4: lse_merge_chunked_kernel<4><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 8: lse_merge_chunked_kernel<8><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 16: lse_merge_chunked_kernel<16><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

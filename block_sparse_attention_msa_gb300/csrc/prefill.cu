@@ -9,24 +9,23 @@
 // reduction rescales and sums the partials of the selected blocks.
 //
 // GB300 design.
-//  (a) Bucketing inverts block_ids [T, Hkv, k] into per-(group, block) lists of
-//      (query, slot) entries: a count pass (shared atomics would not help: the lists are
-//      global), one single-CTA scan that also lays out fixed-size work tiles, and a scatter.
-//  (b) Work tile = (group g, block j, up to 128/G queries from the list) = 128 query-head
-//      rows. A persistent grid of one CTA per SM walks a contiguous range of the global tile
-//      list, so consecutive tiles of a CTA share (g, j): the K/V block (64 KB, loaded with
-//      two 3-D TMA boxes per tensor straight out of [S_kv, Hkv, D]) stays in shared memory
-//      across them, while the gathered query rows of the next tile stream in with cp.async
-//      behind the current tile's math. Each of 8 warps owns 16 rows (bf16 MMA, fp32
-//      accumulate): S = Q K^T over the 128 keys, causal mask, softmax, O = P V, and writes a
-//      bf16 partial O and its fp32 LSE per (query, group, slot) and head.
-//  (c) The LSE merge (page_table_merge.cu) reduces the <= k partials of each (query, head).
+//  (a) Bucketing inverts block_ids [T, Hkv, k] into lists of (query, slot) entries per
+//      (group, query window, block): a count pass, a scan per (group, window) segment, a scan
+//      over segments, a scatter, then one 16-byte descriptor per work tile.
+//  (b) Work tile = (group g, block j, up to 128/G queries of the list) = 128 query-head rows,
+//      on tcgen05: S = Q K^T and O = P V with accumulators in tensor memory, query rows
+//      gathered by TMA, the K/V block loaded once per list; one bf16 partial O and its fp32
+//      LSE per (query, group, slot) and head (see the attention section below).
+//  (c) The LSE merge (page_table_merge.cu) reduces the partials of each (query, head).
+// With G in {8, 16}, the slots that many queries of a 2*128/G-query pair share are taken out
+// first and computed query-major (prefill_dense.cu); (a)-(b) then run on the remainder.
 #include <algorithm>
 #include <climits>
 
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "softmax_math.cuh"
 
 MSA_DEFINE_ERROR_WORD(pre)
 
@@ -236,37 +235,6 @@ struct PreKParams {
   int64_t part_rows;               // T*Hkv*topk*G
   float* part_lse;
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// Packed fp32 pair arithmetic (one instruction for two lanes of data) and a three-input max.
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                     float c0, float c1) {
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
-  asm("{\n .reg .b64 ra, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
-      " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1));
-}
-__device__ __forceinline__ void mul2(float& d0, float& d1, float b0, float b1) {
-  asm("{\n .reg .b64 rb, rd;\n mov.b64 rb, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
-      " mul.rn.f32x2 rd, rd, rb;\n mov.b64 {%0, %1}, rd;\n}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(b0), "f"(b1));
-}
 
 // Tile descriptor: list gj = g*nblk + j, first entry of the tile, valid query slots.
 __device__ __forceinline__ int4 load_desc(const PreKParams& p, int64_t tile) {
@@ -677,7 +645,24 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
   const int32_t win = prefill_window(a.T, a.nblk, a.topk);
   const int32_t nwin = prefill_nwin(a.T, a.nblk, a.topk);
-  cudaError_t e = launch_bucket(a.block_ids, a.T, a.Hkv, a.topk, a.nblk, win, qpt,
+  // G 8 / 16: the slots shared by many queries of a query pair are computed query-major; the
+  // block-major pass and the merge's slot skipping then use the residual selections
+  const bool hybrid = prefill_hybrid(G);
+  DenseWorkspace dw{};
+  const int32_t* ids = a.block_ids;
+  cudaError_t e = cudaSuccess;
+  if (hybrid) {
+    dw.residual = reinterpret_cast<int32_t*>(a.workspace + W.residual);
+    dw.dcnt = reinterpret_cast<int32_t*>(a.workspace + W.dcnt);
+    dw.dblk = reinterpret_cast<int32_t*>(a.workspace + W.dblk);
+    dw.dmask = reinterpret_cast<uint32_t*>(a.workspace + W.dmask);
+    dw.part_o = reinterpret_cast<uint16_t*>(a.workspace + W.dense_o);
+    dw.part_lse = reinterpret_cast<float*>(a.workspace + W.dense_lse);
+    e = launch_dense_select(a.block_ids, a.T, a.Hkv, G, a.topk, dw, stream);
+    if (e != cudaSuccess) return e;
+    ids = dw.residual;
+  }
+  e = launch_bucket(ids, a.T, a.Hkv, a.topk, a.nblk, win, qpt,
                                 offsets, entries, counts, group_base, tile_offsets, stream);
   if (e != cudaSuccess) return e;
 
@@ -735,7 +720,12 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   prefill_block_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_lse_merge_chunked(part_o, part_lse, a.block_ids, (int64_t)a.T * a.Hkv, a.topk, G,
+  if (hybrid) {
+    e = launch_dense_attention(qmap, kmap, vmap, q_atoms, a.T, a.S_kv, a.Hkv, G, dw, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_lse_merge_chunked(part_o, part_lse, ids, hybrid ? dw.part_o : nullptr,
+                                  hybrid ? dw.part_lse : nullptr, (int64_t)a.T * a.Hkv, a.topk, G,
                                   a.o, a.lse, stream);
 }
 

@@ -1,0 +1,600 @@
+// Query-major part of the sparse prefill: the KV blocks that many queries of a query pair
+// share are computed with the queries as the outer loop, the scattered remainder stays
+// block-major (prefill.cu).
+//
+// Together AI MiniMax-M3 serving article, section "KV-block-major sparse attention reduces
+// redundant KV movement": the block-major remap exists because queries that chose the same
+// KV block would otherwise each move it from HBM; its cost is one partial output per
+// selection and a Log-Sum-Exp reduction over them. Where neighbouring queries choose the
+// same blocks (the sink, the local block, a shared set), a query-major pass moves each such
+// block once for all of them as well, and accumulates their output across blocks without
+// partials. The combination is exact: every selection is computed once, by one of the two
+// passes, and the merge (row a7) combines the query-major partial with the block-major ones.
+//
+// GB300 design.
+//  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G consecutive
+//      queries of one group): sorts the pair's (block, query, slot) selections, keeps the
+//      blocks chosen by at least 3/8 of the pair's queries (at most kMaxDense, ascending) with
+//      a bit mask of the queries that chose each, and writes the residual selections (the
+//      dense ones replaced by -1) for the block-major pass.
+//  (b) prefill_dense_tc_kernel, one persistent CTA per SM over the pairs: the two tiles of a
+//      pair share each K/V block load; per block S = Q K^T and O += P V run on tcgen05 with
+//      S, P and O in tensor memory; one softmax warpgroup per tile keeps a running row max and
+//      sum (rows of queries that did not choose the block get P = 0; O and the sum are
+//      rescaled only when the max grows by more than 2^8), and writes one bf16 partial and its
+//      LSE per (query, head) after the pair's last block.
+#include <climits>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "kernels.h"
+#include "softmax_math.cuh"
+
+MSA_DEFINE_ERROR_WORD(dense)
+
+namespace msa {
+
+namespace {
+
+// ------------------------------------------------------------------------------ selection
+constexpr int kSelThreads = 256;
+constexpr int kSelKeys = 2048;  // 2*qpt (<= 32) queries x topk (<= 64) selections
+
+// Key of one selection: block id in the high bits, then query (5 bits) and slot (6 bits), so
+// that sorting groups the selections of one block and orders them by query.
+__global__ void __launch_bounds__(kSelThreads)
+    dense_select_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv, int32_t G,
+                        int32_t topk, int32_t qpt, int32_t ppg, int32_t thr,
+                        int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
+                        int32_t* __restrict__ dblk, uint32_t* __restrict__ dmask,
+                        float* __restrict__ part_lse) {
+  __shared__ uint32_t keys[kSelKeys];
+  __shared__ uint8_t member[kSelKeys];
+  __shared__ int32_t cand[kSelKeys];
+  __shared__ int32_t warp_sum[kSelThreads / 32];
+  const int tid = threadIdx.x;
+  const int64_t pair = blockIdx.x;
+  const int g = (int)(pair / ppg);
+  const int64_t t0 = (pair % ppg) * 2 * qpt;
+  const int nq = 2 * qpt, n = nq * topk;
+  int N = 1;
+  while (N < n) N <<= 1;
+  for (int e = tid; e < N; e += kSelThreads) {
+    uint32_t key = 0xffffffffu;
+    if (e < n) {
+      const int q = e / topk, s = e % topk;
+      const int64_t t = t0 + q;
+      if (t < T) {
+        const int64_t at = (t * Hkv + g) * topk + s;
+        const int32_t id = block_ids[at];
+        if (id >= 0)
+          key = ((uint32_t)id << 11) | ((uint32_t)q << 6) | (uint32_t)s;
+        else
+          residual[at] = -1;
+      }
+    }
+    keys[e] = key;
+    member[e] = 0;
+  }
+  // the query-major partial of a row stays -inf unless a dense block reaches it
+  for (int r = tid; r < nq * G; r += kSelThreads) {
+    const int64_t t = t0 + r / G;
+    if (t < T) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int e = tid; e < N; e += kSelThreads) {
+        const int o = e ^ j;
+        if (o > e) {
+          const uint32_t a = keys[e], b = keys[o];
+          const bool up = (e & k) == 0;
+          if ((a > b) == up) {
+            keys[e] = b;
+            keys[o] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // runs of one block: the first element of a run counts it and ORs its query bits
+  uint32_t run_mask[kSelKeys / kSelThreads];
+  int run_len[kSelKeys / kSelThreads];
+  int local_cnt = 0;
+  const int per = N / kSelThreads > 0 ? N / kSelThreads : 1;
+  const int e0 = tid * per;
+#pragma unroll
+  for (int r = 0; r < kSelKeys / kSelThreads; ++r) {
+    run_mask[r] = 0u;
+    run_len[r] = 0;
+    const int e = e0 + r;
+    int c = 0;
+    if (r < per && e < N) {
+      const uint32_t key = keys[e];
+      if (key != 0xffffffffu && (e == 0 || (keys[e - 1] >> 11) != (key >> 11))) {
+        uint32_t m = 0u;
+        while (e + c < N && keys[e + c] != 0xffffffffu && (keys[e + c] >> 11) == (key >> 11)) {
+          m |= 1u << ((keys[e + c] >> 6) & 31u);
+          ++c;
+        }
+        run_mask[r] = m;
+        run_len[r] = c;
+      }
+      cand[e] = c >= thr ? 1 : 0;
+    }
+    local_cnt += (r < per && e < N && c >= thr) ? 1 : 0;
+  }
+  // exclusive scan of the dense-run flags in sorted (ascending block) order
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local_cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    if (w < warp) base += warp_sum[w];
+    total += warp_sum[w];
+  }
+  int rank = base + incl - local_cnt;
+#pragma unroll
+  for (int r = 0; r < kSelKeys / kSelThreads; ++r) {
+    const int e = e0 + r;
+    if (r < per && e < N && cand[e]) {
+      if (rank < kMaxDense) {
+        dblk[pair * kMaxDense + rank] = (int32_t)(keys[e] >> 11);
+        dmask[pair * kMaxDense + rank] = run_mask[r];
+        for (int c = 0; c < run_len[r]; ++c) member[e + c] = 1;
+      }
+      ++rank;
+    }
+  }
+  if (tid == 0) dcnt[pair] = total < kMaxDense ? total : kMaxDense;
+  __syncthreads();
+  for (int e = tid; e < N; e += kSelThreads) {
+    const uint32_t key = keys[e];
+    if (key == 0xffffffffu) continue;
+    const int q = (int)((key >> 6) & 31u), s = (int)(key & 63u);
+    residual[((t0 + q) * Hkv + g) * topk + s] = member[e] ? -1 : (int32_t)(key >> 11);
+  }
+}
+
+// ------------------------------------------------------------------------------ attention
+constexpr int kThreads = 384;
+constexpr uint32_t kBox = 128 * 64 * 2;          // 128 rows x 64 channels bf16 = 16 KB
+constexpr uint32_t kTileBytes = 2 * kBox;        // a query tile, a K block or a V block: 32 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;                 // log2 headroom before O is rescaled
+constexpr uint32_t kTmemCols = 512;              // S_A, S_B at 0 / 128; O_A, O_B at 256 / 384
+constexpr uint32_t kIssuerNap = 100;             // ns an idle MMA issuer blocks on a barrier
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
+
+// shared memory (offsets from a 1024-aligned base): the pair's two query tiles, a two-deep
+// ring of K/V blocks, barriers
+constexpr uint32_t kOffQ = 0;                    // Q_A, Q_B
+constexpr uint32_t kOffKV = 2 * kTileBytes;      // {K, V}[2]
+constexpr uint32_t kOffBar = 6 * kTileBytes;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+  uint32_t tmem_base;
+  int32_t fail;
+};
+
+struct DenseKParams {
+  const int32_t* dcnt;
+  const int32_t* dblk;
+  const uint32_t* dmask;
+  int32_t T, Hkv, G, qpt, ppg, q_atoms;
+  int64_t npairs, q_start;
+  uint16_t* part_o;   // chunk-major [16][part_rows][8] bf16
+  int64_t part_rows;  // T*Hkv*G
+  float* part_lse;    // [T*Hkv*G]
+};
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int32_t* fail) {
+  if (*fail) return false;
+  if (mbar_wait(bar, parity)) return true;
+  msa_record_error(kErrTimeout);
+  *fail = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_dense_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                            const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const DenseKParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars& B = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int32_t* fail = &B.fail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // pairs p = blockIdx.x + r*gridDim.x with at least one dense block, in (group, query) order
+  if (tid == 0) {
+    mbar_init(&B.q_full, 1);
+    mbar_init(&B.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B.kv_full[b], 1);
+      mbar_init(&B.kv_empty[b], 1);
+      mbar_init(&B.s_full[b], 1);
+      mbar_init(&B.p_full[b], 4);
+      mbar_init(&B.o_full[b], 1);
+      mbar_init(&B.o_free[b], 4);
+    }
+    B.fail = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&B.tmem_base)), "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  const uint32_t sbase = smem_u32(smem);
+  const int G = p.G, qpt = p.qpt;
+
+  static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+      // ============================================================== producer (whole warp)
+      // lane q gathers query q of the pair; lane 0 loads the K/V blocks
+      if (lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+      }
+      int pairs_done = 0, kv_loads = 0;
+      for (int64_t pr = blockIdx.x; pr < p.npairs && !*fail; pr += gridDim.x) {
+        const int L = p.dcnt[pr];
+        if (L <= 0) continue;
+        const int g = (int)(pr / p.ppg);
+        const int64_t t0 = (pr % p.ppg) * 2 * qpt;
+        const int nvalid = (int)min((int64_t)2 * qpt, (int64_t)p.T - t0);
+        if (pairs_done > 0 && !wait_or_fail(&B.q_empty, (pairs_done - 1) & 1, fail)) break;
+        if (lane == 0) mbar_expect_tx(&B.q_full, (uint32_t)(nvalid * G * 256));
+        __syncwarp();
+        if (lane < nvalid) {
+          const int64_t t = t0 + lane;
+          uint8_t* qdst = smem + kOffQ + (lane / qpt) * kTileBytes;
+          const int q = lane % qpt;
+          if (p.q_atoms) {
+            tma_load_5d(qdst + q * G * 256, &qmap, &B.q_full, 0, 0, 0, 0, (int32_t)(t * p.Hkv + g));
+          } else {
+            tma_load_3d(qdst + q * G * 128, &qmap, &B.q_full, 0, g * G, (int32_t)t);
+            tma_load_3d(qdst + kBox + q * G * 128, &qmap, &B.q_full, 64, g * G, (int32_t)t);
+          }
+        }
+        for (int j = 0; j < L; ++j) {
+          const int c = kv_loads & 1;
+          if (lane == 0) {
+            // load kv_loads goes to buffer kv_loads & 1, free once both O MMAs of load
+            // kv_loads - 2 have completed
+            if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
+              const int tok = p.dblk[pr * kMaxDense + j] * 128;
+              uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
+              mbar_expect_tx(&B.kv_full[c], 4 * kBox);
+              tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
+              tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
+              tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
+              tma_load_3d(kvb + kTileBytes + kBox, &vmap, &B.kv_full[c], 64, g, tok);
+            }
+          }
+          if (__shfl_sync(0xffffffffu, (int)*fail, 0)) break;
+          ++kv_loads;
+        }
+        ++pairs_done;
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ============================================================== MMA issuer
+      // Per warpgroup X (tile A = 0, B = 1) and block n of the CTA's block sequence:
+      //   S_X(n) needs K/V(n), the pair's queries and O_X(n-1) complete (P_X(n-1) lives in
+      //   S_X's columns); O_X(n) needs P_X(n) and, on a pair's first block, the epilogue of
+      //   the previous pair done with O_X. K/V buffer n%2 is released after both O(n), the
+      //   query tiles after both S of a pair's last block.
+      if (lane == 0) {
+        const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);
+        const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);
+        // the CTA's block sequence: total count, and the pair boundaries as they come
+        int total = 0;
+        for (int64_t pr = blockIdx.x; pr < p.npairs; pr += gridDim.x) total += max(p.dcnt[pr], 0);
+        int sN[2] = {0, 0}, oN[2] = {0, 0};
+        // per X: pair index and first/last block index of the pair that block sN[X] / oN[X]
+        // belongs to (advanced lazily)
+        int64_t s_pr[2] = {blockIdx.x, blockIdx.x}, o_pr[2] = {blockIdx.x, blockIdx.x};
+        int s_end[2] = {0, 0}, s_pairs[2] = {-1, -1};
+        int o_first[2] = {0, 0}, o_end[2] = {0, 0}, o_pairs[2] = {-1, -1};
+        uint32_t idle = 0;
+        while ((oN[0] < total || oN[1] < total) && !*fail) {
+          bool progress = false;
+#pragma unroll
+          for (int X = 0; X < 2; ++X) {
+            // ---- O_X(oN[X])
+            if (oN[X] < sN[X]) {
+              const int n = oN[X];
+              while (n >= o_end[X] && o_pr[X] < p.npairs) {  // advance to the pair of block n
+                if (o_pairs[X] >= 0) o_pr[X] += gridDim.x;
+                while (o_pr[X] < p.npairs && p.dcnt[o_pr[X]] <= 0) o_pr[X] += gridDim.x;
+                if (o_pr[X] >= p.npairs) break;
+                o_first[X] = o_end[X];
+                o_end[X] += p.dcnt[o_pr[X]];
+                ++o_pairs[X];
+              }
+              if (n >= o_end[X]) {  // block sequence inconsistent with the pair counts
+                msa_record_error(kErrBadBlock);
+                *fail = 1;
+                break;
+              }
+              const bool first = n == o_first[X];
+              if (mbar_test(&B.p_full[X], n & 1) &&
+                  (!first || o_pairs[X] == 0 || mbar_test(&B.o_free[X], (o_pairs[X] - 1) & 1))) {
+                tmem_fence_after();
+                const int c = n & 1;
+                const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
+                  umma_bf16_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, bd, idesc_o,
+                               (!first || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&B.o_full[X]);
+                ++oN[X];
+                if (oN[1 - X] >= oN[X]) umma_commit(&B.kv_empty[c]);  // both O(n) issued
+                progress = true;
+              }
+            }
+            // ---- S_X(sN[X])
+            if (sN[X] < total && oN[X] >= sN[X]) {
+              const int n = sN[X];
+              while (n >= s_end[X] && s_pr[X] < p.npairs) {
+                if (s_pairs[X] >= 0) s_pr[X] += gridDim.x;
+                while (s_pr[X] < p.npairs && p.dcnt[s_pr[X]] <= 0) s_pr[X] += gridDim.x;
+                if (s_pr[X] >= p.npairs) break;
+                s_end[X] += p.dcnt[s_pr[X]];
+                ++s_pairs[X];
+              }
+              if (n >= s_end[X]) {
+                msa_record_error(kErrBadBlock);
+                *fail = 1;
+                break;
+              }
+              if (mbar_test(&B.kv_full[n & 1], (n >> 1) & 1) &&
+                  mbar_test(&B.q_full, s_pairs[X] & 1) &&
+                  (n == 0 || mbar_test(&B.o_full[X], (n - 1) & 1))) {
+                tmem_fence_after();
+                const uint32_t qa = sbase + kOffQ + X * kTileBytes;
+                const uint32_t ka = sbase + kOffKV + (n & 1) * 2 * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
+                                                  : (kk >> 2) * kBox + (kk & 3) * 32;
+                  const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                  umma_bf16(tmem + X * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
+                            umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                }
+                umma_commit(&B.s_full[X]);
+                ++sN[X];
+                // the pair's last block: once both tiles' S of it are issued (the two tiles run
+                // the same block sequence) the query tiles are free
+                if (sN[X] == s_end[X] && sN[1 - X] >= sN[X]) umma_commit(&B.q_empty);
+                progress = true;
+              }
+            }
+          }
+          if (progress) {
+            idle = 0;
+          } else {
+            const int X = oN[0] <= oN[1] ? 0 : 1;
+            if (oN[X] < sN[X]) mbar_try_wait_hint(&B.p_full[X], oN[X] & 1, kIssuerNap);
+            else __nanosleep(32);
+            if (++idle > kWaitLimit) {
+              msa_record_error(kErrTimeout);
+              *fail = 1;
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    // ================================================================ softmax + epilogue
+    const int X = (warp - 4) >> 2;                 // tile A (warps 4-7) or B (warps 8-11)
+    const int row = (tid - 128) & 127;             // tile row = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+    const int qi = row / G, h = row % G;
+    const uint32_t s_tmem = tmem + lane_addr + X * 128;
+    const uint32_t o_tmem = tmem + lane_addr + 256 + X * 128;
+    const uint32_t qbit = 1u << (X * qpt + qi);
+    int n = 0, pairs_done = 0;
+    for (int64_t pr = blockIdx.x; pr < p.npairs && !*fail; pr += gridDim.x) {
+      const int L = p.dcnt[pr];
+      if (L <= 0) continue;
+      const int g = (int)(pr / p.ppg);
+      const int64_t t = (pr % p.ppg) * 2 * qpt + X * qpt + qi;
+      const bool valid = t < p.T;
+      const int64_t pos = p.q_start + t;
+      float m_run = -INFINITY, l = 0.f;             // running max (log2 units) and sum
+      uint32_t mask_next = p.dmask[pr * kMaxDense];
+      int blk_next = p.dblk[pr * kMaxDense];
+      for (int j = 0; j < L; ++j, ++n) {
+        const uint32_t mbits = mask_next;
+        const int blk = blk_next;
+        if (j + 1 < L) {
+          mask_next = p.dmask[pr * kMaxDense + j + 1];
+          blk_next = p.dblk[pr * kMaxDense + j + 1];
+        }
+        const bool sel = valid && (mbits & qbit) != 0u;
+        if (!wait_or_fail(&B.s_full[X], n & 1, fail)) break;
+        tmem_fence_after();
+        float v[128];
+        float factor = 1.f;
+        bool need = false;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, v + c * 32);
+        tmem_wait_ld();
+        // a row whose query did not choose this block is masked entirely; otherwise only the
+        // keys after the query on its own block
+        const int64_t lim64 = sel ? pos - (int64_t)blk * 128 : -1;  // last visible column
+        if (lim64 < 127) {
+          const int lim = lim64 < -1 ? -1 : (int)lim64;
+#pragma unroll
+          for (int x = 0; x < 128; ++x)
+            if (x > lim) v[x] = -INFINITY;
+        }
+        float m4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+        for (int x = 4; x < 128; x += 2) m4[(x >> 1) & 3] = max3(m4[(x >> 1) & 3], v[x], v[x + 1]);
+        const float m2 = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]) * kLog2e;
+        if (m_run == -INFINITY) {
+          m_run = m2;  // the row's O is still zero
+        } else if (m2 > m_run + kRescale) {
+          factor = ex2(m_run - m2);
+          need = true;
+          m_run = m2;
+          l *= factor;
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;  // masked rows: 2^-inf = 0
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int x = 0; x < 128; x += 2) {
+          fma2(v[x], v[x + 1], v[x], v[x + 1], kLog2e, kLog2e, -m_use, -m_use);
+          v[x] = ex2(v[x]);
+          v[x + 1] = ex2(v[x + 1]);
+          add2(l8[(x >> 1) & 3], l8[4 + ((x >> 1) & 3)], v[x], v[x + 1]);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        // P row (bf16 pairs) into the first 64 columns of the tile's S buffer
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(v[h2 * 64 + 2 * x], v[h2 * 64 + 2 * x + 1]);
+          tmem_st32(s_tmem + h2 * 32, pk);
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // the row max grew by more than 2^8: rescale O once O(n-1) has completed
+          if (!wait_or_fail(&B.o_full[X], (n - 1) & 1, fail)) break;
+          tmem_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(o_tmem + c * 32, o);
+            tmem_wait_ld();
+            uint32_t ob[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ob[x] = __float_as_uint(o[x] * factor);
+            tmem_st32(o_tmem + c * 32, ob);
+          }
+        }
+        tmem_wait_st();
+        tmem_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_full[X]);
+      }
+      if (*fail) break;
+      // ---------------- epilogue of the pair: normalised bf16 partial + fp32 LSE per row
+      if (!wait_or_fail(&B.o_full[X], (n - 1) & 1, fail)) break;
+      tmem_fence_after();
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(o_tmem + c * 32, v + c * 32);
+      tmem_wait_ld();
+      tmem_fence_before();
+      if (valid) {
+        const int64_t prow = (t * p.Hkv + g) * G + h;
+        p.part_lse[prow] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.part_o) + prow;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          uint4 u;
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) mul2(v[c * 8 + e], v[c * 8 + e + 1], inv, inv);
+          u.x = pack_bf16x2(v[c * 8 + 0], v[c * 8 + 1]);
+          u.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
+          u.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
+          u.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
+          dst[(int64_t)c * p.part_rows] = u;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.o_free[X]);
+      ++pairs_done;
+    }
+  }
+  // ------------------------------------------------------------------ teardown
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t G,
+                                int32_t topk, const DenseWorkspace& w, cudaStream_t stream) {
+  const int32_t qpt = 128 / G;
+  const int32_t ppg = (int32_t)((T + 2 * qpt - 1) / (2 * qpt));
+  const int32_t nq = 2 * qpt;
+  const int32_t thr = std::max(2, (3 * nq + 7) / 8);
+  const int64_t npairs = (int64_t)Hkv * ppg;
+  if (npairs <= 0) return cudaSuccess;
+  dense_select_kernel<<<(unsigned)npairs, kSelThreads, 0, stream>>>(
+      block_ids, T, Hkv, G, topk, qpt, ppg, thr, w.residual, w.dcnt, w.dblk, w.dmask, w.part_lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
+                                   int64_t S_kv, int32_t Hkv, int32_t G, const DenseWorkspace& w,
+                                   cudaStream_t stream) {
+  DenseKParams p;
+  p.dcnt = w.dcnt;
+  p.dblk = w.dblk;
+  p.dmask = w.dmask;
+  p.T = T;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.qpt = 128 / G;
+  p.ppg = (int32_t)((T + 2 * p.qpt - 1) / (2 * p.qpt));
+  p.q_atoms = q_atoms;
+  p.npairs = (int64_t)Hkv * p.ppg;
+  p.q_start = S_kv - T;
+  p.part_o = w.part_o;
+  p.part_rows = (int64_t)T * Hkv * G;
+  p.part_lse = w.part_lse;
+  if (p.npairs <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(prefill_dense_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_dense_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  const int64_t grid = std::min<int64_t>(p.npairs, sm_count());
+  prefill_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -134,6 +134,29 @@ def test_sparse_prefill(T, S, Hq, Hkv, topk, n_shared):
     check_attention(o, lse, ref, what="prefill")
 
 
+def test_sparse_prefill_shared_blocks_beyond_the_dense_cap():
+    """k 64 with two query halves per 32-query pair choosing disjoint 62-block sets: 126 blocks
+    are shared by at least 3/8 of the pair, more than the query-major pass takes, so the blocks
+    past its cap must reach the output through the block-major pass."""
+    T, prefix, Hq, Hkv, D, k = 64, 16384, 16, 2, 128, 64
+    S = prefix + T
+    gen = torch.Generator().manual_seed(77)
+    q = workloads.randn_bf16((T, Hq, D), gen, "cpu", scale=D ** -0.5)
+    kk = workloads.randn_bf16((S, Hkv, D), gen, "cpu")
+    vv = workloads.randn_bf16((S, Hkv, D), gen, "cpu")
+    local = (prefix + torch.arange(T)) // 128            # block 128 for every query
+    ids = torch.empty((T, Hkv, k), dtype=torch.int32)
+    for t in range(T):
+        half = (t % 32) // 16
+        body = torch.arange(1 + 62 * half, 63 + 62 * half)  # 62 blocks, disjoint per half
+        row = torch.cat([torch.tensor([0]), body, local[t:t + 1]]).to(torch.int32)
+        ids[t, :, :] = torch.sort(row).values
+    o, lse = msa.sparse_prefill(q.to(DEV), kk.to(DEV), vv.to(DEV), ids.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sparse_prefill(u16(q), u16(kk), u16(vv), ids.numpy())
+    check_attention(o, lse, ref, what="prefill beyond the dense cap")
+
+
 def test_prefill_bucket_lists():
     w = workloads.prefill_workload(900, 1500, 16, 4, 128, 6, seed=4, device="cpu", n_shared=3)
     nblk = (1500 + 127) // 128
