@@ -157,7 +157,26 @@ __global__ void __launch_bounds__(256)
 // Prefill merge over chunk-major partials: part_o[c][row][8] bf16 with c = 16 channel chunks
 // and row = (u*S + s)*G + e; one warp per unit u (all G heads). Lane slot idx = lane + 32*r
 // covers head idx % G and chunk idx / G, so for a fixed r the lanes of one chunk plane read the
-// G adjacent rows of a partial: 16*G contiguous bytes.
+// G adjacent rows of a partial: 16*G contiguous bytes. The valid slots (ids >= 0) are found
+// with one ballot; their partials stream two at a time (loads of both issued together) into
+// accumulators kept relative to a running max, rescaled when the max grows. The optional
+// query-major partial (dense_o / dense_lse, one per unit and head) is the first "slot".
+template <int G>
+__device__ __forceinline__ void merge_fma(float (&acc)[(G * 16 + 31) / 32][8], float w,
+                                          const uint4 (&v)[(G * 16 + 31) / 32]) {
+#pragma unroll
+  for (int r = 0; r < (G * 16 + 31) / 32; ++r) {
+    acc[r][0] = fmaf(w, bf16_lo(v[r].x), acc[r][0]);
+    acc[r][1] = fmaf(w, bf16_hi(v[r].x), acc[r][1]);
+    acc[r][2] = fmaf(w, bf16_lo(v[r].y), acc[r][2]);
+    acc[r][3] = fmaf(w, bf16_hi(v[r].y), acc[r][3]);
+    acc[r][4] = fmaf(w, bf16_lo(v[r].z), acc[r][4]);
+    acc[r][5] = fmaf(w, bf16_hi(v[r].z), acc[r][5]);
+    acc[r][6] = fmaf(w, bf16_lo(v[r].w), acc[r][6]);
+    acc[r][7] = fmaf(w, bf16_hi(v[r].w), acc[r][7]);
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(256)
     lse_merge_chunked_kernel(const uint4* __restrict__ part_o, int64_t part_rows,
@@ -169,64 +188,68 @@ __global__ void __launch_bounds__(256)
   const int64_t u = (int64_t)blockIdx.x * 8 + warp;
   if (u >= U) return;
   const int e = lane % G;
-  float m = -INFINITY;
-  for (int s = 0; s < S; ++s) {
-    if (ids[u * S + s] < 0) continue;
-    m = fmaxf(m, lse_parts[(u * S + s) * G + e]);
+  // valid slots of the unit (S <= 64)
+  uint64_t vmask = 0;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    const bool ok = s < S && __ldg(ids + u * S + s) >= 0;
+    vmask |= (uint64_t)__ballot_sync(0xffffffffu, ok) << s0;
   }
-  // the query-major partial (one per unit and head), when the prefill has one
-  const float ld = dense_lse ? dense_lse[u * G + e] : -INFINITY;
-  m = fmaxf(m, ld);
   float acc[R][8];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[r][x] = 0.f;
-  float total = 0.f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      if (ids[u * S + s] < 0) continue;
-      const float ls = lse_parts[(u * S + s) * G + e];
-      if (ls == -INFINITY) continue;
-      const float w = __expf(ls - m);
-      total += w;
-      const int64_t row = (u * S + s) * G + e;
+  float m = -INFINITY, total = 0.f;  // acc and total are relative to 2^(m) in natural units
+  auto rescale_to = [&](float m_new) {
+    const float sc = m == -INFINITY ? 0.f : __expf(m - m_new);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[r][x] *= sc;
+    total *= sc;
+    m = m_new;
+  };
+  if (dense_lse) {
+    const float ld = dense_lse[u * G + e];
+    if (ld != -INFINITY) {
+      uint4 v[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int idx = lane + 32 * r;
-        if (idx < G * 16) {
-          const uint4 v = __ldcs(part_o + (int64_t)(idx / G) * part_rows + row);
-          acc[r][0] = fmaf(w, bf16_lo(v.x), acc[r][0]);
-          acc[r][1] = fmaf(w, bf16_hi(v.x), acc[r][1]);
-          acc[r][2] = fmaf(w, bf16_lo(v.y), acc[r][2]);
-          acc[r][3] = fmaf(w, bf16_hi(v.y), acc[r][3]);
-          acc[r][4] = fmaf(w, bf16_lo(v.z), acc[r][4]);
-          acc[r][5] = fmaf(w, bf16_hi(v.z), acc[r][5]);
-          acc[r][6] = fmaf(w, bf16_lo(v.w), acc[r][6]);
-          acc[r][7] = fmaf(w, bf16_hi(v.w), acc[r][7]);
-        }
+        v[r] = idx < G * 16 ? __ldcs(dense_o + (int64_t)(idx / G) * (U * G) + u * G + e)
+                            : make_uint4(0u, 0u, 0u, 0u);
       }
+      m = ld;
+      total = 1.f;
+      merge_fma<G>(acc, 1.f, v);
     }
   }
-  if (m != -INFINITY && ld != -INFINITY) {
-    const float w = __expf(ld - m);
-    total += w;
-    const int64_t drows = U * G;
+  while (vmask) {
+    const int sa = __ffsll((long long)vmask) - 1;
+    vmask &= vmask - 1;
+    const int sb = vmask ? __ffsll((long long)vmask) - 1 : -1;
+    if (sb >= 0) vmask &= vmask - 1;
+    const int64_t ra = (u * S + sa) * G + e;
+    const int64_t rb = sb >= 0 ? (u * S + sb) * G + e : ra;
+    const float la = lse_parts[ra];
+    const float lb = sb >= 0 ? lse_parts[rb] : -INFINITY;
+    uint4 va[R], vb[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int idx = lane + 32 * r;
-      if (idx < G * 16) {
-        const uint4 v = __ldcs(dense_o + (int64_t)(idx / G) * drows + u * G + e);
-        acc[r][0] = fmaf(w, bf16_lo(v.x), acc[r][0]);
-        acc[r][1] = fmaf(w, bf16_hi(v.x), acc[r][1]);
-        acc[r][2] = fmaf(w, bf16_lo(v.y), acc[r][2]);
-        acc[r][3] = fmaf(w, bf16_hi(v.y), acc[r][3]);
-        acc[r][4] = fmaf(w, bf16_lo(v.z), acc[r][4]);
-        acc[r][5] = fmaf(w, bf16_hi(v.z), acc[r][5]);
-        acc[r][6] = fmaf(w, bf16_lo(v.w), acc[r][6]);
-        acc[r][7] = fmaf(w, bf16_hi(v.w), acc[r][7]);
-      }
+      const bool in = idx < G * 16;
+      va[r] = in ? __ldcs(part_o + (int64_t)(idx / G) * part_rows + ra) : make_uint4(0u, 0u, 0u, 0u);
+      vb[r] = in && sb >= 0 ? __ldcs(part_o + (int64_t)(idx / G) * part_rows + rb)
+                            : make_uint4(0u, 0u, 0u, 0u);
     }
+    const float mx = fmaxf(la, lb);
+    if (mx == -INFINITY) continue;
+    if (mx > m) rescale_to(mx);
+    const float wa = __expf(la - m), wb = lb == -INFINITY ? 0.f : __expf(lb - m);
+    total += wa + wb;
+    merge_fma<G>(acc, wa, va);
+    merge_fma<G>(acc, wb, vb);
   }
   const float inv = total > 0.f ? 1.0f / total : 0.f;
 #pragma unroll
