@@ -271,15 +271,11 @@ def run_ours(args, ws, rank, local):
     err = msa.device_error()
 
     # prefill sub-steps, timed separately after the main loop: bucketing and merge alone
-    sub = prefill_breakdown(msa, c3, wsp, dev, reps=max(3, args.steps)) if "prefill" in run \
-        else {"bucket_ms": 0.0}
 
     eps = 1e-9
     score_gbs = c2["bytes"] / (max(score_ms, eps) * 1e-3) / 1e9
     dec_gbs = c4["bytes"] / (max(pt_ms + dec_ms, eps) * 1e-3) / 1e9
     pre_tflops = c3["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
-    attn_ms = max(pre_ms - sub["bucket_ms"], 1e-6)
-    attn_tflops = c3["flops"] / (attn_ms * 1e-3) / 1e12
     value = score_gbs * ws
 
     # e2e through host buffers for the headline stage
@@ -303,16 +299,16 @@ def run_ours(args, ws, rank, local):
         "sparse_prefill": {"config": "T 32768 causal, Hq 64, Hkv 8, D 128, k 16", "ms": round(pre_ms, 4),
                            "TFLOP/s": round(pre_tflops, 1),
                            "frac_bf16": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
-                           "attention_merge_ms": round(attn_ms, 4),
-                           "attention_merge_TFLOP/s": round(attn_tflops, 1),
-                           "attention_merge_frac_bf16": round(attn_tflops / pk["bf16_tflops_sustained"], 4),
-                           "bucket_ms": round(sub["bucket_ms"], 4),
+                           "kernels": "query-major selection + attention for blocks shared by a "
+                                      "query pair; bucketing + block-major attention for the "
+                                      "rest; LSE merge (per-kernel shares: profiles/)",
                            "flops": c3["flops"],
-                           # block-major design: every (query, block) selection writes a bf16
-                           # partial of G rows that the merge reads back; that traffic alone
-                           # takes partials_floor_ms at the measured HBM bandwidth
-                           "partials_bytes": c3["partial_bytes"],
-                           "partials_floor_ms": round(c3["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
+                           # a purely block-major prefill writes one bf16 partial of G rows per
+                           # (query, block) selection and reads it back: that traffic alone takes
+                           # block_major_floor_ms at the measured HBM bandwidth (the query-major
+                           # pass removes most of it for shared blocks)
+                           "block_major_partials_bytes": c3["partial_bytes"],
+                           "block_major_floor_ms": round(c3["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
                            "traffic": recorded_traffic("prefill_block_tc_kernel", src_hash("prefill.cu"))},
     }
     line = {
@@ -343,24 +339,6 @@ def run_ours(args, ws, rank, local):
         line["cpu_baseline"] = cpu_baseline(c2, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
-
-
-def prefill_breakdown(msa, c3, wsp, dev, reps: int):
-    """The bucketing step timed alone on the prefill workload (the same kernels the prefill call
-    runs first), to attribute the prefill call's time; the attention kernel merges rows itself."""
-    nblk = (c3["S_kv"] + BLOCK - 1) // BLOCK
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    msa.prefill_bucket(c3["block_ids"], nblk, workspace=wsp)
-    torch.cuda.synchronize()
-    bt = 0.0
-    for _ in range(reps):
-        a.record()
-        msa.prefill_bucket(c3["block_ids"], nblk, workspace=wsp)
-        b.record()
-        torch.cuda.synchronize()
-        bt += a.elapsed_time(b)
-    return {"bucket_ms": bt / reps}
 
 
 def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
