@@ -49,6 +49,22 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(vals, ws: int, device):
+    """Each value's maximum over all ranks (identity on one rank): the job's time is the slowest
+    rank's."""
+    if ws <= 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(units_per_rank: float, ms: float, ws: int) -> float:
+    """Whole-job throughput: every rank processes its own replica of `units_per_rank`, the job
+    takes `ms` (the max over ranks)."""
+    return units_per_rank * ws / (ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -243,7 +259,6 @@ def run_ours(args, ws, rank, local):
 
     for _ in range(args.warmup):
         step()
-    # per-kernel breakdown of the prefill call (separate entry points, timed once, not in value)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -261,22 +276,18 @@ def run_ours(args, ws, rank, local):
         torch.distributed.barrier()
     total_ms = start.elapsed_time(stop)
     stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(4)]
-    if ws > 1:
-        t = torch.tensor([total_ms] + stage_ms, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, stage_ms = float(t[0]), [float(x) for x in t[1:]]
+    # the slowest rank sets the job's time
+    total_ms, *stage_ms = max_over_ranks([total_ms] + stage_ms, ws, dev)
     ms_per_step = total_ms / args.steps
     score_ms, pt_ms, dec_ms, pre_ms = stage_ms
     # device error word: none expected
     err = msa.device_error()
 
-    # prefill sub-steps, timed separately after the main loop: bucketing and merge alone
-
     eps = 1e-9
     score_gbs = c2["bytes"] / (max(score_ms, eps) * 1e-3) / 1e9
     dec_gbs = c4["bytes"] / (max(pt_ms + dec_ms, eps) * 1e-3) / 1e9
     pre_tflops = c3["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
-    value = score_gbs * ws
+    value = job_throughput(c2["bytes"], max(score_ms, eps), ws) / 1e9
 
     # e2e through host buffers for the headline stage
     e2e = e2e_score(msa, c2, wsp, dev, args.steps, ws) if "score" in run else None
@@ -368,6 +379,8 @@ def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
     for _ in range(3):
         one()
     torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record()
@@ -375,10 +388,10 @@ def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
         one()
     e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    ms = max_over_ranks([s.elapsed_time(e) / steps], ws, dev)[0]
     h2d = h_q.numel() * 2 + h_pt.numel() * 4 + h_sl.numel() * 4
     d2h = h_ids.numel() * 4 + h_sc.numel() * 4
-    return {"value": round(c2["bytes"] / (ms * 1e-3) / 1e9 * ws, 1), "unit": "GB/s",
+    return {"value": round(job_throughput(c2["bytes"], ms, ws) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "note": "per-step inputs copied from pinned host memory; paged K-index resident"}
 
