@@ -210,6 +210,12 @@ def recorded_traffic(kernel: str, source_hash: str):
     return rec.get("bytes_per_launch")
 
 
+def prefill_traffic():
+    blk = recorded_traffic("prefill_block_tc_kernel", src_hash("prefill.cu"))
+    dense = recorded_traffic("prefill_dense_tc_kernel", src_hash("prefill_dense.cu"))
+    return None if blk is None or dense is None else blk + dense
+
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, ws, rank, local):
@@ -320,7 +326,9 @@ def run_ours(args, ws, rank, local):
                            # pass removes most of it for shared blocks)
                            "block_major_partials_bytes": c3["partial_bytes"],
                            "block_major_floor_ms": round(c3["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
-                           "traffic": recorded_traffic("prefill_block_tc_kernel", src_hash("prefill.cu"))},
+                           # DRAM bytes of the two attention kernels per call (null when either
+                           # source changed since it was profiled)
+                           "traffic": prefill_traffic()},
     }
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
