@@ -140,8 +140,9 @@ struct DenseWorkspace {
   uint16_t* part_o;    // chunk-major [16][T*Hkv*G][8] bf16
   float* part_lse;     // [T*Hkv*G]
 };
-cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t G,
-                                int32_t topk, const DenseWorkspace& w, cudaStream_t stream);
+cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
+                                int32_t G, int32_t topk, const DenseWorkspace& w,
+                                cudaStream_t stream);
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
                                    int64_t S_kv, int32_t Hkv, int32_t G, const DenseWorkspace& w,

@@ -658,7 +658,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
     dw.dmask = reinterpret_cast<uint32_t*>(a.workspace + W.dmask);
     dw.part_o = reinterpret_cast<uint16_t*>(a.workspace + W.dense_o);
     dw.part_lse = reinterpret_cast<float*>(a.workspace + W.dense_lse);
-    e = launch_dense_select(a.block_ids, a.T, a.Hkv, G, a.topk, dw, stream);
+    e = launch_dense_select(a.block_ids, a.T, a.S_kv, a.Hkv, G, a.topk, dw, stream);
     if (e != cudaSuccess) return e;
     ids = dw.residual;
   }

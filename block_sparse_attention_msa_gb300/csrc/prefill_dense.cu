@@ -13,9 +13,9 @@
 //
 // GB300 design.
 //  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G consecutive
-//      queries of one group): sorts the pair's (block, query, slot) selections, keeps the
-//      blocks chosen by at least 3/8 of the pair's queries (at most kMaxDense, ascending) with
-//      a bit mask of the queries that chose each, and writes the residual selections (the
+//      queries of one group): counts the pair's selections per block in shared memory, keeps
+//      the blocks chosen by at least 3/8 of the pair's queries (at most kMaxDense, ascending)
+//      with a bit mask of the queries that chose each, and writes the residual selections (the
 //      dense ones replaced by -1) for the block-major pass.
 //  (b) prefill_dense_tc_kernel, one persistent CTA per SM over the pairs: the two tiles of a
 //      pair share each K/V block load; per block S = Q K^T and O += P V run on tcgen05 with
@@ -38,130 +38,95 @@ namespace {
 
 // ------------------------------------------------------------------------------ selection
 constexpr int kSelThreads = 256;
-constexpr int kSelKeys = 2048;  // 2*qpt (<= 32) queries x topk (<= 64) selections
+// One CTA per pair of 128/G-query tiles (nq = 2*128/G <= 32 consecutive queries of group g).
+// The ids a pair can choose are at most the local block of its last query (nb blocks); they are
+// counted in windows of kHistBlocks blocks: a query mask per block in shared memory, filled with
+// shared atomics (a block's count is its mask's popcount: a query chooses a block at most once),
+// then a prefix scan over the window ranks the dense blocks in ascending order.
+constexpr int kHistBlocks = 16384;
 
-// Key of one selection: block id in the high bits, then query (5 bits) and slot (6 bits), so
-// that sorting groups the selections of one block and orders them by query.
 __global__ void __launch_bounds__(kSelThreads)
     dense_select_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv, int32_t G,
-                        int32_t topk, int32_t qpt, int32_t ppg, int32_t thr,
+                        int32_t topk, int32_t qpt, int32_t ppg, int32_t thr, int64_t q_start,
                         int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
                         int32_t* __restrict__ dblk, uint32_t* __restrict__ dmask,
                         float* __restrict__ part_lse) {
-  __shared__ uint32_t keys[kSelKeys];
-  __shared__ uint8_t member[kSelKeys];
-  __shared__ int32_t cand[kSelKeys];
+  extern __shared__ __align__(16) uint8_t hist_smem[];
+  uint32_t* msk = reinterpret_cast<uint32_t*>(hist_smem);                  // [kHistBlocks]
+  int16_t* rnk = reinterpret_cast<int16_t*>(hist_smem + 4 * kHistBlocks);  // dense rank or -1
   __shared__ int32_t warp_sum[kSelThreads / 32];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t pair = blockIdx.x;
   const int g = (int)(pair / ppg);
   const int64_t t0 = (pair % ppg) * 2 * qpt;
   const int nq = 2 * qpt, n = nq * topk;
-  int N = 1;
-  while (N < n) N <<= 1;
-  for (int e = tid; e < N; e += kSelThreads) {
-    uint32_t key = 0xffffffffu;
-    if (e < n) {
-      const int q = e / topk, s = e % topk;
-      const int64_t t = t0 + q;
-      if (t < T) {
-        const int64_t at = (t * Hkv + g) * topk + s;
-        const int32_t id = block_ids[at];
-        if (id >= 0)
-          key = ((uint32_t)id << 11) | ((uint32_t)q << 6) | (uint32_t)s;
-        else
-          residual[at] = -1;
-      }
-    }
-    keys[e] = key;
-    member[e] = 0;
-  }
-  // the query-major partial of a row stays -inf unless a dense block reaches it
+  const int64_t t_last = min((int64_t)T - 1, t0 + nq - 1);
+  const int64_t nb = (q_start + t_last) / 128 + 1;  // blocks the pair can have chosen
   for (int r = tid; r < nq * G; r += kSelThreads) {
     const int64_t t = t0 + r / G;
     if (t < T) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
   }
-  __syncthreads();
-  // bitonic sort, ascending
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int e = tid; e < N; e += kSelThreads) {
-        const int o = e ^ j;
-        if (o > e) {
-          const uint32_t a = keys[e], b = keys[o];
-          const bool up = (e & k) == 0;
-          if ((a > b) == up) {
-            keys[e] = b;
-            keys[o] = a;
-          }
+  int ranked = 0;  // dense blocks ranked in earlier windows
+  for (int64_t base = 0; base < nb; base += kHistBlocks) {
+    const int w = (int)min((int64_t)kHistBlocks, nb - base);
+    for (int j = tid; j < w; j += kSelThreads) msk[j] = 0u;
+    __syncthreads();
+    for (int e = tid; e < n; e += kSelThreads) {
+      const int q = e / topk;
+      const int64_t t = t0 + q;
+      if (t >= T) continue;
+      const int64_t id = block_ids[(t * Hkv + g) * topk + e % topk];
+      if (id >= base && id < base + w) atomicOr(&msk[id - base], 1u << q);
+    }
+    __syncthreads();
+    const int per = (w + kSelThreads - 1) / kSelThreads;
+    const int j0 = tid * per, j1 = min(w, j0 + per);
+    int local = 0;
+    for (int j = j0; j < j1; ++j) local += __popc(msk[j]) >= thr ? 1 : 0;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int rank = ranked + incl - local, total = 0;
+    for (int v = 0; v < kSelThreads / 32; ++v) {
+      if (v < warp) rank += warp_sum[v];
+      total += warp_sum[v];
+    }
+    for (int j = j0; j < j1; ++j) {
+      const uint32_t m = msk[j];
+      int16_t rk = -1;
+      if (__popc(m) >= thr) {
+        if (rank < kMaxDense) {
+          dblk[pair * kMaxDense + rank] = (int32_t)(base + j);
+          dmask[pair * kMaxDense + rank] = m;
+          rk = (int16_t)rank;
         }
+        ++rank;
       }
-      __syncthreads();
+      rnk[j] = rk;
     }
-  }
-  // runs of one block: the first element of a run counts it and ORs its query bits
-  uint32_t run_mask[kSelKeys / kSelThreads];
-  int run_len[kSelKeys / kSelThreads];
-  int local_cnt = 0;
-  const int per = N / kSelThreads > 0 ? N / kSelThreads : 1;
-  const int e0 = tid * per;
-#pragma unroll
-  for (int r = 0; r < kSelKeys / kSelThreads; ++r) {
-    run_mask[r] = 0u;
-    run_len[r] = 0;
-    const int e = e0 + r;
-    int c = 0;
-    if (r < per && e < N) {
-      const uint32_t key = keys[e];
-      if (key != 0xffffffffu && (e == 0 || (keys[e - 1] >> 11) != (key >> 11))) {
-        uint32_t m = 0u;
-        while (e + c < N && keys[e + c] != 0xffffffffu && (keys[e + c] >> 11) == (key >> 11)) {
-          m |= 1u << ((keys[e + c] >> 6) & 31u);
-          ++c;
-        }
-        run_mask[r] = m;
-        run_len[r] = c;
-      }
-      cand[e] = c >= thr ? 1 : 0;
+    __syncthreads();
+    // residual selections of this window: the dense ones leave, the others stay; ids outside
+    // every window (negative or past the causal range) are copied once, with the first window
+    for (int e = tid; e < n; e += kSelThreads) {
+      const int q = e / topk;
+      const int64_t t = t0 + q;
+      if (t >= T) continue;
+      const int64_t at = (t * Hkv + g) * topk + e % topk;
+      const int32_t id = block_ids[at];
+      if (id >= base && id < base + w)
+        residual[at] = rnk[id - base] >= 0 ? -1 : id;
+      else if (base == 0 && (id < 0 || id >= nb))
+        residual[at] = id;
     }
-    local_cnt += (r < per && e < N && c >= thr) ? 1 : 0;
+    ranked += total;
+    __syncthreads();  // the window's arrays are reused by the next window
   }
-  // exclusive scan of the dense-run flags in sorted (ascending block) order
-  const int lane = tid & 31, warp = tid >> 5;
-  int incl = local_cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_sum[warp] = incl;
-  __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    if (w < warp) base += warp_sum[w];
-    total += warp_sum[w];
-  }
-  int rank = base + incl - local_cnt;
-#pragma unroll
-  for (int r = 0; r < kSelKeys / kSelThreads; ++r) {
-    const int e = e0 + r;
-    if (r < per && e < N && cand[e]) {
-      if (rank < kMaxDense) {
-        dblk[pair * kMaxDense + rank] = (int32_t)(keys[e] >> 11);
-        dmask[pair * kMaxDense + rank] = run_mask[r];
-        for (int c = 0; c < run_len[r]; ++c) member[e + c] = 1;
-      }
-      ++rank;
-    }
-  }
-  if (tid == 0) dcnt[pair] = total < kMaxDense ? total : kMaxDense;
-  __syncthreads();
-  for (int e = tid; e < N; e += kSelThreads) {
-    const uint32_t key = keys[e];
-    if (key == 0xffffffffu) continue;
-    const int q = (int)((key >> 6) & 31u), s = (int)(key & 63u);
-    residual[((t0 + q) * Hkv + g) * topk + s] = member[e] ? -1 : (int32_t)(key >> 11);
-  }
+  if (tid == 0) dcnt[pair] = ranked < kMaxDense ? ranked : kMaxDense;
 }
 
 // ------------------------------------------------------------------------------ attention
@@ -552,16 +517,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t G,
-                                int32_t topk, const DenseWorkspace& w, cudaStream_t stream) {
+cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
+                                int32_t G, int32_t topk, const DenseWorkspace& w,
+                                cudaStream_t stream) {
   const int32_t qpt = 128 / G;
   const int32_t ppg = (int32_t)((T + 2 * qpt - 1) / (2 * qpt));
   const int32_t nq = 2 * qpt;
   const int32_t thr = std::max(2, (3 * nq + 7) / 8);
   const int64_t npairs = (int64_t)Hkv * ppg;
   if (npairs <= 0) return cudaSuccess;
-  dense_select_kernel<<<(unsigned)npairs, kSelThreads, 0, stream>>>(
-      block_ids, T, Hkv, G, topk, qpt, ppg, thr, w.residual, w.dcnt, w.dblk, w.dmask, w.part_lse);
+  const size_t smem = 6 * (size_t)kHistBlocks;
+  cudaError_t e = cudaFuncSetAttribute(dense_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dense_select_kernel<<<(unsigned)npairs, kSelThreads, smem, stream>>>(
+      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, w.residual, w.dcnt, w.dblk, w.dmask,
+      w.part_lse);
   return cudaGetLastError();
 }
 

@@ -157,6 +157,29 @@ def test_sparse_prefill_shared_blocks_beyond_the_dense_cap():
     check_attention(o, lse, ref, what="prefill beyond the dense cap")
 
 
+def test_sparse_prefill_beyond_two_million_tokens():
+    """A 64-token chunk after a 2,098,152-token prefix (16392 blocks): the blocks a query pair
+    shares lie on both sides of the 16384-block windows the shared-block selection counts in."""
+    T, prefix, Hq, Hkv, D, k = 64, 16391 * 128 + 104, 8, 1, 128, 16
+    S = prefix + T
+    gen = torch.Generator().manual_seed(78)
+    q = workloads.randn_bf16((T, Hq, D), gen, "cpu", scale=D ** -0.5)
+    kk = workloads.randn_bf16((S, Hkv, D), gen, "cpu")
+    vv = workloads.randn_bf16((S, Hkv, D), gen, "cpu")
+    shared = [0, 100, 5000, 16383, 16384, 16385, 16390]
+    ids = torch.empty((T, Hkv, k), dtype=torch.int32)
+    for t in range(T):
+        local = (prefix + t) // 128
+        pool = torch.tensor([b for b in range(1, local) if b not in shared])
+        extra = pool[torch.randperm(pool.numel(), generator=gen)[:k - len(shared) - 1]]
+        row = torch.cat([torch.tensor(shared), extra, torch.tensor([local])]).to(torch.int32)
+        ids[t, 0, :] = torch.sort(row).values
+    o, lse = msa.sparse_prefill(q.to(DEV), kk.to(DEV), vv.to(DEV), ids.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sparse_prefill(u16(q), u16(kk), u16(vv), ids.numpy())
+    check_attention(o, lse, ref, what="prefill past 16384 blocks")
+
+
 def test_prefill_bucket_lists():
     w = workloads.prefill_workload(900, 1500, 16, 4, 128, 6, seed=4, device="cpu", n_shared=3)
     nblk = (1500 + 127) // 128
