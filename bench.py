@@ -444,7 +444,8 @@ def cpu_baseline(c2, seconds: float):
 def run_cfg5(args, local):
     """1M-token layer, reported per stage (not part of the headline step): 4 x 1,048,576-token
     decode (score + top-k, sparse page table, paged decode, k 32) and a 32768-token prefill chunk
-    on a 1,048,576-token prefix (score + top-k over every chunk row, then block-major attention)."""
+    on a 1,048,576-token prefix (score + top-k over every chunk row, then sparse attention with
+    contiguous K/V and with the prefix read through a page table)."""
     import block_sparse_attention_msa_gb300 as msa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -506,6 +507,16 @@ def run_cfg5(args, local):
     out["prefill_attention"] = {"ms": round(ms_pa, 3), "TFLOP/s": round(attn_flops / ms_pa / 1e9, 1),
                                 "frac_bf16": round(attn_flops / ms_pa / 1e9 / pk["bf16_tflops_sustained"], 4),
                                 "flops": attn_flops}
+    # the same chunk with the prefix read from the paged cache through its page table (the
+    # chunk's K/V viewed as [P, 128, Hkv, D] pages; a block's rows have the same layout as in
+    # the contiguous form, only the block's base comes from the table)
+    kc = w["k"].view(P, 128, Hkv, w["D"])
+    vc = w["v"].view(P, 128, Hkv, w["D"])
+    pt = w["page_table"][0].contiguous()
+    ms_pp = timed(lambda: msa.sparse_prefill_paged(w["q"], kc, vc, pt, ids, S, workspace=ws2), 3)
+    out["prefill_attention_paged"] = {"ms": round(ms_pp, 3),
+                                      "TFLOP/s": round(attn_flops / ms_pp / 1e9, 1),
+                                      "frac_bf16": round(attn_flops / ms_pp / 1e9 / pk["bf16_tflops_sustained"], 4)}
     return out
 
 

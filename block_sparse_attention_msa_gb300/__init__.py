@@ -239,6 +239,41 @@ def sparse_prefill(q, k, v, block_ids, with_lse: bool = True,
     return o, lse
 
 
+def sparse_prefill_paged(q, k_cache, v_cache, page_table, block_ids, S_kv: int,
+                         with_lse: bool = True, workspace: Workspace | None = None, out=None):
+    """Sparse prefill over a paged K/V cache (``msa_sparse_prefill_paged``).
+
+    q [T, Hq, D] bf16 at positions S_kv-T..S_kv-1; k_cache, v_cache [P, 128, Hkv, D] bf16;
+    page_table [ceil(S_kv/128)] int32 (page of each 128-token block); block_ids
+    [T, Hkv, topk] int32. Returns (o [T, Hq, D] bf16, lse [T, Hq] fp32 or None).
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 1)
+    _need(block_ids, "block_ids", torch.int32, 3)
+    T, Hq, D = q.shape
+    P, _, Hkv, _ = k_cache.shape
+    topk = block_ids.shape[2]
+    if v_cache.shape != k_cache.shape or block_ids.shape[:2] != (T, Hkv) \
+            or page_table.numel() < (S_kv + 127) // 128:
+        raise ValueError("sparse_prefill_paged: inconsistent shapes")
+    dev = q.device
+    if out is None:
+        o = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev) if with_lse else None
+    else:
+        o, lse = out
+    lib = load()
+    nbytes = lib.msa_sparse_prefill_workspace_size(T, S_kv, Hq, Hkv, topk)
+    buf = _ws(workspace, dev).get("prefill", nbytes, dev)
+    rc = lib.msa_sparse_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), P,
+                                      _ptr(block_ids), T, S_kv, Hq, Hkv, D, topk, _ptr(o),
+                                      _ptr(lse), _ptr(buf), buf.numel(), _stream(dev))
+    _lib.check("msa_sparse_prefill_paged", rc)
+    return o, lse
+
+
 def prefill_bucket(block_ids, nblk: int, workspace: Workspace | None = None):
     """Invert selections into per-(group, block) lists (``msa_prefill_bucket``).
 

@@ -140,13 +140,23 @@ struct DenseWorkspace {
   uint16_t* part_o;    // chunk-major [16][T*Hkv*G][8] bf16
   float* part_lse;     // [T*Hkv*G]
 };
+// Row of the K/V tensor map that holds token 0 of block j: j*128 for contiguous K/V, else the
+// block's page * 128 (an out-of-range page is reported through `bad` and read as page 0).
+__device__ __forceinline__ int32_t kv_block_row(const int32_t* page_table, int64_t num_pages,
+                                                int32_t j, bool& bad) {
+  if (!page_table) return j * 128;
+  const int32_t pg = page_table[j];
+  bad = pg < 0 || pg >= num_pages;
+  return (bad ? 0 : pg) * 128;
+}
 cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
                                 int32_t G, int32_t topk, const DenseWorkspace& w,
                                 cudaStream_t stream);
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
-                                   int64_t S_kv, int32_t Hkv, int32_t G, const DenseWorkspace& w,
-                                   cudaStream_t stream);
+                                   int64_t S_kv, int32_t Hkv, int32_t G,
+                                   const int32_t* page_table, int64_t num_pages,
+                                   const DenseWorkspace& w, cudaStream_t stream);
 
 // (a) bucketing; tiles of `qpt` queries are laid out for the attention kernel.
 // List of selection (t, slot) of group g: ((g * nwin + t / win) * nblk + j); the per-list
@@ -157,8 +167,10 @@ cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int3
                           int32_t* tile_offsets, cudaStream_t stream);
 struct PrefillArgs {
   const uint16_t* q;           // [T, Hq, D]
-  const uint16_t* k;           // [S_kv, Hkv, D]
+  const uint16_t* k;           // [S_kv, Hkv, D], or paged [num_pages, 128, Hkv, D]
   const uint16_t* v;
+  const int32_t* page_table;   // null (contiguous K/V) or [nblk]: page of each 128-token block
+  int64_t num_pages;
   const int32_t* block_ids;    // [T, Hkv, topk]
   int32_t T, Hq, Hkv, D, topk, nblk;
   int64_t S_kv;

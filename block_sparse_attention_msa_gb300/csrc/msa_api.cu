@@ -207,31 +207,33 @@ size_t msa_sparse_prefill_workspace_size(int32_t T, int64_t S_kv, int32_t Hq, in
   return msa::prefill_ws_layout(T, Hkv, topk, nblk, Hq / Hkv, true).total;
 }
 
-int msa_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hq,
-                       int32_t Hkv, int32_t D, int32_t topk, uint16_t* o, float* lse,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+static int sparse_prefill_impl(const char* name, const uint16_t* q, const uint16_t* k,
+                               const uint16_t* v, const int32_t* page_table, int64_t num_pages,
+                               const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hq,
+                               int32_t Hkv, int32_t D, int32_t topk, uint16_t* o, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   if (T == 0) return ok();
-  if (!q || !k || !v || !block_ids || !o)
-    return fail(MSA_ERR_ARG, "msa_sparse_prefill: null tensor pointer");
+  if (!q || !k || !v || !block_ids || !o) return fail(MSA_ERR_ARG, "%s: null tensor pointer", name);
   if (T < 0 || S_kv < T || topk < 1 || topk > 64)
-    return fail(MSA_ERR_ARG, "msa_sparse_prefill: T=%d S_kv=%lld topk=%d", T, (long long)S_kv,
-                topk);
-  if (S_kv > kInt32Max - 128) return fail(MSA_ERR_UNSUPPORTED, "msa_sparse_prefill: S_kv too large");
-  if (D != 128) return fail(MSA_ERR_UNSUPPORTED, "msa_sparse_prefill: D=%d (only 128)", D);
+    return fail(MSA_ERR_ARG, "%s: T=%d S_kv=%lld topk=%d", name, T, (long long)S_kv, topk);
+  if (S_kv > kInt32Max - 128) return fail(MSA_ERR_UNSUPPORTED, "%s: S_kv too large", name);
+  if (D != 128) return fail(MSA_ERR_UNSUPPORTED, "%s: D=%d (only 128)", name, D);
   if (!pow2_upto(Hkv, 16) || Hq % Hkv != 0 || !pow2_upto(Hq / Hkv, 16))
-    return fail(MSA_ERR_UNSUPPORTED, "msa_sparse_prefill: Hq=%d Hkv=%d", Hq, Hkv);
+    return fail(MSA_ERR_UNSUPPORTED, "%s: Hq=%d Hkv=%d", name, Hq, Hkv);
   if ((int64_t)T * Hkv * topk > kInt32Max)
-    return fail(MSA_ERR_UNSUPPORTED, "msa_sparse_prefill: T*Hkv*topk exceeds int32");
+    return fail(MSA_ERR_UNSUPPORTED, "%s: T*Hkv*topk exceeds int32", name);
+  if (page_table && (num_pages <= 0 || num_pages * 128 > kInt32Max))
+    return fail(MSA_ERR_ARG, "%s: num_pages=%lld", name, (long long)num_pages);
   const size_t need = msa_sparse_prefill_workspace_size(T, S_kv, Hq, Hkv, topk);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
-    return fail(MSA_ERR_WORKSPACE,
-                "msa_sparse_prefill: workspace %p of %zu bytes (need %zu, 256-byte aligned)",
-                workspace, workspace_bytes, need);
+    return fail(MSA_ERR_WORKSPACE, "%s: workspace %p of %zu bytes (need %zu, 256-byte aligned)",
+                name, workspace, workspace_bytes, need);
   msa::PrefillArgs a;
   a.q = q;
   a.k = k;
   a.v = v;
+  a.page_table = page_table;
+  a.num_pages = num_pages;
   a.block_ids = block_ids;
   a.T = T;
   a.Hq = Hq;
@@ -243,7 +245,26 @@ int msa_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   a.o = o;
   a.lse = lse;
   a.workspace = static_cast<uint8_t*>(workspace);
-  return cuda_status(msa::launch_sparse_prefill(a, as_stream(stream)), "msa_sparse_prefill");
+  return cuda_status(msa::launch_sparse_prefill(a, as_stream(stream)), name);
+}
+
+int msa_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hq,
+                       int32_t Hkv, int32_t D, int32_t topk, uint16_t* o, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return sparse_prefill_impl("msa_sparse_prefill", q, k, v, nullptr, 0, block_ids, T, S_kv, Hq,
+                             Hkv, D, topk, o, lse, workspace, workspace_bytes, stream);
+}
+
+int msa_sparse_prefill_paged(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* page_table, int64_t num_pages,
+                             const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hq,
+                             int32_t Hkv, int32_t D, int32_t topk, uint16_t* o, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (T != 0 && !page_table) return fail(MSA_ERR_ARG, "msa_sparse_prefill_paged: null page table");
+  return sparse_prefill_impl("msa_sparse_prefill_paged", q, k_cache, v_cache, page_table,
+                             num_pages, block_ids, T, S_kv, Hq, Hkv, D, topk, o, lse, workspace,
+                             workspace_bytes, stream);
 }
 
 size_t msa_prefill_bucket_workspace_size(int32_t Hkv, int32_t nblk) {

@@ -231,6 +231,8 @@ struct PreKParams {
   // per 8 heads); 0: two 3-D copies per query, one per channel half.
   int32_t q_atoms;
   int64_t q_start;
+  const int32_t* page_table;      // null: contiguous K/V; else the page of each block
+  int64_t num_pages;
   uint16_t* part_o;               // chunk-major [16][part_rows][8] bf16
   int64_t part_rows;               // T*Hkv*topk*G
   float* part_lse;
@@ -386,7 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int g = (int)(gj / lists_per_group), j = gj % p.nblk;
               uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
               mbar_expect_tx(&B.kv_full[c], 4 * kBox);
-              const int tok = j * 128;
+              bool bad = false;
+              const int tok = kv_block_row(p.page_table, p.num_pages, j, bad);
+              if (bad) msa_record_error(kErrBadPage);
               tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
               tma_load_3d(kvb + kBox, &kmap, &B.kv_full[c], 64, g, tok);
               tma_load_3d(kvb + kTileBytes, &vmap, &B.kv_full[c], 0, g, tok);
@@ -681,7 +685,8 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const uint64_t qdims[3] = {(uint64_t)a.D, (uint64_t)a.Hq, (uint64_t)a.T};
   const uint64_t qstrides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hq * a.D * 2};
   const uint32_t qbox[3] = {64, (uint32_t)G, 1};
-  const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.Hkv, (uint64_t)a.S_kv};
+  const uint64_t kv_rows = a.page_table ? (uint64_t)a.num_pages * 128 : (uint64_t)a.S_kv;
+  const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.Hkv, kv_rows};
   const uint64_t strides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hkv * a.D * 2};
   const uint32_t box[3] = {64, 1, 128};
   if ((!q_atoms && !encode_bf16_map(&qmap, a.q, 3, qdims, qstrides, qbox, true)) ||
@@ -706,6 +711,8 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.nwin = nwin;
   p.q_atoms = q_atoms;
   p.q_start = a.S_kv - a.T;
+  p.page_table = a.page_table;
+  p.num_pages = a.num_pages;
   p.part_o = part_o;
   p.part_rows = (int64_t)a.T * a.Hkv * a.topk * G;
   p.part_lse = part_lse;
@@ -721,7 +728,8 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (hybrid) {
-    e = launch_dense_attention(qmap, kmap, vmap, q_atoms, a.T, a.S_kv, a.Hkv, G, dw, stream);
+    e = launch_dense_attention(qmap, kmap, vmap, q_atoms, a.T, a.S_kv, a.Hkv, G, a.page_table,
+                               a.num_pages, dw, stream);
     if (e != cudaSuccess) return e;
   }
   return launch_lse_merge_chunked(part_o, part_lse, ids, hybrid ? dw.part_o : nullptr,

@@ -163,6 +163,8 @@ struct DenseKParams {
   const uint32_t* dmask;
   int32_t T, Hkv, G, qpt, ppg, q_atoms;
   int64_t npairs, q_start;
+  const int32_t* page_table;  // null: contiguous K/V; else the page of each block
+  int64_t num_pages;
   uint16_t* part_o;   // chunk-major [16][part_rows][8] bf16
   int64_t part_rows;  // T*Hkv*G
   float* part_lse;    // [T*Hkv*G]
@@ -252,7 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // load kv_loads goes to buffer kv_loads & 1, free once both O MMAs of load
             // kv_loads - 2 have completed
             if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
-              const int tok = p.dblk[pr * kMaxDense + j] * 128;
+              bool bad = false;
+              const int tok = kv_block_row(p.page_table, p.num_pages, p.dblk[pr * kMaxDense + j], bad);
+              if (bad) msa_record_error(kErrBadPage);
               uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
               mbar_expect_tx(&B.kv_full[c], 4 * kBox);
               tma_load_3d(kvb, &kmap, &B.kv_full[c], 0, g, tok);
@@ -538,8 +542,9 @@ cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_k
 
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
-                                   int64_t S_kv, int32_t Hkv, int32_t G, const DenseWorkspace& w,
-                                   cudaStream_t stream) {
+                                   int64_t S_kv, int32_t Hkv, int32_t G,
+                                   const int32_t* page_table, int64_t num_pages,
+                                   const DenseWorkspace& w, cudaStream_t stream) {
   DenseKParams p;
   p.dcnt = w.dcnt;
   p.dblk = w.dblk;
@@ -552,6 +557,8 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
   p.q_atoms = q_atoms;
   p.npairs = (int64_t)Hkv * p.ppg;
   p.q_start = S_kv - T;
+  p.page_table = page_table;
+  p.num_pages = num_pages;
   p.part_o = w.part_o;
   p.part_rows = (int64_t)T * Hkv * G;
   p.part_lse = w.part_lse;

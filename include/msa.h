@@ -171,7 +171,10 @@ MSA_API int msa_paged_sparse_decode(const uint16_t* q, const uint16_t* k_cache, 
  * group g, query t attends to keys pos <= q_start + t in the blocks block_ids[t, g, :]
  * (-1 entries ignored). Steps, all on the GPU: (a) invert the selections into per-(group,
  * block) query lists, (b) block-major attention writing one partial (O, lse) per
- * (query, group, slot), (c) merge the partials of each (query, head).
+ * (query, group, slot), (c) merge the partials of each (query, head). With G = Hq/Hkv of 8
+ * or 16, the blocks that at least 3/8 of a pair of 128/G-query tiles chose are first taken
+ * out and computed query-major (one partial per (query, head) for all of them); (a)-(b) run
+ * on the remaining selections and (c) merges both.
  *
  *   q     [T, Hq, D] bf16; k, v [S_kv, Hkv, D] bf16 (contiguous K/V of the sequence)
  *   block_ids [T, Hkv, topk] int32, each id -1 or a causal block of its query
@@ -186,6 +189,29 @@ MSA_API int msa_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint1
                        const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hq,
                        int32_t Hkv, int32_t D, int32_t topk, uint16_t* o, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * msa_sparse_prefill over a paged K/V cache: a prefill chunk against a prefix that is
+ * already in the paged cache (chunked prefill), the K/V of every block read through the
+ * page table as in the paged decode.
+ *
+ * Passages: as msa_sparse_prefill; the paged cache and its page table as in
+ * msa_paged_sparse_decode (Together AI MiniMax-M3 serving article, section "MSA needs a new
+ * paged-attention integration").
+ *
+ *   k_cache, v_cache [num_pages, 128, Hkv, D] bf16
+ *   page_table [ceil(S_kv/128)] int32: the page holding tokens 128*j .. 128*j+127 of the
+ *              sequence; each in [0, num_pages) (an out-of-range page is read as page 0 and
+ *              recorded in the device error word); num_pages*128 <= 2^31-1
+ *   everything else, the result and the workspace as msa_sparse_prefill.
+ * Returns MSA_ERR_ARG for a null page table.
+ * ------------------------------------------------------------------------------------ */
+MSA_API int msa_sparse_prefill_paged(const uint16_t* q, const uint16_t* k_cache,
+                                     const uint16_t* v_cache, const int32_t* page_table,
+                                     int64_t num_pages, const int32_t* block_ids, int32_t T,
+                                     int64_t S_kv, int32_t Hq, int32_t Hkv, int32_t D,
+                                     int32_t topk, uint16_t* o, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Step (a) of msa_sparse_prefill on its own: invert the selections.

@@ -86,6 +86,13 @@ def test_argument_validation_rejects_before_launch(lib):
                                   1 << 30, None) == -1
     assert lib.msa_sparse_prefill(FAKE, FAKE, FAKE, FAKE, 100, 200, 64, 8, 256, 16, FAKE, None, ws,
                                   1 << 30, None) == -3
+    # paged prefill: null page table, bad page count, then the shared checks
+    assert lib.msa_sparse_prefill_paged(FAKE, FAKE, FAKE, None, 16, FAKE, 100, 200, 64, 8, 128, 16,
+                                        FAKE, None, ws, 1 << 30, None) == -1
+    assert lib.msa_sparse_prefill_paged(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 100, 200, 64, 8, 128, 16,
+                                        FAKE, None, ws, 1 << 30, None) == -1
+    assert lib.msa_sparse_prefill_paged(FAKE, FAKE, FAKE, FAKE, 16, FAKE, 100, 200, 64, 8, 256, 16,
+                                        FAKE, None, ws, 1 << 30, None) == -3
     # page table: null output
     assert lib.msa_build_sparse_page_table(FAKE, FAKE, FAKE, 1, 1, 8, 16, 4, 4, None, FAKE,
                                            None) == -1

@@ -180,6 +180,38 @@ def test_sparse_prefill_beyond_two_million_tokens():
     check_attention(o, lse, ref, what="prefill past 16384 blocks")
 
 
+@pytest.mark.parametrize("T,prefix,Hq,Hkv,topk,n_shared", [
+    (300, 1000, 64, 8, 8, 6),       # G 8: query-major pass + block-major remainder
+    (200, 333, 16, 4, 4, 0),        # G 4: block-major only; partial last page
+])
+def test_sparse_prefill_paged_equals_contiguous(T, prefix, Hq, Hkv, topk, n_shared):
+    """The paged form reads the same K/V through a shuffled page table: bit-identical to the
+    contiguous form, and within tolerance of the oracle."""
+    S = prefix + T
+    w = workloads.prefill_workload(T, S, Hq, Hkv, 128, topk, seed=13, device="cpu", n_shared=n_shared)
+    nblk = (S + 127) // 128
+    P = nblk + 3                                   # a few unused pages
+    gen = torch.Generator().manual_seed(14)
+    perm = torch.randperm(P, generator=gen)[:nblk].to(torch.int32)
+    pad = nblk * 128 - S
+    def paged(x):
+        xp = torch.cat([x, torch.zeros((pad,) + x.shape[1:], dtype=x.dtype)]).view(nblk, 128, Hkv, 128)
+        cache = workloads.randn_bf16((P, 128, Hkv, 128), gen, "cpu")   # garbage in unused pages
+        cache[perm.long()] = xp
+        return cache
+    kc, vc = paged(w["k"]), paged(w["v"])
+    o_p, lse_p = msa.sparse_prefill_paged(w["q"].to(DEV), kc.to(DEV), vc.to(DEV), perm.to(DEV),
+                                          w["block_ids"].to(DEV), S)
+    o_c, lse_c = msa.sparse_prefill(w["q"].to(DEV), w["k"].to(DEV), w["v"].to(DEV),
+                                    w["block_ids"].to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_c)
+    assert torch.equal(lse_p, lse_c)
+    ref = oracle.sparse_prefill(u16(w["q"]), u16(w["k"]), u16(w["v"]), w["block_ids"].numpy())
+    check_attention(o_p, lse_p, ref, what="paged prefill")
+    assert msa.device_error() == 0
+
+
 def test_prefill_bucket_lists():
     w = workloads.prefill_workload(900, 1500, 16, 4, 128, 6, seed=4, device="cpu", n_shared=3)
     nblk = (1500 + 127) // 128
