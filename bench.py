@@ -485,6 +485,11 @@ def run_cfg5(args, local):
     out["decode_score_topk"] = {"ms": round(ms_s, 4), "GB/s": round(kidx_bytes / ms_s / 1e6, 1),
                                 "frac_hbm": round(kidx_bytes / ms_s / 1e6 / pk["hbm_gbs"], 4)}
     out["decode_page_table_ms"] = round(ms_pt, 4)
+    # the same selection with its page table built in the scorer's tail (one launch)
+    ms_sf = timed(lambda: msa.index_score_topk_page_table(w["q_idx"], w["k_idx_pages"],
+                                                          w["page_table"], w["seq_lens"], 1, k,
+                                                          workspace=ws_), max(3, args.steps))
+    out["decode_score_topk_page_table_fused_ms"] = round(ms_sf, 4)
     out["decode_attention"] = {"ms": round(ms_d, 4), "GB/s": round(kv_bytes / ms_d / 1e6, 1),
                                "frac_hbm": round(kv_bytes / ms_d / 1e6 / pk["hbm_gbs"], 4)}
     del w, ids, fpt, lens

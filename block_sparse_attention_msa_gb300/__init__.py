@@ -116,6 +116,37 @@ def index_score_topk(q_idx, k_idx_pages, page_table, seq_lens, N: int, topk: int
     return ids, sc
 
 
+def index_score_topk_page_table(q_idx, k_idx_pages, page_table, seq_lens, N: int, topk: int,
+                                with_scores: bool = True, workspace: Workspace | None = None):
+    """Selection and its sparse page table in one call (``msa_index_score_topk_page_table``).
+
+    Arguments as ``index_score_topk``. Returns (block_ids [B*N, Hkv, topk] int32, scores or None,
+    flat_page_table [B*N*Hkv, topk] int32, flat_kv_lens [B*N*Hkv] int32).
+    """
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx_pages, "k_idx_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, max_blocks = page_table.shape
+    R, Hkv, Di = q_idx.shape
+    if R != B * N or k_idx_pages.shape[1:] != (BLOCK, Hkv, Di) or seq_lens.numel() != B:
+        raise ValueError("index_score_topk_page_table: inconsistent shapes")
+    dev = q_idx.device
+    ids = torch.empty((R, Hkv, topk), dtype=torch.int32, device=dev)
+    sc = torch.empty((R, Hkv, topk), dtype=torch.float32, device=dev) if with_scores else None
+    fpt = torch.empty((R * Hkv, topk), dtype=torch.int32, device=dev)
+    lens = torch.empty((R * Hkv,), dtype=torch.int32, device=dev)
+    lib = load()
+    nbytes = lib.msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks)
+    buf = _ws(workspace, dev).get("score", nbytes, dev)
+    rc = lib.msa_index_score_topk_page_table(
+        _ptr(q_idx), _ptr(k_idx_pages), _ptr(page_table), _ptr(seq_lens), B, N, Hkv, Di,
+        max_blocks, k_idx_pages.shape[0], topk, _ptr(ids), _ptr(sc), _ptr(fpt), _ptr(lens),
+        _ptr(buf), buf.numel(), _stream(dev))
+    _lib.check("msa_index_score_topk_page_table", rc)
+    return ids, sc, fpt, lens
+
+
 def index_score_topk_noalloc(q_idx, k_idx_pages, page_table, seq_lens, N: int, topk: int,
                              with_scores: bool = True, out=None):
     """``index_score_topk`` without a workspace (``msa_index_score_topk_noalloc``).

@@ -24,6 +24,8 @@ SIGNATURES = [
     ("msa_index_score_topk_workspace_size", SZ, [I32, I32, I32, I32]),
     ("msa_index_score_topk", ctypes.c_int,
      [P, P, P, P, I32, I32, I32, I32, I32, I64, I32, P, P, P, SZ, P]),
+    ("msa_index_score_topk_page_table", ctypes.c_int,
+     [P, P, P, P, I32, I32, I32, I32, I32, I64, I32, P, P, P, P, P, SZ, P]),
     ("msa_index_score_topk_noalloc", ctypes.c_int,
      [P, P, P, P, I32, I32, I32, I32, I32, I64, I32, P, P, P]),
     ("msa_build_sparse_page_table", ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, I64, P, P, P]),

@@ -20,6 +20,8 @@ struct ScoreArgs {
   float* sel_scores;           // [B*N, Hkv, topk] or null
   float* scores;               // workspace [B*N, Hkv, max_blocks]
   int32_t* tickets;            // workspace [B], cleared by the launcher before each call
+  int32_t* fpt = nullptr;      // optional: sparse page table [B*N*Hkv, topk] (decode scorer's
+  int32_t* fpt_lens = nullptr; //   tail builds it with the selection) and lengths [B*N*Hkv]
 };
 // Streaming scorer for N <= kDecodeMaxN with the top-k fused into the last CTA per request.
 constexpr int kDecodeMaxN = 8;

@@ -67,32 +67,34 @@ size_t msa_index_score_topk_workspace_size(int32_t B, int32_t N, int32_t Hkv, in
   return score_ws_scores_bytes(B, N, Hkv, max_blocks) + msa::ws_align((size_t)B * sizeof(int32_t));
 }
 
-int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pages,
-                         const int32_t* page_table, const int32_t* seq_lens, int32_t B,
-                         int32_t N, int32_t Hkv, int32_t Di, int32_t max_blocks,
-                         int64_t num_pages, int32_t topk, int32_t* block_ids, float* scores,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+static int index_score_topk_impl(const char* name, const uint16_t* q_idx,
+                                 const uint16_t* k_idx_pages, const int32_t* page_table,
+                                 const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,
+                                 int32_t Di, int32_t max_blocks, int64_t num_pages, int32_t topk,
+                                 int32_t* block_ids, float* scores, int32_t* fpt,
+                                 int32_t* fpt_lens, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
   if (B == 0 || N == 0) return ok();
   if (!q_idx || !k_idx_pages || !page_table || !seq_lens || !block_ids)
-    return fail(MSA_ERR_ARG, "msa_index_score_topk: null tensor pointer");
+    return fail(MSA_ERR_ARG, "%s: null tensor pointer", name);
   if (B < 0 || N < 0 || max_blocks <= 0 || num_pages <= 0)
-    return fail(MSA_ERR_ARG, "msa_index_score_topk: B=%d N=%d max_blocks=%d num_pages=%lld", B, N,
+    return fail(MSA_ERR_ARG, "%s: B=%d N=%d max_blocks=%d num_pages=%lld", name, B, N,
                 max_blocks, (long long)num_pages);
   if (topk < 2 || topk > 64)
-    return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk: topk=%d outside [2, 64]", topk);
-  if (!pow2_upto(Hkv, 16)) return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk: Hkv=%d", Hkv);
-  if (Di != 64 && Di != 128) return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk: Di=%d", Di);
+    return fail(MSA_ERR_UNSUPPORTED, "%s: topk=%d outside [2, 64]", name, topk);
+  if (!pow2_upto(Hkv, 16)) return fail(MSA_ERR_UNSUPPORTED, "%s: Hkv=%d", name, Hkv);
+  if (Di != 64 && Di != 128) return fail(MSA_ERR_UNSUPPORTED, "%s: Di=%d", name, Di);
   if (num_pages * 128 * Hkv > kInt32Max)
-    return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk: num_pages*128*Hkv exceeds int32");
+    return fail(MSA_ERR_UNSUPPORTED, "%s: num_pages*128*Hkv exceeds int32", name);
   if ((int64_t)max_blocks * 128 > kInt32Max || (int64_t)B * N > kInt32Max)
-    return fail(MSA_ERR_SHAPE, "msa_index_score_topk: sizes exceed int32");
+    return fail(MSA_ERR_SHAPE, "%s: sizes exceed int32", name);
   if ((int64_t)N > (int64_t)max_blocks * 128)
-    return fail(MSA_ERR_SHAPE, "msa_index_score_topk: N=%d exceeds max_blocks*128", N);
+    return fail(MSA_ERR_SHAPE, "%s: N=%d exceeds max_blocks*128", name, N);
   const size_t need = msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(MSA_ERR_WORKSPACE,
-                "msa_index_score_topk: workspace %p of %zu bytes (need %zu, 256-byte aligned)",
-                workspace, workspace_bytes, need);
+                "%s: workspace %p of %zu bytes (need %zu, 256-byte aligned)", name, workspace,
+                workspace_bytes, need);
   msa::ScoreArgs a;
   a.q_idx = q_idx;
   a.k_idx = k_idx_pages;
@@ -107,6 +109,8 @@ int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pages,
   a.num_pages = num_pages;
   a.block_ids = block_ids;
   a.sel_scores = scores;
+  a.fpt = fpt;
+  a.fpt_lens = fpt_lens;
   // workspace: per-request tickets [B] int32 first, then the block scores
   a.tickets = reinterpret_cast<int32_t*>(workspace);
   a.scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -116,12 +120,39 @@ int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pages,
   if (N <= msa::kDecodeMaxN && nstage >= 2) {
     // the fused top-k counts finished pages per request from zero
     cudaError_t e = cudaMemsetAsync(a.tickets, 0, (size_t)B * sizeof(int32_t), as_stream(stream));
-    if (e == cudaSuccess) e = msa::launch_score_decode(a, as_stream(stream));
-    return cuda_status(e, "msa_index_score_topk");
+    if (e == cudaSuccess) e = msa::launch_score_decode(a, as_stream(stream));  // + page table
+    return cuda_status(e, name);
   }
   cudaError_t e = msa::launch_score_rows(a, as_stream(stream));
   if (e == cudaSuccess) e = msa::launch_topk_rows(a, as_stream(stream));
-  return cuda_status(e, "msa_index_score_topk");
+  if (e == cudaSuccess && fpt)
+    e = msa::launch_build_page_table(block_ids, page_table, seq_lens, B, N, Hkv, topk, max_blocks,
+                                     num_pages, fpt, fpt_lens, as_stream(stream));
+  return cuda_status(e, name);
+}
+
+int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                         const int32_t* page_table, const int32_t* seq_lens, int32_t B,
+                         int32_t N, int32_t Hkv, int32_t Di, int32_t max_blocks,
+                         int64_t num_pages, int32_t topk, int32_t* block_ids, float* scores,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return index_score_topk_impl("msa_index_score_topk", q_idx, k_idx_pages, page_table, seq_lens,
+                               B, N, Hkv, Di, max_blocks, num_pages, topk, block_ids, scores,
+                               nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int msa_index_score_topk_page_table(const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                                    const int32_t* page_table, const int32_t* seq_lens, int32_t B,
+                                    int32_t N, int32_t Hkv, int32_t Di, int32_t max_blocks,
+                                    int64_t num_pages, int32_t topk, int32_t* block_ids,
+                                    float* scores, int32_t* flat_page_table, int32_t* flat_kv_lens,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (B != 0 && N != 0 && (!flat_page_table || !flat_kv_lens))
+    return fail(MSA_ERR_ARG, "msa_index_score_topk_page_table: null page-table output");
+  return index_score_topk_impl("msa_index_score_topk_page_table", q_idx, k_idx_pages, page_table,
+                               seq_lens, B, N, Hkv, Di, max_blocks, num_pages, topk, block_ids,
+                               scores, flat_page_table, flat_kv_lens, workspace, workspace_bytes,
+                               stream);
 }
 
 // ------------------------------------------------------------------------------ page table

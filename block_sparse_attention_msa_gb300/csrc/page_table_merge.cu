@@ -14,6 +14,7 @@
 // written as bf16 with its fp32 LSE.
 #include "common.cuh"
 #include "kernels.h"
+#include "page_table_row.cuh"
 
 MSA_DEFINE_ERROR_WORD(ptm)
 
@@ -35,29 +36,10 @@ __global__ void __launch_bounds__(256)
   bool bad = false;
   const int q_pos = clamp_seq(seq_lens, (int)b, N, max_blocks, bad) - N + (int)(r % N);
   if (bad && lane == 0 && g == 0) msa_record_error(kErrBadBlock);
-  const int local = q_pos / MSA_BLOCK_TOKENS;
-  int len = 0;
-  for (int i = lane; i < topk; i += 32) {
-    const int32_t j = block_ids[f * topk + i];
-    int32_t v = -1;
-    if (j >= 0) {
-      if (j > local || j >= max_blocks) {
-        msa_record_error(kErrBadBlock);
-      } else {
-        const int32_t p = page_table[b * max_blocks + j];
-        if (p < 0 || p >= num_pages) {
-          msa_record_error(kErrBadPage);
-        } else {
-          v = (int32_t)((int64_t)p * MSA_BLOCK_TOKENS * Hkv + g);
-          len += (j == local) ? (q_pos % MSA_BLOCK_TOKENS) + 1 : MSA_BLOCK_TOKENS;
-        }
-      }
-    }
-    fpt[f * topk + i] = v;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) len += __shfl_xor_sync(0xffffffffu, len, o);
-  if (lane == 0) lens[f] = len;
+  const uint32_t err = warp_flat_page_table_row(block_ids + f * topk, page_table + b * max_blocks,
+                                                q_pos, Hkv, g, topk, max_blocks, num_pages,
+                                                fpt + f * topk, lens + f);
+  if (err) msa_record_error(err);
 }
 
 // One warp per (unit u, head e). Lane s < S loads partial s's LSE (and skip id) and turns it

@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "page_table_row.cuh"
 
 MSA_DEFINE_ERROR_WORD(score)
 
@@ -188,6 +189,8 @@ struct DecodeKParams {
   float* sel_scores;
   float* scores;
   int32_t* tickets;
+  int32_t* fpt;        // optional: flat page table [B*N*Hkv, topk] built in the tail (row a3)
+  int32_t* fpt_lens;   // optional: [B*N*Hkv]
 };
 
 __device__ __forceinline__ void consumer_sync() {
@@ -340,6 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t orow = (r * Hkv + gg) * p.topk;
         warp_topk(p.scores + (r * Hkv + gg) * p.max_blocks, qp / 128, p.topk, p.block_ids + orow,
                   p.sel_scores ? p.sel_scores + orow : nullptr, stopk[warp]);
+        if (p.fpt) {
+          // the sparse page table row of the selection just written (same warp: ordered by
+          // the warp barrier)
+          __syncwarp();
+          const uint32_t err = warp_flat_page_table_row(
+              p.block_ids + orow, p.page_table + (int64_t)rb * p.max_blocks, qp, Hkv, gg, p.topk,
+              p.max_blocks, p.num_pages, p.fpt + orow, p.fpt_lens + r * Hkv + gg);
+          if (err) msa_record_error(err);
+        }
       }
     }
     consumer_sync();
@@ -765,6 +777,8 @@ cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
   p.sel_scores = a.sel_scores;
   p.scores = a.scores;
   p.tickets = a.tickets;
+  p.fpt = a.fpt;
+  p.fpt_lens = a.fpt_lens;
   const int grid = sm_count();
   auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -106,6 +106,30 @@ MSA_API int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pa
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * msa_index_score_topk followed by msa_build_sparse_page_table on its selection, in one
+ * call: for N <= 8 the warp that selects a row's blocks in the scorer's last CTA for the
+ * request also writes the row's sparse page table and length, so no separate launch and no
+ * round trip of block_ids sits between the selection and the paged decode.
+ *
+ * Passages: as msa_index_score_topk and msa_build_sparse_page_table (Together AI MiniMax-M3
+ * serving article, sections "The index scorer becomes the decode critical path" and "MSA
+ * needs a new paged-attention integration"; the pages list top-k and the page-table build
+ * among the small kernels around the attention).
+ *
+ *   arguments as msa_index_score_topk, plus
+ *   flat_page_table [B*N*Hkv, topk] int32 (out), flat_kv_lens [B*N*Hkv] int32 (out), exactly
+ *   as msa_build_sparse_page_table(block_ids, page_table, seq_lens, ...) would write them.
+ * Returns MSA_ERR_ARG for a null page-table output; otherwise as msa_index_score_topk.
+ * ------------------------------------------------------------------------------------ */
+MSA_API int msa_index_score_topk_page_table(const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                                            const int32_t* page_table, const int32_t* seq_lens,
+                                            int32_t B, int32_t N, int32_t Hkv, int32_t Di,
+                                            int32_t max_blocks, int64_t num_pages, int32_t topk,
+                                            int32_t* block_ids, float* scores,
+                                            int32_t* flat_page_table, int32_t* flat_kv_lens,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Sparse page table for paged decode.
  *
  * Passage: Together AI MiniMax-M3 serving article, section "MSA needs a new paged-attention

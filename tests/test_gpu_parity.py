@@ -91,6 +91,28 @@ def test_score_topk_workspace_reuse_and_ties():
         assert np.array_equal(ids.cpu().numpy(), ids_ref)
 
 
+@pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
+    ([5000, 129, 3000, 777], 1, 8, 128, 16),     # decode: page table built in the scorer's tail
+    ([2500, 1400], 4, 4, 64, 8),                  # multi-token rows, still the fused tail
+    ([2048, 1500], 33, 2, 128, 5),                # long rows: scorer, top-k, page-table kernels
+])
+def test_index_score_topk_page_table_equals_the_two_calls(seq_lens, N, Hkv, Di, topk):
+    w = workloads.index_workload(seq_lens, N, Hkv, Di, seed=31, device="cpu")
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    args = (d["q_idx"], d["k_idx_pages"], d["page_table"], d["seq_lens"], N, topk)
+    ids_f, sc_f, fpt_f, lens_f = msa.index_score_topk_page_table(*args)
+    ids, sc = msa.index_score_topk(*args)
+    fpt, lens = msa.build_sparse_page_table(ids, d["page_table"], d["seq_lens"], N,
+                                            d["k_idx_pages"].shape[0])
+    torch.cuda.synchronize()
+    assert torch.equal(ids_f, ids) and torch.equal(sc_f, sc)
+    assert torch.equal(fpt_f, fpt) and torch.equal(lens_f, lens)
+    fpt_ref, lens_ref = oracle.build_sparse_page_table(ids.cpu().numpy(), w["page_table"].numpy(),
+                                                       w["seq_lens"].numpy(), N)
+    assert np.array_equal(fpt_f.cpu().numpy(), fpt_ref) and np.array_equal(lens_f.cpu().numpy(), lens_ref)
+    assert msa.device_error() == 0
+
+
 @pytest.mark.parametrize("N", [1, 3])
 def test_sparse_page_table_bit_exact(N):
     w = workloads.decode_workload([517, 1500, 129, 9000], N, 16, 8, 128, 7, seed=2, device="cpu")
