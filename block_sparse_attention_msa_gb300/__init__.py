@@ -206,6 +206,35 @@ def build_sparse_page_table(block_ids, page_table, seq_lens, N: int, num_pages: 
 
 # ------------------------------------------------------------------------------ stage 2
 
+def stage_selected_kv(k_cache, v_cache, flat_page_table):
+    """Copy the selected blocks' K/V to a device staging cache (``msa_stage_selected_kv``).
+
+    k_cache, v_cache [P, 128, Hkv, D] bf16: CUDA tensors or pinned host tensors (read by the
+    device directly); flat_page_table [R*Hkv, topk] int32 (CUDA). Returns (k_stage, v_stage
+    [R*topk, 128, Hkv, D] bf16, stage_page_table [R*Hkv, topk] int32) for ``paged_sparse_decode``.
+    """
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name}: must be a CUDA tensor or pinned host memory")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous bf16 [P, 128, Hkv, D] tensor")
+    _need(flat_page_table, "flat_page_table", torch.int32, 2)
+    P, _, Hkv, D = k_cache.shape
+    RH, topk = flat_page_table.shape
+    if v_cache.shape != k_cache.shape or RH % Hkv:
+        raise ValueError("stage_selected_kv: inconsistent shapes")
+    R = RH // Hkv
+    dev = flat_page_table.device
+    k_stage = torch.empty((R * topk, BLOCK, Hkv, D), dtype=torch.bfloat16, device=dev)
+    v_stage = torch.empty_like(k_stage)
+    spt = torch.empty_like(flat_page_table)
+    rc = load().msa_stage_selected_kv(k_cache.data_ptr(), v_cache.data_ptr(), P,
+                                      _ptr(flat_page_table), R, Hkv, D, topk, _ptr(k_stage),
+                                      _ptr(v_stage), _ptr(spt), _stream(dev))
+    _lib.check("msa_stage_selected_kv", rc)
+    return k_stage, v_stage, spt
+
+
 def paged_sparse_decode(q, k_cache, v_cache, flat_page_table, flat_kv_lens,
                         with_lse: bool = True, workspace: Workspace | None = None, out=None):
     """Paged sparse decode attention (``msa_paged_sparse_decode``).

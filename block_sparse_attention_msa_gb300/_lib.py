@@ -29,6 +29,7 @@ SIGNATURES = [
     ("msa_index_score_topk_noalloc", ctypes.c_int,
      [P, P, P, P, I32, I32, I32, I32, I32, I64, I32, P, P, P]),
     ("msa_build_sparse_page_table", ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, I64, P, P, P]),
+    ("msa_stage_selected_kv", ctypes.c_int, [P, P, I64, P, I32, I32, I32, I32, P, P, P, P]),
     ("msa_paged_sparse_decode_workspace_size", SZ, [I32, I32, I32, I32]),
     ("msa_paged_sparse_decode", ctypes.c_int,
      [P, P, P, P, P, I32, I32, I32, I32, I32, I64, P, P, P, SZ, P]),

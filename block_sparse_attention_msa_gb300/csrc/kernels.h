@@ -55,6 +55,15 @@ struct DecodeArgs {
 void decode_split(int32_t topk, int32_t* nsplit, int32_t* pages_per_split);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// ------------------------------------------------------------------ KV residency split
+// Copies the K/V rows of every selected (row f, slot i) from the (host-resident) paged caches
+// into staging page (f/Hkv)*topk + i, group f%Hkv, of k_dst/v_dst [R*topk, 128, Hkv, D], and
+// writes the staging flat page table [R*Hkv, topk] (-1 where fpt is -1).
+cudaError_t launch_stage_kv(const uint16_t* k_src, const uint16_t* v_src, int64_t num_pages,
+                            const int32_t* fpt, int32_t R, int32_t Hkv, int32_t topk,
+                            uint16_t* k_dst, uint16_t* v_dst, int32_t* stage_fpt,
+                            cudaStream_t stream);
+
 // ------------------------------------------------------------------ LSE merge
 // skip_ids: optional [U, S]; partial s of unit u is ignored when skip_ids[u*S+s] < 0.
 cudaError_t launch_lse_merge(const void* o_parts, bool parts_bf16, const float* lse_parts,

@@ -18,6 +18,7 @@ cudaError_t msa_read_error_ptm(uint32_t* w);
 cudaError_t msa_read_error_dec(uint32_t* w);
 cudaError_t msa_read_error_pre(uint32_t* w);
 cudaError_t msa_read_error_dense(uint32_t* w);
+cudaError_t msa_read_error_stage(uint32_t* w);
 
 namespace {
 
@@ -176,6 +177,27 @@ int msa_build_sparse_page_table(const int32_t* block_ids, const int32_t* page_ta
                                                   max_blocks, num_pages, flat_page_table,
                                                   flat_kv_lens, as_stream(stream)),
                      "msa_build_sparse_page_table");
+}
+
+// ------------------------------------------------------------------------------ KV staging
+int msa_stage_selected_kv(const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_pages,
+                          const int32_t* flat_page_table, int32_t R, int32_t Hkv, int32_t D,
+                          int32_t topk, uint16_t* k_stage, uint16_t* v_stage,
+                          int32_t* stage_page_table, void* stream) {
+  if (R == 0) return ok();
+  if (!k_cache || !v_cache || !flat_page_table || !k_stage || !v_stage || !stage_page_table)
+    return fail(MSA_ERR_ARG, "msa_stage_selected_kv: null pointer");
+  if (R < 0 || num_pages <= 0 || topk < 1 || topk > 64)
+    return fail(MSA_ERR_ARG, "msa_stage_selected_kv: R=%d num_pages=%lld topk=%d", R,
+                (long long)num_pages, topk);
+  if (D != 128) return fail(MSA_ERR_UNSUPPORTED, "msa_stage_selected_kv: D=%d (only 128)", D);
+  if (!pow2_upto(Hkv, 16)) return fail(MSA_ERR_UNSUPPORTED, "msa_stage_selected_kv: Hkv=%d", Hkv);
+  if (num_pages * 128 * Hkv > kInt32Max || (int64_t)R * topk * 128 * Hkv > kInt32Max)
+    return fail(MSA_ERR_UNSUPPORTED, "msa_stage_selected_kv: pages*128*Hkv exceeds int32");
+  return cuda_status(msa::launch_stage_kv(k_cache, v_cache, num_pages, flat_page_table, R, Hkv,
+                                          topk, k_stage, v_stage, stage_page_table,
+                                          as_stream(stream)),
+                     "msa_stage_selected_kv");
 }
 
 // ------------------------------------------------------------------------------ decode
@@ -404,7 +426,7 @@ int msa_device_error(uint32_t* word) {
   uint32_t all = 0, w = 0;
   cudaError_t (*readers[])(uint32_t*) = {msa_read_error_score, msa_read_error_ptm,
                                          msa_read_error_dec, msa_read_error_pre,
-                                         msa_read_error_dense};
+                                         msa_read_error_dense, msa_read_error_stage};
   for (auto rd : readers) {
     w = 0;
     e = rd(&w);

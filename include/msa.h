@@ -156,6 +156,35 @@ MSA_API int msa_build_sparse_page_table(const int32_t* block_ids, const int32_t*
                                 int32_t* flat_page_table, int32_t* flat_kv_lens, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * KV residency split: copy only the selected blocks' K/V to the device.
+ *
+ * Passages: Together AI MiniMax-M3 serving article, sections "The index scorer becomes the
+ * decode critical path" (the scorer reads the small key index of every block; the attention
+ * needs only the selected blocks) and "MSA needs a new paged-attention integration" (the
+ * selection as a page table over the strided per-head view).
+ *
+ * The paged caches may live in host memory (pinned, so that the device can read it: on a
+ * Grace host over NVLink-C2C) while the key index and the scorer stay on the device. For every
+ * flattened row f = r*Hkv + g and slot i with flat_page_table[f, i] = p*128*Hkv + g >= 0, the
+ * 128 token rows of group g of page p are copied from k_cache / v_cache to staging page
+ * r*topk + i, group slot g, of k_stage / v_stage, and stage_page_table[f, i] = (r*topk + i)*
+ * 128*Hkv + g (-1 where the input is -1). msa_paged_sparse_decode(q, k_stage, v_stage,
+ * stage_page_table, flat_kv_lens, R, Hq, Hkv, D, topk, R*topk, ...) then gives the same result
+ * as on the full caches.
+ *
+ *   k_cache, v_cache [num_pages, 128, Hkv, D] bf16 (device or device-readable host memory)
+ *   flat_page_table  [R*Hkv, topk] int32 (from msa_build_sparse_page_table)
+ *   k_stage, v_stage [R*topk, 128, Hkv, D] bf16 device (out; rows of unselected slots untouched)
+ *   stage_page_table [R*Hkv, topk] int32 device (out)
+ * A virtual page outside the caches or of another group is recorded in the device error
+ * word (kErrBadPage) and staged as -1.
+ * ------------------------------------------------------------------------------------ */
+MSA_API int msa_stage_selected_kv(const uint16_t* k_cache, const uint16_t* v_cache,
+                                  int64_t num_pages, const int32_t* flat_page_table, int32_t R,
+                                  int32_t Hkv, int32_t D, int32_t topk, uint16_t* k_stage,
+                                  uint16_t* v_stage, int32_t* stage_page_table, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Paged sparse decode attention over the strided per-head view.
  *
  * Passages: Together AI MiniMax-M3 serving article, sections "MSA needs a new

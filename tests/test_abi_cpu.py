@@ -93,6 +93,11 @@ def test_argument_validation_rejects_before_launch(lib):
                                         FAKE, None, ws, 1 << 30, None) == -1
     assert lib.msa_sparse_prefill_paged(FAKE, FAKE, FAKE, FAKE, 16, FAKE, 100, 200, 64, 8, 256, 16,
                                         FAKE, None, ws, 1 << 30, None) == -3
+    # KV staging: null stage output, D
+    assert lib.msa_stage_selected_kv(FAKE, FAKE, 16, FAKE, 4, 8, 128, 16, FAKE, None, FAKE,
+                                     None) == -1
+    assert lib.msa_stage_selected_kv(FAKE, FAKE, 16, FAKE, 4, 8, 64, 16, FAKE, FAKE, FAKE,
+                                     None) == -3
     # page table: null output
     assert lib.msa_build_sparse_page_table(FAKE, FAKE, FAKE, 1, 1, 8, 16, 4, 4, None, FAKE,
                                            None) == -1

@@ -234,6 +234,29 @@ def test_sparse_prefill_paged_equals_contiguous(T, prefix, Hq, Hkv, topk, n_shar
     assert msa.device_error() == 0
 
 
+@pytest.mark.parametrize("host", [True, False])
+def test_staged_kv_decode_equals_decode_on_the_full_cache(host):
+    """Selected blocks' K/V copied from the paged caches (pinned host memory or device) to a
+    staging cache: the paged decode on it equals the decode on the full caches (LSE bit for bit;
+    O to one bf16 ulp: the decode sums its warps' partials with shared-memory atomics, whose
+    order varies from run to run)."""
+    w = workloads.decode_workload([517, 1500, 129, 9000], 2, 32, 8, 128, 7, seed=9, device="cpu")
+    kc = w["k_cache"].pin_memory() if host else w["k_cache"].to(DEV)
+    vc = w["v_cache"].pin_memory() if host else w["v_cache"].to(DEV)
+    fpt, lens = msa.build_sparse_page_table(w["block_ids"].to(DEV), w["page_table"].to(DEV),
+                                            w["seq_lens"].to(DEV), 2, w["num_pages"])
+    ks, vs, spt = msa.stage_selected_kv(kc, vc, fpt)
+    q = w["q"].to(DEV)
+    o_s, lse_s = msa.paged_sparse_decode(q, ks, vs, spt, lens)
+    o_f, lse_f = msa.paged_sparse_decode(q, w["k_cache"].to(DEV), w["v_cache"].to(DEV), fpt, lens)
+    torch.cuda.synchronize()
+    assert torch.equal(lse_s, lse_f)
+    a, b = o_s.float(), o_f.float()
+    assert ((a - b).abs() <= b.abs() * 2.0 ** -7 + 1e-6).all()
+    assert torch.equal(spt < 0, fpt < 0)
+    assert msa.device_error() == 0
+
+
 def test_prefill_bucket_lists():
     w = workloads.prefill_workload(900, 1500, 16, 4, 128, 6, seed=4, device="cpu", n_shared=3)
     nblk = (1500 + 127) // 128
