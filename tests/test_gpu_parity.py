@@ -147,6 +147,8 @@ def test_paged_sparse_decode(seq_lens, N, Hq, Hkv, topk):
     (1000, 1000, 64, 8, 16, 12),    # causal, cfg3 structure at small T
     (200, 200, 8, 8, 3, 0),         # G 1
     (129, 5000, 32, 2, 8, 4),       # G 16, long prefix
+    (257, 800, 8, 4, 5, 3),         # G 2: block-major only
+    (1, 4000, 64, 8, 16, 12),       # one query after a prefix: a pair with one valid query
 ])
 def test_sparse_prefill(T, S, Hq, Hkv, topk, n_shared):
     w = workloads.prefill_workload(T, S, Hq, Hkv, 128, topk, seed=11, device="cpu", n_shared=n_shared)
