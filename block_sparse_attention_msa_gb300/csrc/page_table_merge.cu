@@ -139,10 +139,12 @@ __global__ void __launch_bounds__(256)
 // Prefill merge over chunk-major partials: part_o[c][row][8] bf16 with c = 16 channel chunks
 // and row = (u*S + s)*G + e; one warp per unit u (all G heads). Lane slot idx = lane + 32*r
 // covers head idx % G and chunk idx / G, so for a fixed r the lanes of one chunk plane read the
-// G adjacent rows of a partial: 16*G contiguous bytes. The valid slots (ids >= 0) are found
-// with one ballot; their partials stream two at a time (loads of both issued together) into
-// accumulators kept relative to a running max, rescaled when the max grows. The optional
-// query-major partial (dense_o / dense_lse, one per unit and head) is the first "slot".
+// G adjacent rows of a partial: 16*G contiguous bytes. The stream is latency-bound, so the
+// dependent round trips per unit are kept few: the ids, every slot's LSE (staged in shared
+// memory) and the query-major LSE are requested together; then the valid partials, the
+// query-major one (dense_o / dense_lse, one per unit and head) first, stream NB at a time with
+// all their loads in flight at once, into accumulators kept relative to a running max that are
+// rescaled when the max grows.
 template <int G>
 __device__ __forceinline__ void merge_fma(float (&acc)[(G * 16 + 31) / 32][8], float w,
                                           const uint4 (&v)[(G * 16 + 31) / 32]) {
@@ -160,78 +162,100 @@ __device__ __forceinline__ void merge_fma(float (&acc)[(G * 16 + 31) / 32][8], f
 }
 
 template <int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, G >= 16 ? 1 : 2)
     lse_merge_chunked_kernel(const uint4* __restrict__ part_o, int64_t part_rows,
                              const float* __restrict__ lse_parts, const int32_t* __restrict__ ids,
                              const uint4* __restrict__ dense_o, const float* __restrict__ dense_lse,
                              int64_t U, int32_t S, uint16_t* __restrict__ o, float* __restrict__ lse) {
   constexpr int R = (G * 16 + 31) / 32;  // chunk slots per lane
+  constexpr int NB = R >= 8 ? 2 : 3;     // partials per batch of loads
+  extern __shared__ float s_lse[];       // [8 warps][S*G]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = (int64_t)blockIdx.x * 8 + warp;
   if (u >= U) return;
   const int e = lane % G;
-  // valid slots of the unit (S <= 64)
-  uint64_t vmask = 0;
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s = s0 + lane;
-    const bool ok = s < S && __ldg(ids + u * S + s) >= 0;
-    vmask |= (uint64_t)__ballot_sync(0xffffffffu, ok) << s0;
+  const int SG = S * G;
+  float* wl = s_lse + warp * SG;
+  // first round trip: ids (S <= 64), the LSE of every slot, the query-major LSE
+  const int id0 = lane < S ? __ldg(ids + u * S + lane) : -1;
+  const int id1 = lane + 32 < S ? __ldg(ids + u * S + lane + 32) : -1;
+  const float ld = dense_lse ? __ldg(dense_lse + u * G + e) : -INFINITY;
+  for (int i0 = 0; i0 < SG; i0 += 128) {
+    float t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + lane + 32 * k;
+      t[k] = i < SG ? __ldg(lse_parts + u * SG + i) : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + lane + 32 * k;
+      if (i < SG) wl[i] = t[k];
+    }
   }
+  uint64_t vmask = (uint64_t)__ballot_sync(0xffffffffu, id0 >= 0) |
+                   ((uint64_t)__ballot_sync(0xffffffffu, id1 >= 0) << 32);
+  __syncwarp();
   float acc[R][8];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[r][x] = 0.f;
-  float m = -INFINITY, total = 0.f;  // acc and total are relative to 2^(m) in natural units
-  auto rescale_to = [&](float m_new) {
-    const float sc = m == -INFINITY ? 0.f : __expf(m - m_new);
+  float m = -INFINITY, total = 0.f;  // acc and total are relative to e^m
+  bool dense_pending = dense_lse != nullptr;
+  while (vmask || dense_pending) {
+    const uint4* base[NB];
+    int64_t stride[NB];
+    float l[NB];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int k = 0; k < NB; ++k) {
+      base[k] = nullptr;
+      stride[k] = 0;
+      l[k] = -INFINITY;
+      if (dense_pending) {
+        dense_pending = false;
+        base[k] = dense_o + u * G + e;
+        stride[k] = U * G;
+        l[k] = ld;
+      } else if (vmask) {
+        const int s = __ffsll((long long)vmask) - 1;
+        vmask &= vmask - 1;
+        base[k] = part_o + (u * S + s) * G + e;
+        stride[k] = part_rows;
+        l[k] = wl[s * G + e];
+      }
+    }
+    uint4 v[NB][R];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) acc[r][x] *= sc;
-    total *= sc;
-    m = m_new;
-  };
-  if (dense_lse) {
-    const float ld = dense_lse[u * G + e];
-    if (ld != -INFINITY) {
-      uint4 v[R];
+    for (int k = 0; k < NB; ++k)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int idx = lane + 32 * r;
-        v[r] = idx < G * 16 ? __ldcs(dense_o + (int64_t)(idx / G) * (U * G) + u * G + e)
-                            : make_uint4(0u, 0u, 0u, 0u);
+        v[k][r] = base[k] && idx < G * 16 ? __ldcs(base[k] + (int64_t)(idx / G) * stride[k])
+                                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      m = ld;
-      total = 1.f;
-      merge_fma<G>(acc, 1.f, v);
-    }
-  }
-  while (vmask) {
-    const int sa = __ffsll((long long)vmask) - 1;
-    vmask &= vmask - 1;
-    const int sb = vmask ? __ffsll((long long)vmask) - 1 : -1;
-    if (sb >= 0) vmask &= vmask - 1;
-    const int64_t ra = (u * S + sa) * G + e;
-    const int64_t rb = sb >= 0 ? (u * S + sb) * G + e : ra;
-    const float la = lse_parts[ra];
-    const float lb = sb >= 0 ? lse_parts[rb] : -INFINITY;
-    uint4 va[R], vb[R];
+    float mx = l[0];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int idx = lane + 32 * r;
-      const bool in = idx < G * 16;
-      va[r] = in ? __ldcs(part_o + (int64_t)(idx / G) * part_rows + ra) : make_uint4(0u, 0u, 0u, 0u);
-      vb[r] = in && sb >= 0 ? __ldcs(part_o + (int64_t)(idx / G) * part_rows + rb)
-                            : make_uint4(0u, 0u, 0u, 0u);
-    }
-    const float mx = fmaxf(la, lb);
+    for (int k = 1; k < NB; ++k) mx = fmaxf(mx, l[k]);
     if (mx == -INFINITY) continue;
-    if (mx > m) rescale_to(mx);
-    const float wa = __expf(la - m), wb = lb == -INFINITY ? 0.f : __expf(lb - m);
-    total += wa + wb;
-    merge_fma<G>(acc, wa, va);
-    merge_fma<G>(acc, wb, vb);
+    if (mx > m) {
+      const float sc = m == -INFINITY ? 0.f : __expf(m - mx);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int x = 0; x < 8; ++x) acc[r][x] *= sc;
+      total *= sc;
+      m = mx;
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      // a partial with LSE -inf contributes nothing; its rows may never have been written
+      if (l[k] != -INFINITY) {
+        const float w = __expf(l[k] - m);
+        total += w;
+        merge_fma<G>(acc, w, v[k]);
+      }
+    }
   }
   const float inv = total > 0.f ? 1.0f / total : 0.f;
 #pragma unroll
@@ -259,12 +283,13 @@ cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
   const int64_t rows = U * S * G;
   const uint4* po = reinterpret_cast<const uint4*>(part_o);
   const uint4* pd = reinterpret_cast<const uint4*>(dense_o);
+  const size_t smem = (size_t)8 * S * G * sizeof(float);
   switch (G) {
-    case 1: lse_merge_chunked_kernel<1><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 2: lse_merge_chunked_kernel<2><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 4: lse_merge_chunked_kernel<4><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 8: lse_merge_chunked_kernel<8><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 16: lse_merge_chunked_kernel<16><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 1: lse_merge_chunked_kernel<1><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 2: lse_merge_chunked_kernel<2><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 4: lse_merge_chunked_kernel<4><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 8: lse_merge_chunked_kernel<8><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 16: lse_merge_chunked_kernel<16><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
