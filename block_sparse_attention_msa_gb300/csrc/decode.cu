@@ -3,22 +3,28 @@
 // Together AI MiniMax-M3 serving article, section "MSA needs a new paged-attention
 // integration": the KV-group dimension is flattened into the batch and each flattened row
 // reads its selected pages through a strided view of one physical KV tensor (page address
-// steps by D, tokens by Hkv*D). Here that view is a 3-D TMA tensor map over the cache
-// [num_pages*128 tokens][Hkv][D]: one box {64 channels, 1 group, 128 tokens} is exactly one
-// per-head page half, so each virtual page v = p*128*Hkv + g becomes the TMA coordinate
-// (0|64, g, 128*p) and the hardware performs the deinterleaving gather.
+// steps by D, tokens by Hkv*D). A virtual page v = p*128*Hkv + g of that view is the 128 token
+// rows of group g in physical page p: 256 contiguous bytes of K (and of V) per token, at a
+// stride of Hkv*D*2 bytes.
 //
 // GB300 design. Decode attention is HBM-bound (every K/V byte is used by the G heads of one
-// group only), so the kernel is built to keep HBM busy:
-//  * work items are (flattened row, split of `pages_per_split` pages); a persistent grid of
-//    one CTA per SM walks its items while a producer warp streams K and V pages through a
-//    3-stage, 64 KB-per-stage TMA ring (128-byte swizzle);
-//  * 8 consumer warps each take 16 tokens of every page; the G heads of the group form the
-//    16-row side of warp-level bf16 MMAs (QK^T and PV, fp32 accumulate) so that tensor
-//    cores, not the FMA pipe, absorb the 4 flops per byte; softmax is online per warp;
-//  * the warps' (m, l, O) are merged in shared memory and each item writes one fp32 partial
-//    and its LSE; the LSE-merge kernel combines the splits of a row.
+// group only), so the kernel is built to keep HBM busy with no synchronisation between warps:
+//  * the (row, selected page) units of the whole batch are split into equal contiguous ranges,
+//    one per warp of a persistent grid (8 warps per SM);
+//  * a warp walks its range in steps of 16 tokens, fetching each step's K and V rows itself
+//    with 16-byte cp.async (lanes 0-15 and 16-31 read two 256-byte rows per instruction) into
+//    its own 3-stage ring, two steps ahead of the math. Plain 16-byte loads read this strided
+//    pattern at the copy bandwidth; one TMA box per 128-row page half (128 separate 128-byte
+//    rows) kept an earlier version of the kernel near half of it;
+//  * the G heads of the group form the 16-row side of warp-level bf16 MMAs (QK^T and PV, fp32
+//    accumulate) so that tensor cores, not the FMA pipe, absorb the 4 flops per byte; softmax
+//    is online across the warp's steps of a row;
+//  * where its range leaves a row, the warp writes that row's partial (normalised fp32 O and
+//    LSE) into the slot of the first page it covered; the other slots of its range hold LSE
+//    -inf, and the LSE-merge kernel combines a row's slots. The result does not depend on warp
+//    timing.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -31,21 +37,23 @@ namespace msa {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kConsumers = kWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr uint32_t kBox = 128 * 64 * 2;        // one box: 128 tokens x 64 channels bf16
-constexpr uint32_t kStage = 4 * kBox;          // K lo/hi + V lo/hi = 64 KB
-constexpr int kMaxStages = 3;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr uint32_t kHalf = 16 * 128;   // 16 tokens x 64 channels bf16, 128-byte swizzled
+constexpr uint32_t kStep = 4 * kHalf;  // K lo/hi + V lo/hi = 8 KB
+constexpr int kWin = 4;                // register windows of 4 x 32 entries
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecKParams {
   const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
   const int32_t* fpt;
   const int32_t* lens;
-  int32_t Hkv, G, topk, nsplit, pps, nstage;
-  int64_t n_items, num_pages;
-  float* part_o;
-  float* part_lse;
+  int32_t Hkv, G, topk;
+  int64_t rows, units, num_pages;  // rows = R*Hkv, units = rows*topk
+  float* part_o;                   // [rows, topk, G, 128]
+  float* part_lse;                 // [rows, topk, G]
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -54,99 +62,146 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-struct Smem {
-  float m[kWarps][16];
-  float l[kWarps][16];
-  float o[16][128];
-  int32_t flag;
+// A warp-uniform, forward-moving view of a 32-bit array through registers: lane l holds
+// a[base + 32*j + l]; reading an index past the window reloads it from that index.
+struct RegWindow {
+  int64_t base;
+  int32_t val[kWin];
+  __device__ __forceinline__ int32_t get(const int32_t* a, int64_t n, int64_t i, int lane) {
+    if (i < base || i >= base + 32 * kWin) {
+      base = i;
+#pragma unroll
+      for (int j = 0; j < kWin; ++j) {
+        const int64_t k = i + 32 * j + lane;
+        val[j] = k < n ? __ldg(a + k) : 0;
+      }
+    }
+    const int o = (int)(i - base), j = o >> 5;
+    int32_t x = val[0];
+#pragma unroll
+    for (int t = 1; t < kWin; ++t) x = j == t ? val[t] : x;
+    return __shfl_sync(0xffffffffu, x, o & 31);
+  }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const DecKParams p) {
+// A warp's walk over its unit range [u, u1): unit u = f*topk + pi is page pi of row f; pages
+// past the row's visible length are skipped; each page is ceil(tokens/16) steps c.
+struct Steps {
+  int64_t u, u1, f;
+  int len, npg, c, nc;
+  bool valid;
+  RegWindow lw;
+  __device__ __forceinline__ void start(int64_t u0, int64_t uend) {
+    u = u0 - 1;
+    u1 = uend;
+    f = -1;
+    len = npg = c = nc = 0;
+    lw.base = LLONG_MIN / 2;
+  }
+  __device__ __forceinline__ void advance(const DecKParams& p, int cap, int lane) {
+    if (++c < nc) return;
+    for (;;) {
+      ++u;
+      if (u >= u1) {
+        valid = false;
+        return;
+      }
+      const int64_t fu = u / p.topk;
+      if (fu != f) {
+        f = fu;
+        len = min(max(lw.get(p.lens, p.rows, fu, lane), 0), cap);
+        npg = (len + 127) >> 7;
+      }
+      const int pi = (int)(u - f * p.topk);
+      if (pi >= npg) {  // the rest of this row has no visible tokens
+        u = (f + 1) * p.topk - 1;
+        continue;
+      }
+      c = 0;
+      nc = (min(128, len - pi * 128) + 15) >> 4;
+      valid = true;
+      return;
+    }
+  }
+};
+
+// Copies tokens t0..t0+15 of K and V of virtual page v into a step buffer: channel half c/8 of
+// token row r, 16-byte chunk c%8, lands at (c/8)*kHalf + sw128(r, c%8) (K) and 2*kHalf past
+// that (V). An invalid page id is recorded and replaced by page 0, group 0.
+__device__ __forceinline__ void load_step(uint32_t st, const DecKParams& p, int32_t v, int t0,
+                                          int lane) {
+  const int64_t vpp = (int64_t)128 * p.Hkv;  // virtual pages per physical page
+  int64_t page = v >= 0 ? v / vpp : -1;
+  int64_t g = v >= 0 ? v % vpp : -1;
+  if (v < 0 || page >= p.num_pages || g >= p.Hkv) {
+    if (lane == 0) msa_record_error(kErrBadPage);
+    page = 0;
+    g = 0;
+  }
+  const int64_t row0 = (page * 128 + t0) * p.Hkv + g;  // D-element row of token t0, group g
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int idx = lane + 32 * j;
+    const int r = idx >> 4, c = idx & 15;
+    const int64_t off = (row0 + (int64_t)r * p.Hkv) * 128 + c * 8;
+    const uint32_t d = (c >> 3) * kHalf + sw128(r, c & 7);
+    cp_async16(st + d, p.k_cache + off);
+    cp_async16(st + 2 * kHalf + d, p.v_cache + off);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const int nstage = p.nstage;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + nstage * kStage);
-  uint64_t* empty_bar = full_bar + kMaxStages;
-  Smem& S = *reinterpret_cast<Smem*>(smem + nstage * kStage + 2 * kMaxStages * 8);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == kConsumers) {
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kWarps);
-    }
-    mbar_fence_init();
-  }
-  if (tid == 0) S.flag = 0;
-  __syncthreads();
-
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ring = smem_u32(smem) + warp * kStages * kStep;
   const int cap = p.topk * 128;
-  if (warp == kWarps) {
-    // ===================================== producer
-    if (lane != 0) return;
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
-    const int64_t vpp = (int64_t)128 * p.Hkv;  // virtual pages per physical page
-    uint32_t it = 0;
-    for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-      const int64_t f = item / p.nsplit;
-      const int s = (int)(item % p.nsplit);
-      const int len = min(max(p.lens[f], 0), cap);
-      const int npages = (len + 127) / 128;
-      const int pbeg = s * p.pps, pend = min(npages, pbeg + p.pps);
-      for (int pi = pbeg; pi < pend; ++pi, ++it) {
-        const int64_t v = p.fpt[f * p.topk + pi];
-        int64_t page = v >= 0 ? v / vpp : -1;
-        int32_t g = v >= 0 ? (int32_t)(v % vpp) : -1;
-        if (v < 0 || page >= p.num_pages || g >= p.Hkv) {
-          msa_record_error(kErrBadPage);
-          page = 0;
-          g = 0;
-        }
-        const uint32_t slot = it % nstage;
-        if (it >= (uint32_t)nstage && !mbar_wait(&empty_bar[slot], ((it / nstage) - 1) & 1)) {
-          msa_record_error(kErrTimeout);
-          // let the copies already issued land before the CTA exits (bounded)
-          for (uint32_t k = it - nstage + 1; k < it; ++k) mbar_wait(&full_bar[k % nstage], (k / nstage) & 1);
-          return;
-        }
-        uint8_t* st = smem + slot * kStage;
-        mbar_expect_tx(&full_bar[slot], kStage);
-        const int32_t tok = (int32_t)(page * 128);
-        tma_load_3d(st, &kmap, &full_bar[slot], 0, g, tok);
-        tma_load_3d(st + kBox, &kmap, &full_bar[slot], 64, g, tok);
-        tma_load_3d(st + 2 * kBox, &vmap, &full_bar[slot], 0, g, tok);
-        tma_load_3d(st + 3 * kBox, &vmap, &full_bar[slot], 64, g, tok);
-      }
+  const int G = p.G;
+  const int64_t nw = (int64_t)gridDim.x * kWarps, wg = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t u0 = p.units * wg / nw, u1 = p.units * (wg + 1) / nw;
+
+  // every slot of the range starts empty; a row segment's partial overwrites its first slot
+  for (int64_t i = u0 * G + lane; i < u1 * G; i += 32) p.part_lse[i] = -INFINITY;
+  __syncwarp();
+
+  Steps cur, pf;
+  cur.start(u0, u1);
+  pf.start(u0, u1);
+  cur.advance(p, cap, lane);
+  pf.advance(p, cap, lane);
+  RegWindow vw;
+  vw.base = LLONG_MIN / 2;
+  // prefetch the first kStages - 1 steps (one commit group per step; empty groups past the
+  // end keep the count uniform)
+#pragma unroll
+  for (int k = 0; k < kStages - 1; ++k) {
+    if (pf.valid) {
+      const int32_t v = vw.get(p.fpt, p.units, pf.u, lane);
+      load_step(ring + k * kStep, p, v, pf.c * 16, lane);
+      pf.advance(p, cap, lane);
     }
-    for (uint32_t k = (it > (uint32_t)nstage ? it - nstage : 0); k < it; ++k)
-      if (!mbar_wait(&empty_bar[k % nstage], (k / nstage) & 1)) msa_record_error(kErrTimeout);
-    return;
+    cp_async_commit();
   }
 
-  // ======================================= consumers
   const int gid = lane >> 2, tig = lane & 3;
-  const int G = p.G;
-  const int tb = warp * 16;  // this warp's tokens inside every page
   uint32_t it = 0;
-  for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-    const int64_t f = item / p.nsplit;
-    const int s = (int)(item % p.nsplit);
-    const int len = min(max(p.lens[f], 0), cap);
-    const int npages = (len + 127) / 128;
-    const int pbeg = s * p.pps, pend = min(npages, pbeg + p.pps);
-    const int64_t pidx = f * p.nsplit + s;
-    if (pend <= pbeg) {
-      if (tid < G) p.part_lse[pidx * G + tid] = -INFINITY;
-      continue;
-    }
+  while (cur.valid) {
+    // ---- a row segment: row f from unit cur.u on
+    const int64_t f = cur.f;
+    const int64_t slot_row = cur.u;  // the segment's first page: its partial's slot
+    const int len = cur.len;
     // Q fragments (A operand, 16 rows = heads of the group, zero rows beyond G)
     uint32_t qa[8][4];
     const uint16_t* qrow0 = p.q + (f * G + gid) * 128;
@@ -163,184 +218,154 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    for (int e = tid; e < 16 * 128; e += kConsumers) (&S.o[0][0])[e] = 0.f;
 
-    for (int pi = pbeg; pi < pend; ++pi, ++it) {
-      const uint32_t slot = it % nstage;
-      const bool ok = mbar_wait(&full_bar[slot], (it / nstage) & 1);
-      if (!ok) {
-        msa_record_error(kErrTimeout);
-        S.flag = 1;
+    do {
+      // step it + kStages - 1 of the walk goes into the buffer step it - 1 used
+      if (pf.valid) {
+        const int32_t v = vw.get(p.fpt, p.units, pf.u, lane);
+        load_step(ring + ((it + kStages - 1) % kStages) * kStep, p, v, pf.c * 16, lane);
+        pf.advance(p, cap, lane);
       }
-      if (ok) {
-        const uint32_t kb = smem_u32(smem + slot * kStage);
-        const uint32_t vb = kb + 2 * kBox;
-        // ---- S = Q K^T for tokens tb..tb+15 (two n-tiles of 8 tokens)
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          const int mi = lane >> 3;
-          const uint32_t tok = tb + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t dc = 2 * ks + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kb + (dc >> 3) * kBox + sw128(tok, dc & 7), b0, b1, b2, b3);
-            mma_bf16_16816(sc[0], qa[ks], b0, b1);
-            mma_bf16_16816(sc[1], qa[ks], b2, b3);
-          }
-        }
-        // ---- mask tokens past the row's visible length, online softmax
-        const int n0 = pi * 128 + tb;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (n0 + nt * 8 + tig * 2 + (c & 1) >= len) sc[nt][c] = -INFINITY;
-        float mx[2];
-        mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-        mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        }
-        float scale[2], mref[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float mnew = fmaxf(mrow[r], mx[r]);
-          mref[r] = mnew == -INFINITY ? 0.f : mnew;
-          scale[r] = ex2((mrow[r] - mref[r]) * kLog2e);
-          mrow[r] = mnew;
-        }
-        float ps[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int r = c >> 1;
-            sc[nt][c] = ex2((sc[nt][c] - mref[r]) * kLog2e);
-            ps[r] += sc[nt][c];
-          }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) lrow[r] = lrow[r] * scale[r] + ps[r];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          o[i][0] *= scale[0];
-          o[i][1] *= scale[0];
-          o[i][2] *= scale[1];
-          o[i][3] *= scale[1];
-        }
-        // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-        pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-        pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-        pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-        {
-          const int mi = lane >> 3;
-          const uint32_t tok = tb + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-          for (int nd = 0; nd < 16; nd += 2) {
-            const uint32_t dc = nd + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(vb + (dc >> 3) * kBox + sw128(tok, dc & 7), b0, b1, b2, b3);
-            mma_bf16_16816(o[nd], pa, b0, b1);
-            mma_bf16_16816(o[nd + 1], pa, b2, b3);
-          }
-        }
-      }
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();  // step it has landed
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[slot]);
-    }
-    // ---- merge the 8 warps' partial softmax states
+      const uint32_t kb = ring + (it % kStages) * kStep;
+      const uint32_t vb = kb + 2 * kHalf;
+      // ---- S = Q K^T for the step's 16 tokens (two n-tiles of 8 tokens)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3;
+        const uint32_t tok = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t dc = 2 * ks + (mi & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kb + (dc >> 3) * kHalf + sw128(tok, dc & 7), b0, b1, b2, b3);
+          mma_bf16_16816(sc[0], qa[ks], b0, b1);
+          mma_bf16_16816(sc[1], qa[ks], b2, b3);
+        }
+      }
+      // ---- mask tokens past the row's visible length, online softmax
+      const int n0 = (int)(cur.u - f * p.topk) * 128 + cur.c * 16;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (n0 + nt * 8 + tig * 2 + (c & 1) >= len) sc[nt][c] = -INFINITY;
+      float mx[2];
+      mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      }
+      float scale[2], mref[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float mnew = fmaxf(mrow[r], mx[r]);
+        mref[r] = mnew == -INFINITY ? 0.f : mnew;
+        scale[r] = ex2((mrow[r] - mref[r]) * kLog2e);
+        mrow[r] = mnew;
+      }
+      float ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = c >> 1;
+          sc[nt][c] = ex2((sc[nt][c] - mref[r]) * kLog2e);
+          ps[r] += sc[nt][c];
+        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) lrow[r] = lrow[r] * scale[r] + ps[r];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= scale[0];
+        o[i][1] *= scale[0];
+        o[i][2] *= scale[1];
+        o[i][3] *= scale[1];
+      }
+      // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+      {
+        const int mi = lane >> 3;
+        const uint32_t tok = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int nd = 0; nd < 16; nd += 2) {
+          const uint32_t dc = nd + (mi >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(vb + (dc >> 3) * kHalf + sw128(tok, dc & 7), b0, b1, b2, b3);
+          mma_bf16_16816(o[nd], pa, b0, b1);
+          mma_bf16_16816(o[nd + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();  // every lane is done with the buffer before it is refilled
+      ++it;
+      cur.advance(p, cap, lane);
+    } while (cur.valid && cur.f == f);
+
+    // ---- the segment's partial: normalised O and LSE per head, in its first page's slot
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
       lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
     }
-    if (tig == 0) {
-      S.m[warp][gid] = mrow[0];
-      S.m[warp][gid + 8] = mrow[1];
-      S.l[warp][gid] = lrow[0];
-      S.l[warp][gid + 8] = lrow[1];
-    }
-    consumer_sync();
-    if (S.flag) return;
-    float wgt[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int row = gid + 8 * r;
-      float M = -INFINITY;
+      if (row >= G) continue;
+      const float inv = lrow[r] > 0.f ? 1.0f / lrow[r] : 0.f;
+      float* dst = p.part_o + (slot_row * G + row) * 128;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, S.m[w][row]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        if (S.m[w][row] != -INFINITY) L += S.l[w][row] * ex2((S.m[w][row] - M) * kLog2e);
-      wgt[r] = (mrow[r] == -INFINITY || L <= 0.f) ? 0.f : ex2((mrow[r] - M) * kLog2e) / L;
-      if (warp == 0 && tig == 0 && row < G)
-        p.part_lse[pidx * G + row] = L > 0.f ? M + __logf(L) : -INFINITY;
+      for (int nd = 0; nd < 16; ++nd)
+        *reinterpret_cast<float2*>(dst + nd * 8 + tig * 2) =
+            make_float2(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
+      if (tig == 0)
+        p.part_lse[slot_row * G + row] = lrow[r] > 0.f ? mrow[r] + __logf(lrow[r]) : -INFINITY;
     }
-#pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      const int col = nd * 8 + tig * 2;
-      if (gid < G) {
-        atomicAdd(&S.o[gid][col], o[nd][0] * wgt[0]);
-        atomicAdd(&S.o[gid][col + 1], o[nd][1] * wgt[0]);
-      }
-      if (gid + 8 < G) {
-        atomicAdd(&S.o[gid + 8][col], o[nd][2] * wgt[1]);
-        atomicAdd(&S.o[gid + 8][col + 1], o[nd][3] * wgt[1]);
-      }
-    }
-    consumer_sync();
-    float* dst = p.part_o + pidx * G * 128;
-    for (int e = tid * 4; e < G * 128; e += kConsumers * 4)
-      *reinterpret_cast<float4*>(dst + e) = *reinterpret_cast<const float4*>(&S.o[0][0] + e);
-    consumer_sync();
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace
 
 void decode_split(int32_t topk, int32_t* nsplit, int32_t* pages_per_split) {
-  const int pps = 4;
-  *pages_per_split = pps;
-  *nsplit = (topk + pps - 1) / pps;
+  // one partial slot per selected page: a warp's row segment writes the slot of its first page
+  *pages_per_split = 1;
+  *nsplit = topk;
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
-  CUtensorMap kmap, vmap;
-  const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.Hkv, (uint64_t)a.num_pages * 128};
-  const uint64_t strides[2] = {(uint64_t)a.D * 2, (uint64_t)a.Hkv * a.D * 2};
-  const uint32_t box[3] = {64, 1, 128};
-  if (!encode_bf16_map(&kmap, a.k_cache, 3, dims, strides, box, true) ||
-      !encode_bf16_map(&vmap, a.v_cache, 3, dims, strides, box, true))
-    return cudaErrorInvalidValue;
   DecKParams p;
   p.q = a.q;
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
   p.fpt = a.fpt;
   p.lens = a.lens;
   p.Hkv = a.Hkv;
   p.G = a.Hq / a.Hkv;
   p.topk = a.topk;
-  p.nsplit = a.nsplit;
-  p.pps = a.pages_per_split;
-  p.nstage = kMaxStages;
-  p.n_items = (int64_t)a.R * a.Hkv * a.nsplit;
+  p.rows = (int64_t)a.R * a.Hkv;
+  p.units = p.rows * a.topk;
   p.num_pages = a.num_pages;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  const size_t smem = 1024 + kMaxStages * kStage + 2 * kMaxStages * 8 + sizeof(Smem);
+  if (a.nsplit != a.topk) return cudaErrorInvalidValue;  // one slot per selected page
+  const size_t smem = 1024 + (size_t)kWarps * kStages * kStep;
   cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(p.n_items, sm_count());
-  paged_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(kmap, vmap, p);
+  if (p.units <= 0) return cudaSuccess;
+  const int64_t grid = std::min<int64_t>((p.units + kWarps - 1) / kWarps, sm_count());
+  paged_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_lse_merge(a.part_o, false, a.part_lse, nullptr, (int64_t)a.R * a.Hkv, a.nsplit,
-                          p.G, a.D, a.o, a.lse, stream);
+  return launch_lse_merge(a.part_o, false, a.part_lse, nullptr, p.rows, a.nsplit, p.G, a.D,
+                          a.o, a.lse, stream);
 }
-
 }  // namespace msa
