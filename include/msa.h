@@ -201,7 +201,8 @@ MSA_API int msa_stage_selected_kv(const uint16_t* k_cache, const uint16_t* v_cac
  *   flat_page_table [R*Hkv, topk] int32; flat_kv_lens [R*Hkv] int32, each in [1, topk*128]
  *   o        [R, Hq, D] bf16 (out); lse [R, Hq] fp32 (out, may be NULL)
  *   workspace >= msa_paged_sparse_decode_workspace_size(R, Hq, Hkv, topk) bytes
- *             (split-K partials; no zero-fill needed)
+ *             (one partial slot per selected page; no zero-fill needed)
+ * The result depends only on the inputs (no run-to-run variation).
  * ------------------------------------------------------------------------------------ */
 MSA_API size_t msa_paged_sparse_decode_workspace_size(int32_t R, int32_t Hq, int32_t Hkv, int32_t topk);
 
