@@ -13,9 +13,8 @@
 //    one per warp of a persistent grid (8 warps per SM);
 //  * a warp walks its range in steps of 16 tokens, fetching each step's K and V rows itself
 //    with 16-byte cp.async (lanes 0-15 and 16-31 read two 256-byte rows per instruction) into
-//    its own 3-stage ring, two steps ahead of the math. Plain 16-byte loads read this strided
-//    pattern at the copy bandwidth; one TMA box per 128-row page half (128 separate 128-byte
-//    rows) kept an earlier version of the kernel near half of it;
+//    its own 3-stage ring, two steps ahead of the math, so its loads never wait for another
+//    warp; 16-byte loads of this strided pattern run at the copy bandwidth;
 //  * the G heads of the group form the 16-row side of warp-level bf16 MMAs (QK^T and PV, fp32
 //    accumulate) so that tensor cores, not the FMA pipe, absorb the 4 flops per byte; softmax
 //    is online across the warp's steps of a row;

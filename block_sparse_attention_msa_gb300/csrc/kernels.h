@@ -141,7 +141,7 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
   return w;
 }
 // Query-major part of the prefill (G in {8, 16}): per pair of 128/G-query tiles, the blocks
-// chosen by at least 3/8 of the pair's queries (ascending, at most kMaxDense) with a bit mask of
+// chosen by at least half of the pair's queries (ascending, at most kMaxDense) with a bit mask of
 // the queries that chose each; the residual selections go to the block-major pass.
 struct DenseWorkspace {
   int32_t* residual;   // [T, Hkv, k]

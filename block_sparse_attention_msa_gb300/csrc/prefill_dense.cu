@@ -14,7 +14,7 @@
 // GB300 design.
 //  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G consecutive
 //      queries of one group): counts the pair's selections per block in shared memory, keeps
-//      the blocks chosen by at least 3/8 of the pair's queries (at most kMaxDense, ascending)
+//      the blocks chosen by at least half of the pair's queries (at most kMaxDense, ascending)
 //      with a bit mask of the queries that chose each, and writes the residual selections (the
 //      dense ones replaced by -1) for the block-major pass.
 //  (b) prefill_dense_tc_kernel, one persistent CTA per SM over the pairs: the two tiles of a
@@ -527,7 +527,7 @@ cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_k
   const int32_t qpt = 128 / G;
   const int32_t ppg = (int32_t)((T + 2 * qpt - 1) / (2 * qpt));
   const int32_t nq = 2 * qpt;
-  const int32_t thr = std::max(2, (3 * nq + 7) / 8);
+  const int32_t thr = std::max(2, (nq + 1) / 2);  // at least half of the pair's queries
   const int64_t npairs = (int64_t)Hkv * ppg;
   if (npairs <= 0) return cudaSuccess;
   const size_t smem = 6 * (size_t)kHistBlocks;

@@ -226,7 +226,7 @@ MSA_API int msa_paged_sparse_decode(const uint16_t* q, const uint16_t* k_cache, 
  * (-1 entries ignored). Steps, all on the GPU: (a) invert the selections into per-(group,
  * block) query lists, (b) block-major attention writing one partial (O, lse) per
  * (query, group, slot), (c) merge the partials of each (query, head). With G = Hq/Hkv of 8
- * or 16, the blocks that at least 3/8 of a pair of 128/G-query tiles chose are first taken
+ * or 16, the blocks that at least half of a pair of 128/G-query tiles chose are first taken
  * out and computed query-major (one partial per (query, head) for all of them); (a)-(b) run
  * on the remaining selections and (c) merges both.
  *

@@ -181,7 +181,7 @@ def test_sparse_prefill(T, S, Hq, Hkv, topk, n_shared):
 
 def test_sparse_prefill_shared_blocks_beyond_the_dense_cap():
     """k 64 with two query halves per 32-query pair choosing disjoint 62-block sets: 126 blocks
-    are shared by at least 3/8 of the pair, more than the query-major pass takes, so the blocks
+    are shared by at least half of the pair, more than the query-major pass takes, so the blocks
     past its cap must reach the output through the block-major pass."""
     T, prefix, Hq, Hkv, D, k = 64, 16384, 16, 2, 128, 64
     S = prefix + T
