@@ -12,7 +12,10 @@
 // sums the partials. The same merge finishes the split-K decode. One warp per (unit, head):
 // lanes own 4 consecutive channels, partials are read once, coalesced, and the result is
 // written as bf16 with its fp32 LSE.
+#include <algorithm>
+
 #include "common.cuh"
+#include "host_util.h"
 #include "kernels.h"
 #include "page_table_row.cuh"
 
@@ -137,14 +140,15 @@ __global__ void __launch_bounds__(256)
 }
 
 // Prefill merge over chunk-major partials: part_o[c][row][8] bf16 with c = 16 channel chunks
-// and row = (u*S + s)*G + e; one warp per unit u (all G heads). Lane slot idx = lane + 32*r
-// covers head idx % G and chunk idx / G, so for a fixed r the lanes of one chunk plane read the
-// G adjacent rows of a partial: 16*G contiguous bytes. The stream is latency-bound, so the
-// dependent round trips per unit are kept few: the ids, every slot's LSE (staged in shared
-// memory) and the query-major LSE are requested together; then the valid partials, the
-// query-major one (dense_o / dense_lse, one per unit and head) first, stream NB at a time with
-// all their loads in flight at once, into accumulators kept relative to a running max that are
-// rescaled when the max grows.
+// and row = (u*S + s)*G + e; one warp per unit u (all G heads) at a time, persistent over the
+// units. Lane slot idx = lane + 32*r covers head idx % G and chunk idx / G, so for a fixed r
+// the lanes of one chunk plane read the G adjacent rows of a partial: 16*G contiguous bytes.
+// The stream is latency-bound, so the dependent round trips per unit are few: the ids, every
+// slot's LSE and the query-major LSE of the warp's next unit are requested while the current
+// unit's partials stream (into registers, moved to shared memory at the top of the next unit);
+// the valid partials, the query-major one (dense_o / dense_lse, one per unit and head) first,
+// stream NB at a time with all their loads in flight, into accumulators kept relative to a
+// running max that are rescaled when the max grows.
 template <int G>
 __device__ __forceinline__ void merge_fma(float (&acc)[(G * 16 + 31) / 32][8], float w,
                                           const uint4 (&v)[(G * 16 + 31) / 32]) {
@@ -161,116 +165,135 @@ __device__ __forceinline__ void merge_fma(float (&acc)[(G * 16 + 31) / 32][8], f
   }
 }
 
-template <int G>
-__global__ void __launch_bounds__(256, G >= 16 ? 1 : 2)
+// The first round trip of unit u: ids (S <= 64), the S*G <= 32*NL slot LSEs (NL per lane),
+// the query-major LSE.
+template <int NL>
+struct MergeHead {
+  int id0, id1;
+  float ld;
+  float lse[NL];
+};
+template <int G, int NL>
+__device__ __forceinline__ void merge_head_load(MergeHead<NL>& m, int64_t u, int64_t U, int S,
+                                                const int32_t* __restrict__ ids,
+                                                const float* __restrict__ lse_parts,
+                                                const float* __restrict__ dense_lse, int lane) {
+  const bool in = u < U;
+  const int SG = S * G;
+  m.id0 = in && lane < S ? __ldg(ids + u * S + lane) : -1;
+  m.id1 = in && lane + 32 < S ? __ldg(ids + u * S + lane + 32) : -1;
+  m.ld = in && dense_lse ? __ldg(dense_lse + u * G + lane % G) : -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NL; ++k) {
+    const int i = lane + 32 * k;
+    m.lse[k] = in && i < SG ? __ldg(lse_parts + u * SG + i) : -INFINITY;
+  }
+}
+
+template <int G, int NL>
+__global__ void __launch_bounds__(256, G >= 16 || NL > 8 ? 1 : 2)
     lse_merge_chunked_kernel(const uint4* __restrict__ part_o, int64_t part_rows,
                              const float* __restrict__ lse_parts, const int32_t* __restrict__ ids,
                              const uint4* __restrict__ dense_o, const float* __restrict__ dense_lse,
                              int64_t U, int32_t S, uint16_t* __restrict__ o, float* __restrict__ lse) {
   constexpr int R = (G * 16 + 31) / 32;  // chunk slots per lane
   constexpr int NB = R >= 8 ? 2 : 3;     // partials per batch of loads
-  extern __shared__ float s_lse[];       // [8 warps][S*G]
+  __shared__ float s_lse[8][NL * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t u = (int64_t)blockIdx.x * 8 + warp;
-  if (u >= U) return;
   const int e = lane % G;
   const int SG = S * G;
-  float* wl = s_lse + warp * SG;
-  // first round trip: ids (S <= 64), the LSE of every slot, the query-major LSE
-  const int id0 = lane < S ? __ldg(ids + u * S + lane) : -1;
-  const int id1 = lane + 32 < S ? __ldg(ids + u * S + lane + 32) : -1;
-  const float ld = dense_lse ? __ldg(dense_lse + u * G + e) : -INFINITY;
-  for (int i0 = 0; i0 < SG; i0 += 128) {
-    float t[4];
+  float* wl = s_lse[warp];
+  const int64_t stride = (int64_t)gridDim.x * 8;
+  int64_t u = (int64_t)blockIdx.x * 8 + warp;
+  MergeHead<NL> nxt;
+  merge_head_load<G, NL>(nxt, u, U, S, ids, lse_parts, dense_lse, lane);
+  for (; u < U; u += stride) {
+    // this unit's head (requested during the previous unit) into shared memory and a mask
+    const MergeHead<NL> cur = nxt;
+    __syncwarp();  // the previous unit is done reading its LSEs
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = i0 + lane + 32 * k;
-      t[k] = i < SG ? __ldg(lse_parts + u * SG + i) : -INFINITY;
-    }
+    for (int k = 0; k < NL; ++k) wl[lane + 32 * k] = cur.lse[k];
+    uint64_t vmask = (uint64_t)__ballot_sync(0xffffffffu, cur.id0 >= 0) |
+                     ((uint64_t)__ballot_sync(0xffffffffu, cur.id1 >= 0) << 32);
+    __syncwarp();
+    // the next unit's head, in flight while this unit's partials stream
+    merge_head_load<G, NL>(nxt, u + stride, U, S, ids, lse_parts, dense_lse, lane);
+    float acc[R][8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = i0 + lane + 32 * k;
-      if (i < SG) wl[i] = t[k];
-    }
-  }
-  uint64_t vmask = (uint64_t)__ballot_sync(0xffffffffu, id0 >= 0) |
-                   ((uint64_t)__ballot_sync(0xffffffffu, id1 >= 0) << 32);
-  __syncwarp();
-  float acc[R][8];
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+      for (int x = 0; x < 8; ++x) acc[r][x] = 0.f;
+    float m = -INFINITY, total = 0.f;  // acc and total are relative to e^m
+    bool dense_pending = dense_lse != nullptr;
+    while (vmask || dense_pending) {
+      const uint4* base[NB];
+      int64_t rstride[NB];
+      float l[NB];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[r][x] = 0.f;
-  float m = -INFINITY, total = 0.f;  // acc and total are relative to e^m
-  bool dense_pending = dense_lse != nullptr;
-  while (vmask || dense_pending) {
-    const uint4* base[NB];
-    int64_t stride[NB];
-    float l[NB];
+      for (int k = 0; k < NB; ++k) {
+        base[k] = nullptr;
+        rstride[k] = 0;
+        l[k] = -INFINITY;
+        if (dense_pending) {
+          dense_pending = false;
+          base[k] = dense_o + u * G + e;
+          rstride[k] = U * G;
+          l[k] = cur.ld;
+        } else if (vmask) {
+          const int s = __ffsll((long long)vmask) - 1;
+          vmask &= vmask - 1;
+          base[k] = part_o + (u * S + s) * G + e;
+          rstride[k] = part_rows;
+          l[k] = wl[s * G + e];
+        }
+      }
+      uint4 v[NB][R];
 #pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      base[k] = nullptr;
-      stride[k] = 0;
-      l[k] = -INFINITY;
-      if (dense_pending) {
-        dense_pending = false;
-        base[k] = dense_o + u * G + e;
-        stride[k] = U * G;
-        l[k] = ld;
-      } else if (vmask) {
-        const int s = __ffsll((long long)vmask) - 1;
-        vmask &= vmask - 1;
-        base[k] = part_o + (u * S + s) * G + e;
-        stride[k] = part_rows;
-        l[k] = wl[s * G + e];
+      for (int k = 0; k < NB; ++k)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int idx = lane + 32 * r;
+          v[k][r] = base[k] && idx < G * 16 ? __ldcs(base[k] + (int64_t)(idx / G) * rstride[k])
+                                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+      float mx = l[0];
+#pragma unroll
+      for (int k = 1; k < NB; ++k) mx = fmaxf(mx, l[k]);
+      if (mx == -INFINITY) continue;
+      if (mx > m) {
+        const float sc = m == -INFINITY ? 0.f : __expf(m - mx);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int x = 0; x < 8; ++x) acc[r][x] *= sc;
+        total *= sc;
+        m = mx;
+      }
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        // a partial with LSE -inf contributes nothing; its rows may never have been written
+        if (l[k] != -INFINITY) {
+          const float w = __expf(l[k] - m);
+          total += w;
+          merge_fma<G>(acc, w, v[k]);
+        }
       }
     }
-    uint4 v[NB][R];
+    const float inv = total > 0.f ? 1.0f / total : 0.f;
 #pragma unroll
-    for (int k = 0; k < NB; ++k)
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int idx = lane + 32 * r;
-        v[k][r] = base[k] && idx < G * 16 ? __ldcs(base[k] + (int64_t)(idx / G) * stride[k])
-                                         : make_uint4(0u, 0u, 0u, 0u);
-      }
-    float mx = l[0];
-#pragma unroll
-    for (int k = 1; k < NB; ++k) mx = fmaxf(mx, l[k]);
-    if (mx == -INFINITY) continue;
-    if (mx > m) {
-      const float sc = m == -INFINITY ? 0.f : __expf(m - mx);
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int x = 0; x < 8; ++x) acc[r][x] *= sc;
-      total *= sc;
-      m = mx;
-    }
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      // a partial with LSE -inf contributes nothing; its rows may never have been written
-      if (l[k] != -INFINITY) {
-        const float w = __expf(l[k] - m);
-        total += w;
-        merge_fma<G>(acc, w, v[k]);
+    for (int r = 0; r < R; ++r) {
+      const int idx = lane + 32 * r;
+      if (idx < G * 16) {
+        uint4 out;
+        out.x = pack_bf16x2(acc[r][0] * inv, acc[r][1] * inv);
+        out.y = pack_bf16x2(acc[r][2] * inv, acc[r][3] * inv);
+        out.z = pack_bf16x2(acc[r][4] * inv, acc[r][5] * inv);
+        out.w = pack_bf16x2(acc[r][6] * inv, acc[r][7] * inv);
+        *reinterpret_cast<uint4*>(o + (u * G + e) * 128 + (idx / G) * 8) = out;
       }
     }
+    if (lse && lane < G) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
   }
-  const float inv = total > 0.f ? 1.0f / total : 0.f;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = lane + 32 * r;
-    if (idx < G * 16) {
-      uint4 out;
-      out.x = pack_bf16x2(acc[r][0] * inv, acc[r][1] * inv);
-      out.y = pack_bf16x2(acc[r][2] * inv, acc[r][3] * inv);
-      out.z = pack_bf16x2(acc[r][4] * inv, acc[r][5] * inv);
-      out.w = pack_bf16x2(acc[r][6] * inv, acc[r][7] * inv);
-      *reinterpret_cast<uint4*>(o + (u * G + e) * 128 + (idx / G) * 8) = out;
-    }
-  }
-  if (lse && lane < G) lse[u * G + e] = total > 0.f ? m + __logf(total) : -INFINITY;
 }
 
 }  // namespace
@@ -279,19 +302,32 @@ cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
                                      const int32_t* ids, const void* dense_o,
                                      const float* dense_lse, int64_t U, int32_t S, int32_t G,
                                      uint16_t* o, float* lse, cudaStream_t stream) {
-  const unsigned grid = (unsigned)((U + 7) / 8);
+  if (U <= 0) return cudaSuccess;
+  if (S > 64 || G > 16 || (int64_t)S * G > 1024) return cudaErrorInvalidValue;
+  const int sg = S * G;
+  const int nl = sg <= 128 ? 4 : sg <= 256 ? 8 : 32;
+  const int per_sm = G >= 16 || nl > 8 ? 1 : 2;
+  const unsigned grid = (unsigned)std::min<int64_t>((U + 7) / 8, (int64_t)sm_count() * per_sm);
   const int64_t rows = U * S * G;
   const uint4* po = reinterpret_cast<const uint4*>(part_o);
   const uint4* pd = reinterpret_cast<const uint4*>(dense_o);
-  const size_t smem = (size_t)8 * S * G * sizeof(float);
+#define MSA_MERGE_LAUNCH(GG, NN)                                                               \
+  lse_merge_chunked_kernel<GG, NN><<<grid, 256, 0, stream>>>(po, rows, lse_parts, ids, pd, \
+                                                              dense_lse, U, S, o, lse)
+#define MSA_MERGE_G(GG)                   \
+  if (nl == 4) MSA_MERGE_LAUNCH(GG, 4);   \
+  else if (nl == 8) MSA_MERGE_LAUNCH(GG, 8); \
+  else MSA_MERGE_LAUNCH(GG, 32);
   switch (G) {
-    case 1: lse_merge_chunked_kernel<1><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 2: lse_merge_chunked_kernel<2><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 4: lse_merge_chunked_kernel<4><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 8: lse_merge_chunked_kernel<8><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
-    case 16: lse_merge_chunked_kernel<16><<<grid, 256, smem, stream>>>(po, rows, lse_parts, ids, pd, dense_lse, U, S, o, lse); break;
+    case 1: MSA_MERGE_G(1) break;
+    case 2: MSA_MERGE_G(2) break;
+    case 4: MSA_MERGE_G(4) break;
+    case 8: MSA_MERGE_G(8) break;
+    case 16: MSA_MERGE_G(16) break;
     default: return cudaErrorInvalidValue;
   }
+#undef MSA_MERGE_G
+#undef MSA_MERGE_LAUNCH
   return cudaGetLastError();
 }
 
