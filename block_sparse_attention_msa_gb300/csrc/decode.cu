@@ -333,12 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKPar
 
 }  // namespace
 
-void decode_split(int32_t topk, int32_t* nsplit, int32_t* pages_per_split) {
-  // one partial slot per selected page: a warp's row segment writes the slot of its first page
-  *pages_per_split = 1;
-  *nsplit = topk;
-}
-
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   DecKParams p;
   p.q = a.q;

@@ -50,9 +50,11 @@ struct DecodeArgs {
   float* lse;                  // [R, Hq] or null
   float* part_o;               // workspace [R*Hkv, nsplit, G, D]
   float* part_lse;             // workspace [R*Hkv, nsplit, G]
-  int32_t nsplit, pages_per_split;
+  int32_t nsplit;              // partial slots per flattened row: decode_slots(topk)
 };
-void decode_split(int32_t topk, int32_t* nsplit, int32_t* pages_per_split);
+// One partial slot per selected page: a warp whose unit range starts a row segment at page i
+// writes slot i.
+inline int32_t decode_slots(int32_t topk) { return topk; }
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ KV residency split

@@ -203,9 +203,7 @@ int msa_stage_selected_kv(const uint16_t* k_cache, const uint16_t* v_cache, int6
 // ------------------------------------------------------------------------------ decode
 size_t msa_paged_sparse_decode_workspace_size(int32_t R, int32_t Hq, int32_t Hkv, int32_t topk) {
   if (R <= 0 || Hq <= 0 || Hkv <= 0 || topk <= 0) return 0;
-  int32_t nsplit, pps;
-  msa::decode_split(topk, &nsplit, &pps);
-  const size_t units = (size_t)R * Hq * nsplit;  // (row, group, split, head)
+  const size_t units = (size_t)R * Hq * msa::decode_slots(topk);  // (row, group, slot, head)
   return msa::ws_align(units * 128 * sizeof(float)) + msa::ws_align(units * sizeof(float));
 }
 
@@ -244,7 +242,7 @@ int msa_paged_sparse_decode(const uint16_t* q, const uint16_t* k_cache, const ui
   a.num_pages = num_pages;
   a.o = o;
   a.lse = lse;
-  msa::decode_split(topk, &a.nsplit, &a.pages_per_split);
+  a.nsplit = msa::decode_slots(topk);
   const size_t units = (size_t)R * Hq * a.nsplit;
   a.part_o = reinterpret_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
