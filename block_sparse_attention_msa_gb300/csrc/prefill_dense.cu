@@ -40,7 +40,8 @@ namespace {
 constexpr int kSelThreads = 256;
 // One CTA per pair of 128/G-query tiles (nq = 2*128/G <= 32 consecutive queries of group g).
 // The ids a pair can choose are at most the local block of its last query (nb blocks); they are
-// counted in windows of kHistBlocks blocks: a query mask per block in shared memory, filled with
+// counted in windows of hw <= kHistBlocks blocks (hw: the chunk's block count, capped): a query
+// mask per block in shared memory, filled with
 // shared atomics (a block's count is its mask's popcount: a query chooses a block at most once),
 // then a prefix scan over the window ranks the dense blocks in ascending order.
 constexpr int kHistBlocks = 16384;
@@ -48,12 +49,12 @@ constexpr int kHistBlocks = 16384;
 __global__ void __launch_bounds__(kSelThreads)
     dense_select_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv, int32_t G,
                         int32_t topk, int32_t qpt, int32_t ppg, int32_t thr, int64_t q_start,
-                        int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
+                        int32_t hw, int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
                         int32_t* __restrict__ dblk, uint32_t* __restrict__ dmask,
                         float* __restrict__ part_lse) {
   extern __shared__ __align__(16) uint8_t hist_smem[];
-  uint32_t* msk = reinterpret_cast<uint32_t*>(hist_smem);                  // [kHistBlocks]
-  int16_t* rnk = reinterpret_cast<int16_t*>(hist_smem + 4 * kHistBlocks);  // dense rank or -1
+  uint32_t* msk = reinterpret_cast<uint32_t*>(hist_smem);          // [hw]
+  int16_t* rnk = reinterpret_cast<int16_t*>(hist_smem + 4 * hw);   // [hw] dense rank or -1
   __shared__ int32_t warp_sum[kSelThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t pair = blockIdx.x;
@@ -67,8 +68,8 @@ __global__ void __launch_bounds__(kSelThreads)
     if (t < T) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
   }
   int ranked = 0;  // dense blocks ranked in earlier windows
-  for (int64_t base = 0; base < nb; base += kHistBlocks) {
-    const int w = (int)min((int64_t)kHistBlocks, nb - base);
+  for (int64_t base = 0; base < nb; base += hw) {
+    const int w = (int)min((int64_t)hw, nb - base);
     for (int j = tid; j < w; j += kSelThreads) msk[j] = 0u;
     __syncthreads();
     for (int e = tid; e < n; e += kSelThreads) {
@@ -530,12 +531,14 @@ cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_k
   const int32_t thr = std::max(2, (nq + 1) / 2);  // at least half of the pair's queries
   const int64_t npairs = (int64_t)Hkv * ppg;
   if (npairs <= 0) return cudaSuccess;
-  const size_t smem = 6 * (size_t)kHistBlocks;
+  // the window covers every block of the chunk when it fits (one pass), else kHistBlocks
+  const int32_t hw = (int32_t)std::min<int64_t>(kHistBlocks, (S_kv + 127) / 128);
+  const size_t smem = (6 * (size_t)hw + 15) / 16 * 16;
   cudaError_t e = cudaFuncSetAttribute(dense_select_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dense_select_kernel<<<(unsigned)npairs, kSelThreads, smem, stream>>>(
-      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, w.residual, w.dcnt, w.dblk, w.dmask,
+      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, hw, w.residual, w.dcnt, w.dblk, w.dmask,
       w.part_lse);
   return cudaGetLastError();
 }
