@@ -98,23 +98,28 @@ struct PrefillWorkspace {
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 // Prefill work lists are per (group, query window, KV block): queries are cut into windows so
 // that the tiles of one window -- whose query rows stay in L2 -- run together. The window is the
-// smallest power of two from 2048 at which a list holds about kListTarget selections on average
-// (window * topk >= kListTarget * nblk), or the whole chunk: with many blocks (a long prefix)
+// smallest power of two from 2048 at which a list holds about `target` selections on average
+// (window * topk >= target * nblk), or the whole chunk: with many blocks (a long prefix)
 // short windows would leave tiles half empty and reload a K/V block for every few queries.
+// The target counts all selections: 64 when every selection is block-major, 512 when the
+// query-major pass (G 8, 16) first takes the shared blocks (about two thirds of them in the
+// clustered workloads), so that the residual lists still fill their tiles.
 constexpr int32_t kListTarget = 64;
-inline int32_t prefill_window(int64_t T, int32_t nblk, int32_t topk) {
+constexpr int32_t kListTargetHybrid = 512;
+inline int32_t prefill_window(int64_t T, int32_t nblk, int32_t topk, int32_t G) {
+  const int64_t target = prefill_hybrid(G) ? kListTargetHybrid : kListTarget;
   int64_t w = 2048;
-  while (w < T && w * topk < (int64_t)kListTarget * nblk) w *= 2;
+  while (w < T && w * topk < target * nblk) w *= 2;
   return (int32_t)w;
 }
-inline int32_t prefill_nwin(int64_t T, int32_t nblk, int32_t topk) {
-  const int64_t w = prefill_window(T, nblk, topk);
+inline int32_t prefill_nwin(int64_t T, int32_t nblk, int32_t topk, int32_t G) {
+  const int64_t w = prefill_window(T, nblk, topk, G);
   return (int32_t)((T + w - 1) / w);
 }
 inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, int32_t nblk,
                                           int32_t G, bool attention) {
   PrefillWorkspace w{};
-  const size_t lists = (size_t)Hkv * (attention ? prefill_nwin(T, nblk, topk) : 1) * nblk;
+  const size_t lists = (size_t)Hkv * (attention ? prefill_nwin(T, nblk, topk, G) : 1) * nblk;
   const size_t groups = lists / nblk;
   size_t off = 0;
   w.counts = off;       off = ws_align(off + 4 * lists);

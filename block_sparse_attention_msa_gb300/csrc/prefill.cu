@@ -647,8 +647,8 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   uint16_t* part_o = reinterpret_cast<uint16_t*>(a.workspace + W.part_o);
   float* part_lse = reinterpret_cast<float*>(a.workspace + W.part_lse);
   int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
-  const int32_t win = prefill_window(a.T, a.nblk, a.topk);
-  const int32_t nwin = prefill_nwin(a.T, a.nblk, a.topk);
+  const int32_t win = prefill_window(a.T, a.nblk, a.topk, G);
+  const int32_t nwin = prefill_nwin(a.T, a.nblk, a.topk, G);
   // G 8 / 16: the slots shared by many queries of a query pair are computed query-major; the
   // block-major pass and the merge's slot skipping then use the residual selections
   const bool hybrid = prefill_hybrid(G);
