@@ -128,7 +128,8 @@ def test_sparse_page_table_bit_exact(N):
     ([517, 1500, 129, 9000, 40], 1, 64, 8, 16),      # G 8, ragged, 1-block request
     ([3000, 700], 1, 16, 4, 5),                       # G 4
     ([2500, 2600, 2700], 2, 32, 2, 9),                # G 16, N 2
-    ([20000], 1, 8, 8, 32),                           # G 1, k 32 (8 splits)
+    ([20000], 1, 8, 8, 32),                           # G 1, k 32
+    ([3000, 5000, 700], 1, 32, 16, 8),                # Hkv 16 (the largest), G 2
 ])
 def test_paged_sparse_decode(seq_lens, N, Hq, Hkv, topk):
     w = workloads.decode_workload(seq_lens, N, Hq, Hkv, 128, topk, seed=5, device="cpu")
@@ -170,6 +171,7 @@ def test_paged_sparse_decode_ranges_cross_rows():
     (129, 5000, 32, 2, 8, 4),       # G 16, long prefix
     (257, 800, 8, 4, 5, 3),         # G 2: block-major only
     (1, 4000, 64, 8, 16, 12),       # one query after a prefix: a pair with one valid query
+    (300, 900, 32, 16, 4, 2),       # Hkv 16 (the largest), G 2
 ])
 def test_sparse_prefill(T, S, Hq, Hkv, topk, n_shared):
     w = workloads.prefill_workload(T, S, Hq, Hkv, 128, topk, seed=11, device="cpu", n_shared=n_shared)
