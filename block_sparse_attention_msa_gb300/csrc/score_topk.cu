@@ -56,6 +56,10 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // Blocks 0 and `local` are forced; the remaining slots take blocks 1..local-1 by score
 // descending with ties to the lower id (radix select on order-preserving keys, then the
 // lowest ids among the keys equal to the threshold). Writes ids ascending, -1 padding.
+// Rows of up to 1 + 32*kTopkRegs blocks keep their candidate keys in registers (lane l's k-th
+// key is block 1 + l + 32k); every pass checks j < local, so padding keys are never counted.
+constexpr int kTopkRegs = 16;
+
 __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int32_t* ids_out,
                           float* sc_out, TopkScratch& ws) {
   const int lane = threadIdx.x & 31;
@@ -72,14 +76,42 @@ __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int3
   if (m == ncand) {
     for (int j = 1 + lane; j < local; j += 32) ws.sel[nforced + j - 1] = j;
   } else if (m > 0) {
+    // A row that fits is read once into registers (all loads in flight together); a longer
+    // row is re-read per pass, 8 keys per lane requested before any is counted.
+    const bool in_regs = ncand <= 32 * kTopkRegs;
+    uint32_t kr[kTopkRegs];
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < kTopkRegs; ++k) {
+        const int j = 1 + lane + 32 * k;
+        kr[k] = j < local ? float_key(__ldcg(s + j)) : 0u;
+      }
+    }
     uint32_t prefix = 0, pmask = 0;
     int remaining = m;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int b = lane; b < 256; b += 32) ws.hist[b] = 0;
       __syncwarp();
-      for (int j = 1 + lane; j < local; j += 32) {
-        uint32_t key = float_key(__ldcg(s + j));
-        if ((key & pmask) == prefix) atomicAdd(&ws.hist[(key >> shift) & 255u], 1u);
+      if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < kTopkRegs; ++k) {
+          const int j = 1 + lane + 32 * k;
+          if (j < local && (kr[k] & pmask) == prefix) atomicAdd(&ws.hist[(kr[k] >> shift) & 255u], 1u);
+        }
+      } else {
+        for (int j0 = 1; j0 < local; j0 += 32 * 8) {
+          uint32_t kb[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + lane + 32 * u;
+            kb[u] = j < local ? float_key(__ldcg(s + j)) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + lane + 32 * u;
+            if (j < local && (kb[u] & pmask) == prefix) atomicAdd(&ws.hist[(kb[u] >> shift) & 255u], 1u);
+          }
+        }
       }
       __syncwarp();
       // lane l owns digits 255-8l .. 248-8l (descending)
@@ -119,11 +151,17 @@ __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int3
       __syncwarp();
     }
     // prefix is the threshold key; take every key above it and the `remaining` lowest
-    // ids among the keys equal to it.
+    // ids among the keys equal to it (ids ascending: 32 consecutive ids per step).
     int base = nforced, eq_seen = 0;
-    for (int j0 = 1; j0 < local; j0 += 32) {
+    for (int j0 = 1, k = 0; j0 < local; j0 += 32, ++k) {
       const int j = j0 + lane;
-      const uint32_t key = j < local ? float_key(__ldcg(s + j)) : 0u;
+      uint32_t key = 0u;
+      if (in_regs) {
+#pragma unroll
+        for (int t = 0; t < kTopkRegs; ++t) key = t == k ? kr[t] : key;
+      } else {
+        key = j < local ? float_key(__ldcg(s + j)) : 0u;
+      }
       const bool gt = j < local && key > prefix;
       const bool eq = j < local && key == prefix;
       const uint32_t eqm = __ballot_sync(full, eq);
