@@ -56,10 +56,13 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // Blocks 0 and `local` are forced; the remaining slots take blocks 1..local-1 by score
 // descending with ties to the lower id (radix select on order-preserving keys, then the
 // lowest ids among the keys equal to the threshold). Writes ids ascending, -1 padding.
-// Rows of up to 1 + 32*kTopkRegs blocks keep their candidate keys in registers (lane l's k-th
-// key is block 1 + l + 32k); every pass checks j < local, so padding keys are never counted.
-constexpr int kTopkRegs = 16;
-
+// KR > 0 (a warp running one top-k at the tail of the decode scorer, where its latency is
+// exposed): rows of up to 1 + 32*KR blocks keep their candidate keys in registers (lane l's
+// k-th key is block 1 + l + 32k), longer rows request 8 keys per lane before counting them.
+// KR = 0 (the multi-row top-k kernel, which hides latency with many resident warps): each
+// pass reads the keys one per lane per step, keeping the register count and occupancy low.
+// Every pass checks j < local, so padding keys are never counted.
+template <int KR>
 __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int32_t* ids_out,
                           float* sc_out, TopkScratch& ws) {
   const int lane = threadIdx.x & 31;
@@ -78,11 +81,11 @@ __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int3
   } else if (m > 0) {
     // A row that fits is read once into registers (all loads in flight together); a longer
     // row is re-read per pass, 8 keys per lane requested before any is counted.
-    const bool in_regs = ncand <= 32 * kTopkRegs;
-    uint32_t kr[kTopkRegs];
+    const bool in_regs = KR > 0 && ncand <= 32 * KR;
+    uint32_t kr[KR > 0 ? KR : 1];
     if (in_regs) {
 #pragma unroll
-      for (int k = 0; k < kTopkRegs; ++k) {
+      for (int k = 0; k < KR; ++k) {
         const int j = 1 + lane + 32 * k;
         kr[k] = j < local ? float_key(__ldcg(s + j)) : 0u;
       }
@@ -94,9 +97,14 @@ __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int3
       __syncwarp();
       if (in_regs) {
 #pragma unroll
-        for (int k = 0; k < kTopkRegs; ++k) {
+        for (int k = 0; k < KR; ++k) {
           const int j = 1 + lane + 32 * k;
           if (j < local && (kr[k] & pmask) == prefix) atomicAdd(&ws.hist[(kr[k] >> shift) & 255u], 1u);
+        }
+      } else if (KR == 0) {
+        for (int j = 1 + lane; j < local; j += 32) {
+          const uint32_t key = float_key(__ldcg(s + j));
+          if ((key & pmask) == prefix) atomicAdd(&ws.hist[(key >> shift) & 255u], 1u);
         }
       } else {
         for (int j0 = 1; j0 < local; j0 += 32 * 8) {
@@ -158,7 +166,7 @@ __device__ void warp_topk(const float* __restrict__ s, int local, int topk, int3
       uint32_t key = 0u;
       if (in_regs) {
 #pragma unroll
-        for (int t = 0; t < kTopkRegs; ++t) key = t == k ? kr[t] : key;
+        for (int t = 0; t < KR; ++t) key = t == k ? kr[t] : key;
       } else {
         key = j < local ? float_key(__ldcg(s + j)) : 0u;
       }
@@ -379,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool bad_r = false;
         const int qp = clamp_seq(p.seq_lens, rb, N, p.max_blocks, bad_r) - N + i;
         const int64_t orow = (r * Hkv + gg) * p.topk;
-        warp_topk(p.scores + (r * Hkv + gg) * p.max_blocks, qp / 128, p.topk, p.block_ids + orow,
+        warp_topk<16>(p.scores + (r * Hkv + gg) * p.max_blocks, qp / 128, p.topk, p.block_ids + orow,
                   p.sel_scores ? p.sel_scores + orow : nullptr, stopk[warp]);
         if (p.fpt) {
           // the sparse page table row of the selection just written (same warp: ordered by
@@ -770,7 +778,7 @@ __global__ void __launch_bounds__(256) topk_rows_kernel(const ScoreArgs a) {
   const int b = (int)(r / a.N);
   bool bad = false;
   const int qp = clamp_seq(a.seq_lens, b, a.N, a.max_blocks, bad) - a.N + (int)(r % a.N);
-  warp_topk(a.scores + item * a.max_blocks, qp / 128, a.topk, a.block_ids + item * a.topk,
+  warp_topk<0>(a.scores + item * a.max_blocks, qp / 128, a.topk, a.block_ids + item * a.topk,
             a.sel_scores ? a.sel_scores + item * a.topk : nullptr, ws[warp]);
 }
 
