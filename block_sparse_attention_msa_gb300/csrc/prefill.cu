@@ -405,10 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == 1) {
       // ================================================================ MMA issuer
-      // Preferred order S(0), S(1), then O(k), S(k+2) for k = 0, 1, ...: S(k+2) writes the tensor
-      // memory that P(k) occupies, so it follows O(k). When the next S is waiting for its data
-      // while P of the next O is ready, the O goes first. An idle issuer blocks in hardware on
-      // the next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
+      // Order S(0), S(1), then O(k), S(k+2) for k = 0, 1, ...: S(k+2) writes the tensor memory
+      // that P(k) occupies, so it follows O(k). A ready O is issued before a ready S: the
+      // warpgroup whose P is ready waits on that O for its epilogue, while the one the next S
+      // serves is usually still in its own epilogue. An idle issuer blocks in hardware on the
+      // next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
       // within a few hundred cycles. All state stays in registers.
       if (lane == 0) {
         const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
@@ -421,6 +422,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int si = 0, oi = 0;
         uint32_t idle = 0;
         while (oi < n && !*fail) {
+          // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
+          if (oi < si) {
+            const int b = oi & 1;
+            if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
+                (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
+              tmem_fence_after();
+              const int c = b ? kvb1 : kvb0;
+              const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
+                umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
+              }
+              umma_commit(&B.o_full[b]);
+              // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
+              // oi is the last one on this K/V load
+              const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
+              if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
+              ++oi;
+              idle = 0;
+              continue;
+            }
+          }
           // ---- S(si): needs O(si-2) issued and completed, its queries and its K/V block
           if (si < n && oi >= si - 1) {
             const int b = si & 1, qs = si % kQStages;
@@ -462,32 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               continue;
             }
           }
-          // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
-          if (oi < si) {
-            const int b = oi & 1;
-            if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
-                (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
-              tmem_fence_after();
-              const int c = b ? kvb1 : kvb0;
-              const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
-  #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-                umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
-              }
-              umma_commit(&B.o_full[b]);
-              // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
-              // oi is the last one on this K/V load
-              const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
-              if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
-              ++oi;
-              idle = 0;
-              continue;
-            }
-            mbar_try_wait_hint(&B.p_full[b], (oi >> 1) & 1, kIssuerNap);
-          } else {
-            __nanosleep(32);
-          }
+          // ---- nothing ready: block briefly on the next O's P
+          if (oi < si) mbar_try_wait_hint(&B.p_full[oi & 1], (oi >> 1) & 1, kIssuerNap);
+          else __nanosleep(32);
           if (++idle > kWaitLimit) {
             msa_record_error(kErrTimeout);
             *fail = 1;
