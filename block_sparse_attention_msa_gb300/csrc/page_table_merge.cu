@@ -9,9 +9,10 @@
 //
 // LSE merge -- same article, section "KV-block-major sparse attention reduces redundant KV
 // movement": every KV block yields a partial O, and a Log-Sum-Exp reduction rescales and
-// sums the partials. The same merge finishes the split-K decode. One warp per (unit, head):
-// lanes own 4 consecutive channels, partials are read once, coalesced, and the result is
-// written as bf16 with its fp32 LSE.
+// sums the partials. The same merge finishes the decode, whose warps each leave one partial
+// per row segment in the slot of the segment's first page. One warp per (unit, head): lanes
+// own 4 consecutive channels, partials are read once, coalesced, and the result is written as
+// bf16 with its fp32 LSE. (The prefill's chunk-major partials have their own merge below.)
 #include <algorithm>
 
 #include "common.cuh"

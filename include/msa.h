@@ -288,8 +288,8 @@ MSA_API int msa_prefill_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv,
                        size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
- * Step (c) of msa_sparse_prefill on its own, also used by the decode split-K: merge
- * partial attention outputs with their log-sum-exp weights.
+ * Step (c) of msa_sparse_prefill on its own (the decode finishes its per-page slots with the
+ * same merge): merge partial attention outputs with their log-sum-exp weights.
  *
  * Passage: Together AI MiniMax-M3 serving article, section "KV-block-major sparse
  * attention reduces redundant KV movement" (a Log-Sum-Exp based reduction rescales and
