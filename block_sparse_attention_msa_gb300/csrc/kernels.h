@@ -91,9 +91,11 @@ inline int64_t prefill_pairs(int64_t T, int32_t Hkv, int32_t G) {
   const int64_t q2 = 2 * (128 / G);
   return (int64_t)Hkv * ((T + q2 - 1) / q2);
 }
+// Pair slots per group: the chunk's queries in 128-query spans (a pair never crosses a span).
+inline int64_t prefill_qpos(int64_t T) { return (T + 127) / 128 * 128; }
 struct PrefillWorkspace {
   size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc;
-  size_t residual, dcnt, dblk, dmask, dense_o, dense_lse, total;  // query-major part (G 8, 16)
+  size_t residual, dcnt, dblk, dmask, dense_o, dense_lse, qperm, total;  // query-major (G 8, 16)
 };
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 // Prefill work lists are per (group, query window, KV block): queries are cut into windows so
@@ -142,6 +144,7 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
       w.dmask = off;      off = ws_align(off + 4 * pairs * kMaxDense);
       w.dense_o = off;    off = ws_align(off + 2 * rows * 128);
       w.dense_lse = off;  off = ws_align(off + 4 * rows);
+      w.qperm = off;      off = ws_align(off + 4 * (size_t)Hkv * prefill_qpos(T));
     }
   }
   w.total = off;
@@ -151,6 +154,7 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
 // chosen by at least half of the pair's queries (ascending, at most kMaxDense) with a bit mask of
 // the queries that chose each; the residual selections go to the block-major pass.
 struct DenseWorkspace {
+  int32_t* qperm;      // [Hkv, prefill_qpos(T)]: query of each pair slot (-1: none)
   int32_t* residual;   // [T, Hkv, k]
   int32_t* dcnt;       // [pairs]
   int32_t* dblk;       // [pairs, kMaxDense]

@@ -12,8 +12,12 @@
 // passes, and the merge (row a7) combines the query-major partial with the block-major ones.
 //
 // GB300 design.
-//  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G consecutive
-//      queries of one group): counts the pair's selections per block in shared memory, keeps
+//  (o) pair_order_kernel, one CTA per (group, 128-query span): orders the span's queries so
+//      that those choosing the span's popular blocks (chosen by at least half of the span) come
+//      first. Pairs are consecutive slots of that order, so queries that share blocks fill the
+//      same tiles and fewer masked rows ride through the query-major MMAs.
+//  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G slots of one
+//      group's order): counts the pair's selections per block in shared memory, keeps
 //      the blocks chosen by at least half of the pair's queries (at most kMaxDense, ascending)
 //      with a bit mask of the queries that chose each, and writes the residual selections (the
 //      dense ones replaced by -1) for the block-major pass.
@@ -46,10 +50,60 @@ constexpr int kSelThreads = 256;
 // then a prefix scan over the window ranks the dense blocks in ascending order.
 constexpr int kHistBlocks = 16384;
 
+// Query of pair slot `pos` of group g (-1: past the chunk). Without an order, slot = query.
+__device__ __forceinline__ int64_t slot_query(const int32_t* qperm, int64_t npos, int g,
+                                              int64_t pos, int32_t T) {
+  if (!qperm) return pos < T ? pos : -1;
+  return qperm[(int64_t)g * npos + pos];
+}
+
+constexpr int kSpan = 128;
+// One CTA per (128-query span, group): block counts of the span's selections in shared memory
+// (nb_max = blocks of the whole key range), each query's number of selections among the blocks
+// chosen by at least half of the span's queries, then a stable rank by that number descending.
+__global__ void __launch_bounds__(kSpan)
+    pair_order_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv,
+                      int32_t topk, int32_t nb_max, int64_t npos, int32_t* __restrict__ qperm) {
+  extern __shared__ uint32_t span_cnt[];  // [nb_max]
+  __shared__ int32_t score[kSpan];
+  const int r = threadIdx.x;
+  const int g = (int)(blockIdx.x % Hkv);
+  const int64_t span = blockIdx.x / Hkv;
+  const int64_t t = span * kSpan + r;
+  const bool valid = t < T;
+  const int nvalid = (int)min((int64_t)kSpan, (int64_t)T - span * kSpan);
+  for (int j = r; j < nb_max; j += kSpan) span_cnt[j] = 0u;
+  __syncthreads();
+  const int32_t* sel = block_ids + (t * Hkv + g) * topk;
+  if (valid)
+    for (int k = 0; k < topk; ++k) {
+      const int32_t j = sel[k];
+      if (j >= 0 && j < nb_max) atomicAdd(&span_cnt[j], 1u);
+    }
+  __syncthreads();
+  int sc = -1;  // slots past the chunk sort last
+  if (valid) {
+    sc = 0;
+    for (int k = 0; k < topk; ++k) {
+      const int32_t j = sel[k];
+      if (j >= 0 && j < nb_max && 2 * (int)span_cnt[j] >= nvalid) ++sc;
+    }
+  }
+  score[r] = sc;
+  __syncthreads();
+  int rank = 0;
+  for (int q = 0; q < kSpan; ++q) {
+    const int s2 = score[q];
+    rank += (s2 > sc || (s2 == sc && q < r)) ? 1 : 0;
+  }
+  qperm[(int64_t)g * npos + span * kSpan + rank] = valid ? (int32_t)t : -1;
+}
+
 __global__ void __launch_bounds__(kSelThreads)
     dense_select_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv, int32_t G,
                         int32_t topk, int32_t qpt, int32_t ppg, int32_t thr, int64_t q_start,
-                        int32_t hw, int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
+                        int32_t hw, const int32_t* __restrict__ qperm, int64_t npos,
+                        int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
                         int32_t* __restrict__ dblk, uint32_t* __restrict__ dmask,
                         float* __restrict__ part_lse) {
   extern __shared__ __align__(16) uint8_t hist_smem[];
@@ -59,13 +113,14 @@ __global__ void __launch_bounds__(kSelThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t pair = blockIdx.x;
   const int g = (int)(pair / ppg);
-  const int64_t t0 = (pair % ppg) * 2 * qpt;
+  const int64_t t0 = (pair % ppg) * 2 * qpt;  // first pair slot
   const int nq = 2 * qpt, n = nq * topk;
-  const int64_t t_last = min((int64_t)T - 1, t0 + nq - 1);
+  // the pair's queries lie in the 128-query span of its slots
+  const int64_t t_last = min((int64_t)T - 1, qperm ? t0 / kSpan * kSpan + kSpan - 1 : t0 + nq - 1);
   const int64_t nb = (q_start + t_last) / 128 + 1;  // blocks the pair can have chosen
   for (int r = tid; r < nq * G; r += kSelThreads) {
-    const int64_t t = t0 + r / G;
-    if (t < T) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
+    const int64_t t = slot_query(qperm, npos, g, t0 + r / G, T);
+    if (t >= 0) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
   }
   int ranked = 0;  // dense blocks ranked in earlier windows
   for (int64_t base = 0; base < nb; base += hw) {
@@ -74,8 +129,8 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     for (int e = tid; e < n; e += kSelThreads) {
       const int q = e / topk;
-      const int64_t t = t0 + q;
-      if (t >= T) continue;
+      const int64_t t = slot_query(qperm, npos, g, t0 + q, T);
+      if (t < 0) continue;
       const int64_t id = block_ids[(t * Hkv + g) * topk + e % topk];
       if (id >= base && id < base + w) atomicOr(&msk[id - base], 1u << q);
     }
@@ -115,8 +170,8 @@ __global__ void __launch_bounds__(kSelThreads)
     // every window (negative or past the causal range) are copied once, with the first window
     for (int e = tid; e < n; e += kSelThreads) {
       const int q = e / topk;
-      const int64_t t = t0 + q;
-      if (t >= T) continue;
+      const int64_t t = slot_query(qperm, npos, g, t0 + q, T);
+      if (t < 0) continue;
       const int64_t at = (t * Hkv + g) * topk + e % topk;
       const int32_t id = block_ids[at];
       if (id >= base && id < base + w)
@@ -159,6 +214,8 @@ struct Bars {
 };
 
 struct DenseKParams {
+  const int32_t* qperm;  // query of each pair slot, or null (slot = query)
+  int64_t npos;
   const int32_t* dcnt;
   const int32_t* dblk;
   const uint32_t* dmask;
@@ -177,6 +234,15 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   msa_record_error(kErrTimeout);
   *fail = 1;
   return false;
+}
+
+// The r-th pair of this CTA (-1: none). Round r covers pairs [r*grid, (r+1)*grid), and the
+// CTA's place in it moves by one each round: pairs are ordered by span and the ordered spans
+// put light pairs (few shared blocks) at fixed positions, which a fixed place would hand to
+// the same CTAs every round.
+__device__ __forceinline__ int64_t cta_pair(int64_t r, int64_t npairs) {
+  const int64_t pr = r * gridDim.x + (blockIdx.x + r) % gridDim.x;
+  return pr < npairs ? pr : -1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -216,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = B.tmem_base;
   const uint32_t sbase = smem_u32(smem);
   const int G = p.G, qpt = p.qpt;
+  const int64_t rounds = (p.npairs + gridDim.x - 1) / gridDim.x;
 
   static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
   if (warp < 4) {
@@ -229,17 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&vmap);
       }
       int pairs_done = 0, kv_loads = 0;
-      for (int64_t pr = blockIdx.x; pr < p.npairs && !*fail; pr += gridDim.x) {
+      for (int64_t r = 0; r < rounds && !*fail; ++r) {
+        const int64_t pr = cta_pair(r, p.npairs);
+        if (pr < 0) continue;
         const int L = p.dcnt[pr];
         if (L <= 0) continue;
         const int g = (int)(pr / p.ppg);
-        const int64_t t0 = (pr % p.ppg) * 2 * qpt;
-        const int nvalid = (int)min((int64_t)2 * qpt, (int64_t)p.T - t0);
+        const int64_t t0 = (pr % p.ppg) * 2 * qpt;  // first pair slot
+        const int64_t tq = lane < 2 * qpt ? slot_query(p.qperm, p.npos, g, t0 + lane, p.T) : -1;
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, tq >= 0));
         if (pairs_done > 0 && !wait_or_fail(&B.q_empty, (pairs_done - 1) & 1, fail)) break;
         if (lane == 0) mbar_expect_tx(&B.q_full, (uint32_t)(nvalid * G * 256));
         __syncwarp();
-        if (lane < nvalid) {
-          const int64_t t = t0 + lane;
+        if (tq >= 0) {
+          const int64_t t = tq;
           uint8_t* qdst = smem + kOffQ + (lane / qpt) * kTileBytes;
           const int q = lane % qpt;
           if (p.q_atoms) {
@@ -284,11 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);
         // the CTA's block sequence: total count, and the pair boundaries as they come
         int total = 0;
-        for (int64_t pr = blockIdx.x; pr < p.npairs; pr += gridDim.x) total += max(p.dcnt[pr], 0);
+        for (int64_t r = 0; r < rounds; ++r) {
+          const int64_t pr = cta_pair(r, p.npairs);
+          if (pr >= 0) total += max(p.dcnt[pr], 0);
+        }
         int sN[2] = {0, 0}, oN[2] = {0, 0};
         // per X: pair index and first/last block index of the pair that block sN[X] / oN[X]
         // belongs to (advanced lazily)
-        int64_t s_pr[2] = {blockIdx.x, blockIdx.x}, o_pr[2] = {blockIdx.x, blockIdx.x};
+        int64_t s_rd[2] = {0, 0}, o_rd[2] = {0, 0};  // rounds of the pairs of blocks sN / oN
         int s_end[2] = {0, 0}, s_pairs[2] = {-1, -1};
         int o_first[2] = {0, 0}, o_end[2] = {0, 0}, o_pairs[2] = {-1, -1};
         uint32_t idle = 0;
@@ -299,12 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- O_X(oN[X])
             if (oN[X] < sN[X]) {
               const int n = oN[X];
-              while (n >= o_end[X] && o_pr[X] < p.npairs) {  // advance to the pair of block n
-                if (o_pairs[X] >= 0) o_pr[X] += gridDim.x;
-                while (o_pr[X] < p.npairs && p.dcnt[o_pr[X]] <= 0) o_pr[X] += gridDim.x;
-                if (o_pr[X] >= p.npairs) break;
+              while (n >= o_end[X] && o_rd[X] < rounds) {  // advance to the pair of block n
+                if (o_pairs[X] >= 0) ++o_rd[X];
+                while (o_rd[X] < rounds && (cta_pair(o_rd[X], p.npairs) < 0 ||
+                                            p.dcnt[cta_pair(o_rd[X], p.npairs)] <= 0))
+                  ++o_rd[X];
+                if (o_rd[X] >= rounds) break;
                 o_first[X] = o_end[X];
-                o_end[X] += p.dcnt[o_pr[X]];
+                o_end[X] += p.dcnt[cta_pair(o_rd[X], p.npairs)];
                 ++o_pairs[X];
               }
               if (n >= o_end[X]) {  // block sequence inconsistent with the pair counts
@@ -333,11 +408,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- S_X(sN[X])
             if (sN[X] < total && oN[X] >= sN[X]) {
               const int n = sN[X];
-              while (n >= s_end[X] && s_pr[X] < p.npairs) {
-                if (s_pairs[X] >= 0) s_pr[X] += gridDim.x;
-                while (s_pr[X] < p.npairs && p.dcnt[s_pr[X]] <= 0) s_pr[X] += gridDim.x;
-                if (s_pr[X] >= p.npairs) break;
-                s_end[X] += p.dcnt[s_pr[X]];
+              while (n >= s_end[X] && s_rd[X] < rounds) {
+                if (s_pairs[X] >= 0) ++s_rd[X];
+                while (s_rd[X] < rounds && (cta_pair(s_rd[X], p.npairs) < 0 ||
+                                            p.dcnt[cta_pair(s_rd[X], p.npairs)] <= 0))
+                  ++s_rd[X];
+                if (s_rd[X] >= rounds) break;
+                s_end[X] += p.dcnt[cta_pair(s_rd[X], p.npairs)];
                 ++s_pairs[X];
               }
               if (n >= s_end[X]) {
@@ -394,12 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tmem = tmem + lane_addr + 256 + X * 128;
     const uint32_t qbit = 1u << (X * qpt + qi);
     int n = 0, pairs_done = 0;
-    for (int64_t pr = blockIdx.x; pr < p.npairs && !*fail; pr += gridDim.x) {
+    for (int64_t r = 0; r < rounds && !*fail; ++r) {
+      const int64_t pr = cta_pair(r, p.npairs);
+      if (pr < 0) continue;
       const int L = p.dcnt[pr];
       if (L <= 0) continue;
       const int g = (int)(pr / p.ppg);
-      const int64_t t = (pr % p.ppg) * 2 * qpt + X * qpt + qi;
-      const bool valid = t < p.T;
+      const int64_t t = slot_query(p.qperm, p.npos, g, (pr % p.ppg) * 2 * qpt + X * qpt + qi, p.T);
+      const bool valid = t >= 0;
       const int64_t pos = p.q_start + t;
       float m_run = -INFINITY, l = 0.f;             // running max (log2 units) and sum
       uint32_t mask_next = p.dmask[pr * kMaxDense];
@@ -534,11 +613,26 @@ cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_k
   // the window covers every block of the chunk when it fits (one pass), else kHistBlocks
   const int32_t hw = (int32_t)std::min<int64_t>(kHistBlocks, (S_kv + 127) / 128);
   const size_t smem = (6 * (size_t)hw + 15) / 16 * 16;
+  // pair order: while the key range's block counts fit in shared memory, else slot = query
+  const int32_t nb_max = (int32_t)std::min<int64_t>((S_kv + 127) / 128, INT32_MAX);
+  const bool ordered = nb_max <= kHistBlocks;
+  const int64_t npos = prefill_qpos(T);
+  if (ordered) {
+    const size_t osmem = 4 * (size_t)nb_max;
+    cudaError_t e0 = cudaFuncSetAttribute(pair_order_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem);
+    if (e0 != cudaSuccess) return e0;
+    pair_order_kernel<<<(unsigned)(Hkv * (npos / kSpan)), kSpan, osmem, stream>>>(
+        block_ids, T, Hkv, topk, nb_max, npos, w.qperm);
+    e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
   cudaError_t e = cudaFuncSetAttribute(dense_select_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dense_select_kernel<<<(unsigned)npairs, kSelThreads, smem, stream>>>(
-      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, hw, w.residual, w.dcnt, w.dblk, w.dmask,
+      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, hw, ordered ? w.qperm : nullptr, npos,
+      w.residual, w.dcnt, w.dblk, w.dmask,
       w.part_lse);
   return cudaGetLastError();
 }
@@ -549,6 +643,8 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
                                    const int32_t* page_table, int64_t num_pages,
                                    const DenseWorkspace& w, cudaStream_t stream) {
   DenseKParams p;
+  p.qperm = (S_kv + 127) / 128 <= kHistBlocks ? w.qperm : nullptr;  // as launch_dense_select
+  p.npos = prefill_qpos(T);
   p.dcnt = w.dcnt;
   p.dblk = w.dblk;
   p.dmask = w.dmask;
