@@ -164,29 +164,29 @@ def visible_keys(block_ids: torch.Tensor, q_pos: torch.Tensor) -> torch.Tensor:
 
 def build_workloads(dev, seed_offset: int, small: bool = False):
     # --small (profiling captures only): 8 decode requests and an 8192-token prefill chunk
-    c2 = workloads.cfg2(dev, seed=2 + seed_offset)
-    c4 = workloads.cfg4(dev, seed=4 + seed_offset, B=8 if small else None)
-    c3 = workloads.cfg3(dev, seed=3 + seed_offset, T=8192 if small else None)
+    wsc = workloads.decode_scoring(dev, seed=2 + seed_offset)
+    wdc = workloads.paged_decode(dev, seed=4 + seed_offset, B=8 if small else None)
+    wpf = workloads.causal_prefill(dev, seed=3 + seed_offset, T=8192 if small else None)
     # algorithmic work per stage
-    B, Hkv, Di = c2["B"], c2["Hkv"], c2["Di"]
-    sl2 = c2["seq_lens"].to(torch.int64)
-    c2["bytes"] = int(sl2.sum().item()) * Hkv * Di * 2 + c2["q_idx"].numel() * 2 \
-        + c2["page_table"].numel() * 4 + B * Hkv * c2["topk"] * 8
-    q_pos4 = c4["seq_lens"].to(torch.int64) - 1
-    keys4 = visible_keys(c4["block_ids"], q_pos4)                 # [B, Hkv]
-    G4 = c4["Hq"] // c4["Hkv"]
-    c4["bytes"] = int(keys4.sum().item()) * c4["D"] * 2 * 2 + c4["q"].numel() * 2 * 2 \
-        + c4["B"] * c4["Hq"] * 4
-    c4["kv_bytes"] = int(keys4.sum().item()) * c4["D"] * 2 * 2
-    q_pos3 = torch.arange(c3["S_kv"] - c3["T"], c3["S_kv"], device=dev, dtype=torch.int64)
-    keys3 = visible_keys(c3["block_ids"], q_pos3)                 # [T, Hkv]
-    G3 = c3["Hq"] // c3["Hkv"]
-    c3["flops"] = 4 * c3["D"] * G3 * int(keys3.sum().item())
+    B, Hkv, Di = wsc["B"], wsc["Hkv"], wsc["Di"]
+    sl2 = wsc["seq_lens"].to(torch.int64)
+    wsc["bytes"] = int(sl2.sum().item()) * Hkv * Di * 2 + wsc["q_idx"].numel() * 2 \
+        + wsc["page_table"].numel() * 4 + B * Hkv * wsc["topk"] * 8
+    q_pos4 = wdc["seq_lens"].to(torch.int64) - 1
+    keys4 = visible_keys(wdc["block_ids"], q_pos4)                 # [B, Hkv]
+    Gdc = wdc["Hq"] // wdc["Hkv"]
+    wdc["bytes"] = int(keys4.sum().item()) * wdc["D"] * 2 * 2 + wdc["q"].numel() * 2 * 2 \
+        + wdc["B"] * wdc["Hq"] * 4
+    wdc["kv_bytes"] = int(keys4.sum().item()) * wdc["D"] * 2 * 2
+    q_pos3 = torch.arange(wpf["S_kv"] - wpf["T"], wpf["S_kv"], device=dev, dtype=torch.int64)
+    keys3 = visible_keys(wpf["block_ids"], q_pos3)                 # [T, Hkv]
+    Gpf = wpf["Hq"] // wpf["Hkv"]
+    wpf["flops"] = 4 * wpf["D"] * Gpf * int(keys3.sum().item())
     # bf16 partial rows (G per selection, D channels) written once and read once, + fp32 LSE
-    nsel3 = int((c3["block_ids"] >= 0).sum().item())
-    c3["partial_bytes"] = nsel3 * G3 * (2 * c3["D"] * 2 + 4 * 2)
-    del G4
-    return c2, c4, c3
+    nsel3 = int((wpf["block_ids"] >= 0).sum().item())
+    wpf["partial_bytes"] = nsel3 * Gpf * (2 * wpf["D"] * 2 + 4 * 2)
+    del Gdc
+    return wsc, wdc, wpf
 
 
 def src_hash(*names):
@@ -224,41 +224,41 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(dev)
     msa.load(build_if_missing=True)
     pk = peaks()
-    c2, c4, c3 = build_workloads(dev, seed_offset=1000 * rank, small=args.small)
+    wsc, wdc, wpf = build_workloads(dev, seed_offset=1000 * rank, small=args.small)
     run = set(args.stages.split(","))
     wsp = msa.Workspace()
     # preallocated outputs
-    R2 = c2["B"]
-    ids2 = torch.empty((R2, c2["Hkv"], c2["topk"]), dtype=torch.int32, device=dev)
-    sc2 = torch.empty((R2, c2["Hkv"], c2["topk"]), dtype=torch.float32, device=dev)
-    R4 = c4["B"]
-    fpt4 = torch.empty((R4 * c4["Hkv"], c4["topk"]), dtype=torch.int32, device=dev)
-    len4 = torch.empty((R4 * c4["Hkv"],), dtype=torch.int32, device=dev)
-    o4 = torch.empty((R4, c4["Hq"], c4["D"]), dtype=torch.bfloat16, device=dev)
-    lse4 = torch.empty((R4, c4["Hq"]), dtype=torch.float32, device=dev)
-    o3 = torch.empty((c3["T"], c3["Hq"], c3["D"]), dtype=torch.bfloat16, device=dev)
-    lse3 = torch.empty((c3["T"], c3["Hq"]), dtype=torch.float32, device=dev)
+    Rsc = wsc["B"]
+    ids_sc = torch.empty((Rsc, wsc["Hkv"], wsc["topk"]), dtype=torch.int32, device=dev)
+    scores_sc = torch.empty((Rsc, wsc["Hkv"], wsc["topk"]), dtype=torch.float32, device=dev)
+    Rdc = wdc["B"]
+    fpt_dc = torch.empty((Rdc * wdc["Hkv"], wdc["topk"]), dtype=torch.int32, device=dev)
+    len4 = torch.empty((Rdc * wdc["Hkv"],), dtype=torch.int32, device=dev)
+    o4 = torch.empty((Rdc, wdc["Hq"], wdc["D"]), dtype=torch.bfloat16, device=dev)
+    lse4 = torch.empty((Rdc, wdc["Hq"]), dtype=torch.float32, device=dev)
+    o3 = torch.empty((wpf["T"], wpf["Hq"], wpf["D"]), dtype=torch.bfloat16, device=dev)
+    lse3 = torch.empty((wpf["T"], wpf["Hq"]), dtype=torch.float32, device=dev)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record()
         if "score" in run:
-            msa.index_score_topk(c2["q_idx"], c2["k_idx_pages"], c2["page_table"], c2["seq_lens"], 1,
-                                 c2["topk"], workspace=wsp, out=(ids2, sc2))
+            msa.index_score_topk(wsc["q_idx"], wsc["k_idx_pages"], wsc["page_table"], wsc["seq_lens"], 1,
+                                 wsc["topk"], workspace=wsp, out=(ids_sc, scores_sc))
         if ev is not None:
             ev[1].record()
         if "decode" in run:
-            msa.build_sparse_page_table(c4["block_ids"], c4["page_table"], c4["seq_lens"], 1,
-                                        c4["num_pages"], out=(fpt4, len4))
+            msa.build_sparse_page_table(wdc["block_ids"], wdc["page_table"], wdc["seq_lens"], 1,
+                                        wdc["num_pages"], out=(fpt_dc, len4))
         if ev is not None:
             ev[2].record()
         if "decode" in run:
-            msa.paged_sparse_decode(c4["q"], c4["k_cache"], c4["v_cache"], fpt4, len4, workspace=wsp,
+            msa.paged_sparse_decode(wdc["q"], wdc["k_cache"], wdc["v_cache"], fpt_dc, len4, workspace=wsp,
                                     out=(o4, lse4))
         if ev is not None:
             ev[3].record()
         if "prefill" in run:
-            msa.sparse_prefill(c3["q"], c3["k"], c3["v"], c3["block_ids"], workspace=wsp,
+            msa.sparse_prefill(wpf["q"], wpf["k"], wpf["v"], wpf["block_ids"], workspace=wsp,
                                out=(o3, lse3))
         if ev is not None:
             ev[4].record()
@@ -290,28 +290,28 @@ def run_ours(args, ws, rank, local):
     err = msa.device_error()
 
     eps = 1e-9
-    score_gbs = c2["bytes"] / (max(score_ms, eps) * 1e-3) / 1e9
-    dec_gbs = c4["bytes"] / (max(pt_ms + dec_ms, eps) * 1e-3) / 1e9
-    pre_tflops = c3["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
-    value = job_throughput(c2["bytes"], max(score_ms, eps), ws) / 1e9
+    score_gbs = wsc["bytes"] / (max(score_ms, eps) * 1e-3) / 1e9
+    dec_gbs = wdc["bytes"] / (max(pt_ms + dec_ms, eps) * 1e-3) / 1e9
+    pre_tflops = wpf["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
+    value = job_throughput(wsc["bytes"], max(score_ms, eps), ws) / 1e9
 
     # e2e through host buffers for the headline stage
-    e2e = e2e_score(msa, c2, wsp, dev, args.steps, ws) if "score" in run else None
+    e2e = e2e_score(msa, wsc, wsp, dev, args.steps, ws) if "score" in run else None
 
     h_score = src_hash("score_topk.cu")
     roofline = {"kernel": "score_decode_kernel (msa_index_score_topk)", "bound": "hbm",
                 "achieved": round(score_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(score_gbs / pk["hbm_gbs"], 4),
                 "traffic": recorded_traffic("score_decode_kernel", h_score),
-                "algorithmic_bytes": c2["bytes"], "peak_source": pk["source"]}
+                "algorithmic_bytes": wsc["bytes"], "peak_source": pk["source"]}
     stages = {
         "index_score_topk": {"config": "8 x 60032 tokens, Hkv 8, Di 128, k 16", "ms": round(score_ms, 4),
                              "GB/s": round(score_gbs, 1), "frac_hbm": round(score_gbs / pk["hbm_gbs"], 4),
-                             "bytes": c2["bytes"]},
+                             "bytes": wsc["bytes"]},
         "sparse_decode": {"config": "64 req, ctx U[8K,128K], Hq 64, Hkv 8, D 128, k 16",
                           "ms_page_table": round(pt_ms, 4), "ms_decode": round(dec_ms, 4),
                           "GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
-                          "bytes": c4["bytes"], "kv_bytes": c4["kv_bytes"],
+                          "bytes": wdc["bytes"], "kv_bytes": wdc["kv_bytes"],
                           "traffic": recorded_traffic("paged_decode_kernel", src_hash("decode.cu"))},
         "sparse_prefill": {"config": "T 32768 causal, Hq 64, Hkv 8, D 128, k 16", "ms": round(pre_ms, 4),
                            "TFLOP/s": round(pre_tflops, 1),
@@ -319,13 +319,13 @@ def run_ours(args, ws, rank, local):
                            "kernels": "query-major selection + attention for blocks shared by a "
                                       "query pair; bucketing + block-major attention for the "
                                       "rest; LSE merge (per-kernel shares: profiles/)",
-                           "flops": c3["flops"],
+                           "flops": wpf["flops"],
                            # a purely block-major prefill writes one bf16 partial of G rows per
                            # (query, block) selection and reads it back: that traffic alone takes
                            # block_major_floor_ms at the measured HBM bandwidth (the query-major
                            # pass removes most of it for shared blocks)
-                           "block_major_partials_bytes": c3["partial_bytes"],
-                           "block_major_floor_ms": round(c3["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
+                           "block_major_partials_bytes": wpf["partial_bytes"],
+                           "block_major_floor_ms": round(wpf["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
                            # DRAM bytes of the two attention kernels per call (null when either
                            # source changed since it was profiled)
                            "traffic": prefill_traffic()},
@@ -350,29 +350,29 @@ def run_ours(args, ws, rank, local):
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
         if key not in run:
             stages[name] = None
-    if args.cfg5:
-        line["cfg5"] = run_cfg5(args, local)
+    if args.long_context:
+        line["long_context"] = run_long_context(args, local)
     if args.small or run != {"score", "decode", "prefill"}:
         line["config"]["partial_run"] = f"stages={sorted(run)} small={args.small} (profiling only)"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and "score" in run:
-        line["cpu_baseline"] = cpu_baseline(c2, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wsc, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
+def e2e_score(msa, wsc, wsp, dev, steps: int, ws: int):
     """Headline stage through the public API with pinned host buffers: per step the query
     index rows, page table and lengths go host->device and the selection comes back; the
     paged K-index cache is resident state (it is written once per token, not per step)."""
-    h_q = c2["q_idx"].cpu().pin_memory()
-    h_pt = c2["page_table"].cpu().pin_memory()
-    h_sl = c2["seq_lens"].cpu().pin_memory()
-    R, Hkv, k = c2["B"], c2["Hkv"], c2["topk"]
+    h_q = wsc["q_idx"].cpu().pin_memory()
+    h_pt = wsc["page_table"].cpu().pin_memory()
+    h_sl = wsc["seq_lens"].cpu().pin_memory()
+    R, Hkv, k = wsc["B"], wsc["Hkv"], wsc["topk"]
     h_ids = torch.empty((R, Hkv, k), dtype=torch.int32).pin_memory()
     h_sc = torch.empty((R, Hkv, k), dtype=torch.float32).pin_memory()
-    d_q = torch.empty_like(c2["q_idx"])
-    d_pt = torch.empty_like(c2["page_table"])
-    d_sl = torch.empty_like(c2["seq_lens"])
+    d_q = torch.empty_like(wsc["q_idx"])
+    d_pt = torch.empty_like(wsc["page_table"])
+    d_sl = torch.empty_like(wsc["seq_lens"])
     ids = torch.empty((R, Hkv, k), dtype=torch.int32, device=dev)
     sc = torch.empty((R, Hkv, k), dtype=torch.float32, device=dev)
 
@@ -380,7 +380,7 @@ def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
         d_q.copy_(h_q, non_blocking=True)
         d_pt.copy_(h_pt, non_blocking=True)
         d_sl.copy_(h_sl, non_blocking=True)
-        msa.index_score_topk(d_q, c2["k_idx_pages"], d_pt, d_sl, 1, k, workspace=wsp, out=(ids, sc))
+        msa.index_score_topk(d_q, wsc["k_idx_pages"], d_pt, d_sl, 1, k, workspace=wsp, out=(ids, sc))
         h_ids.copy_(ids, non_blocking=True)
         h_sc.copy_(sc, non_blocking=True)
 
@@ -399,7 +399,7 @@ def e2e_score(msa, c2, wsp, dev, steps: int, ws: int):
     ms = max_over_ranks([s.elapsed_time(e) / steps], ws, dev)[0]
     h2d = h_q.numel() * 2 + h_pt.numel() * 4 + h_sl.numel() * 4
     d2h = h_ids.numel() * 4 + h_sc.numel() * 4
-    return {"value": round(job_throughput(c2["bytes"], ms, ws) / 1e9, 1), "unit": "GB/s",
+    return {"value": round(job_throughput(wsc["bytes"], ms, ws) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "note": "per-step inputs copied from pinned host memory; paged K-index resident"}
 
@@ -412,21 +412,21 @@ def _oracle_score_step(oracle, h):
     return ids
 
 
-def _host_cfg2(c2, rows):
+def _host_scoring(wsc, rows):
     import numpy as np
     u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    sl = c2["seq_lens"].cpu().numpy()
-    return {"q_idx": u16(c2["q_idx"]), "k_idx": u16(c2["k_idx_pages"]),
-            "pt": c2["page_table"].cpu().numpy(), "sl": sl, "topk": c2["topk"],
+    sl = wsc["seq_lens"].cpu().numpy()
+    return {"q_idx": u16(wsc["q_idx"]), "k_idx": u16(wsc["k_idx_pages"]),
+            "pt": wsc["page_table"].cpu().numpy(), "sl": sl, "topk": wsc["topk"],
             "q_pos": (sl.astype("int64") - 1), "rows": np.asarray(rows, dtype=np.int64)}
 
 
-def cpu_baseline(c2, seconds: float):
+def cpu_baseline(wsc, seconds: float):
     """The oracle as it stands, timed on this host's cores on the headline workload."""
     import oracle
-    B = c2["B"]
-    h = _host_cfg2(c2, list(range(B)))
-    per_row = c2["bytes"] / B
+    B = wsc["B"]
+    h = _host_scoring(wsc, list(range(B)))
+    per_row = wsc["bytes"] / B
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -441,7 +441,7 @@ def cpu_baseline(c2, seconds: float):
             "sample": f"{n} full passes of all {B} requests (scores + top-k) in {dt:.1f} s"}
 
 
-def run_cfg5(args, local):
+def run_long_context(args, local):
     """1M-token layer, reported per stage (not part of the headline step): 4 x 1,048,576-token
     decode (score + top-k, sparse page table, paged decode, k 32) and a 32768-token prefill chunk
     on a 1,048,576-token prefix (score + top-k over every chunk row, then sparse attention with
@@ -454,7 +454,7 @@ def run_cfg5(args, local):
     out = {}
     # --small (profiling captures only): one 131072-token request, an 8192-token chunk on a
     # 131072-token prefix
-    w = workloads.cfg5_decode(dev, seed=5, **(dict(B=1, seq_len=131072) if args.small else {}))
+    w = workloads.long_context_decode(dev, seed=5, **(dict(B=1, seq_len=131072) if args.small else {}))
     ws_ = msa.Workspace()
 
     def timed(fn, reps):
@@ -494,7 +494,7 @@ def run_cfg5(args, local):
                                "frac_hbm": round(kv_bytes / ms_d / 1e6 / pk["hbm_gbs"], 4)}
     del w, ids, fpt, lens
     torch.cuda.empty_cache()
-    w = workloads.cfg5_prefill(dev, seed=6, **(dict(T=8192, prefix=131072) if args.small else {}))
+    w = workloads.long_context_prefill(dev, seed=6, **(dict(T=8192, prefix=131072) if args.small else {}))
     T, S, P = w["T"], w["S"], w["P"]
     kidx_pages = w["k_idx"].view(P, 128, Hkv, Di)
     sl = torch.tensor([S], dtype=torch.int32, device=dev)
@@ -531,11 +531,11 @@ def run_reference(args, ws, rank, local):
     import oracle
     oracle.build()
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    c2 = workloads.cfg2(dev, seed=2)
-    B = c2["B"]
-    c2["bytes"] = int(c2["seq_lens"].to(torch.int64).sum().item()) * c2["Hkv"] * c2["Di"] * 2 \
-        + c2["q_idx"].numel() * 2 + c2["page_table"].numel() * 4 + B * c2["Hkv"] * c2["topk"] * 8
-    h = _host_cfg2(c2, list(range(B)))
+    wsc = workloads.decode_scoring(dev, seed=2)
+    B = wsc["B"]
+    wsc["bytes"] = int(wsc["seq_lens"].to(torch.int64).sum().item()) * wsc["Hkv"] * wsc["Di"] * 2 \
+        + wsc["q_idx"].numel() * 2 + wsc["page_table"].numel() * 4 + B * wsc["Hkv"] * wsc["topk"] * 8
+    h = _host_scoring(wsc, list(range(B)))
     for _ in range(args.warmup):
         _oracle_score_step(oracle, h)
     t0 = time.perf_counter()
@@ -543,7 +543,7 @@ def run_reference(args, ws, rank, local):
         _oracle_score_step(oracle, h)
     dt = time.perf_counter() - t0
     ms = dt / args.steps * 1e3
-    gbs = c2["bytes"] / (ms * 1e-3) / 1e9
+    gbs = wsc["bytes"] / (ms * 1e-3) / 1e9
     cores = min(os.cpu_count() or 1, B)
     line = {"metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "impl": "reference",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
@@ -568,7 +568,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--stages", default="score,decode,prefill",
                     help="comma list of stages to run (profiling captures)")
-    ap.add_argument("--cfg5", action="store_true",
+    ap.add_argument("--long-context", action="store_true",
                     help="also report the 1M-token layer's stages (takes about a minute)")
     ap.add_argument("--small", action="store_true",
                     help="smaller decode/prefill workloads (profiling captures only)")

@@ -33,9 +33,9 @@ def _sample(n_total: int, n: int, seed: int) -> np.ndarray:
     return np.sort(np.concatenate([pick, [0, n_total - 1]])).astype(np.int64)
 
 
-def test_cfg2_decode_scoring_full():
+def test_decode_scoring_8x60032_full():
     """8 requests x 60032 tokens, Hkv 8, Di 128, k 16: every row, every group."""
-    w = workloads.cfg2(DEV, seed=2)
+    w = workloads.decode_scoring(DEV, seed=2)
     ids, sc = msa.index_score_topk(w["q_idx"], w["k_idx_pages"], w["page_table"], w["seq_lens"], 1,
                                    w["topk"])
     torch.cuda.synchronize()
@@ -52,20 +52,20 @@ def test_cfg2_decode_scoring_full():
             assert set(planted[b, g].tolist()) <= set(ids_np[b, g].tolist())
 
 
-def test_cfg3_block_major_prefill_full():
+def test_causal_prefill_32768_full():
     """32768-token causal chunk, Hq 64, Hkv 8, D 128, k 16: sampled (query, head) units."""
-    w = workloads.cfg3(DEV, seed=3)
+    w = workloads.causal_prefill(DEV, seed=3)
     o, lse = msa.sparse_prefill(w["q"], w["k"], w["v"], w["block_ids"])
     torch.cuda.synchronize()
     units = _sample(w["T"] * w["Hq"], 1024, seed=30)
     ref = oracle.sparse_prefill(u16(w["q"]), u16(w["k"]), u16(w["v"]), w["block_ids"].cpu().numpy(),
                                 units=units)
-    check_attention(o, lse, ref, units=units, what="cfg3 prefill")
+    check_attention(o, lse, ref, units=units, what="causal_prefill prefill")
 
 
-def test_cfg4_paged_decode_full():
+def test_paged_decode_64_requests_full():
     """64 requests, context ~U[8K,128K], Hq 64, Hkv 8, D 128, k 16: all page tables, sampled heads."""
-    w = workloads.cfg4(DEV, seed=4)
+    w = workloads.paged_decode(DEV, seed=4)
     fpt, lens = msa.build_sparse_page_table(w["block_ids"], w["page_table"], w["seq_lens"], 1,
                                             w["num_pages"])
     o, lse = msa.paged_sparse_decode(w["q"], w["k_cache"], w["v_cache"], fpt, lens)
@@ -77,12 +77,12 @@ def test_cfg4_paged_decode_full():
     units = _sample(w["B"] * w["Hq"], 768, seed=40)
     ref = oracle.sparse_decode(u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"]), pt, sl, ids, 1,
                                units=units)
-    check_attention(o, lse, ref, units=units, what="cfg4 decode")
+    check_attention(o, lse, ref, units=units, what="paged_decode decode")
 
 
-def test_cfg5_decode_pipeline_1m():
+def test_long_context_decode_pipeline_1m():
     """4 requests x 1,048,576 tokens, k 32: score -> top-k -> sparse page table -> paged decode."""
-    w = workloads.cfg5_decode(DEV, seed=5)
+    w = workloads.long_context_decode(DEV, seed=5)
     ids, sc = msa.index_score_topk(w["q_idx"], w["k_idx_pages"], w["page_table"], w["seq_lens"], 1,
                                    w["topk"])
     fpt, lens = msa.build_sparse_page_table(ids, w["page_table"], w["seq_lens"], 1, w["num_pages"])
@@ -98,13 +98,13 @@ def test_cfg5_decode_pipeline_1m():
     assert np.array_equal(fpt.cpu().numpy(), fpt_ref)
     assert np.array_equal(lens.cpu().numpy(), lens_ref)
     ref = oracle.sparse_decode(u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"]), pt, sl, ids_np, 1)
-    check_attention(o, lse, ref, what="cfg5 decode")
+    check_attention(o, lse, ref, what="1M-token decode")
 
 
-def test_cfg5_prefill_chunk_on_1m_prefix():
+def test_long_context_prefill_chunk_on_1m_prefix():
     """32768-token chunk after a 1,048,576-token prefix, k 32: scoring of every row on the GPU
     (sampled rows against the oracle), then block-major attention on sampled units."""
-    w = workloads.cfg5_prefill(DEV, seed=6)
+    w = workloads.long_context_prefill(DEV, seed=6)
     T, S, Hkv, Di, P = w["T"], w["S"], w["Hkv"], w["Di"], w["P"]
     kidx_pages = w["k_idx"].view(P, 128, Hkv, Di)
     sl = torch.tensor([S], dtype=torch.int32, device=DEV)
@@ -124,4 +124,4 @@ def test_cfg5_prefill_chunk_on_1m_prefix():
     torch.cuda.synchronize()
     units = _sample(T * w["Hq"], 768, seed=51)
     ref = oracle.sparse_prefill(u16(w["q"]), u16(k), u16(v), ids_np, units=units)
-    check_attention(o, lse, ref, units=units, what="cfg5 prefill")
+    check_attention(o, lse, ref, units=units, what="prefill chunk on a 1M prefix")

@@ -166,7 +166,7 @@ def test_paged_sparse_decode_ranges_cross_rows():
 
 @pytest.mark.parametrize("T,S,Hq,Hkv,topk,n_shared", [
     (300, 700, 16, 2, 4, 2),        # chunk after a prefix, ragged
-    (1000, 1000, 64, 8, 16, 12),    # causal, cfg3 structure at small T
+    (1000, 1000, 64, 8, 16, 12),    # causal, causal_prefill structure at small T
     (200, 200, 8, 8, 3, 0),         # G 1
     (129, 5000, 32, 2, 8, 4),       # G 16, long prefix
     (257, 800, 8, 4, 5, 3),         # G 2: block-major only
@@ -322,7 +322,7 @@ def test_lse_merge(dtype):
 
 def test_pr1_layer_end_to_end():
     """PR1: 2048-token layer (Hq 8, Hkv 2, Di 64, k 4): prefill then 16 decode steps."""
-    w = workloads.cfg_pr1("cpu", seed=0)
+    w = workloads.tiny_layer("cpu", seed=0)
     T, Hq, Hkv, D, Di, k, P = w["T"], w["Hq"], w["Hkv"], w["D"], w["Di"], w["topk"], w["P"]
     kidx = w["k_idx"].view(P, 128, Hkv, Di)
     kc, vc = w["k"].view(P, 128, Hkv, D), w["v"].view(P, 128, Hkv, D)

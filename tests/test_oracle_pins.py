@@ -126,7 +126,7 @@ def test_block_scores_bruteforce(seq_lens, N, Hkv, Di):
 
 
 def test_planted_blocks_are_selected():
-    # cfg2 structure at reduced size: planted blocks gain ~2|q|^2 ~ 256 over noise ~ 11
+    # decode_scoring structure at reduced size: planted blocks gain ~2|q|^2 ~ 256 over noise ~ 11
     w = workloads.index_workload([60 * 128, 50 * 128 + 17], 1, 2, 128, seed=5, device="cpu",
                                  n_planted=8)
     sl = w["seq_lens"].numpy()

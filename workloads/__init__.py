@@ -9,15 +9,15 @@ Every generator takes a ``seed`` and a torch ``device``. The stream of numbers d
 the device (torch's CPU and CUDA generators differ), so a test draws the inputs once and
 copies them to the other side; nothing compares two draws made on different devices.
 
-Workload recipes (sizes in the docstrings of each ``cfg_*`` function):
-  * pr1   tiny layer: 1 sequence of 2048 tokens, Hq=8, Hkv=2, D=128, Di=64, k=4, causal
+Workload recipes (sizes in the docstrings of the named workloads below):
+  * tiny_layer: 1 sequence of 2048 tokens, Hq=8, Hkv=2, D=128, Di=64, k=4, causal
           prefill then 16 decode steps, contiguous pages (identity page table).
-  * cfg2  decode index scoring: B=8 x 60032 tokens, Hkv=8, Di=128, k=16, 8 planted
+  * decode_scoring: B=8 x 60032 tokens, Hkv=8, Di=128, k=16, 8 planted
           high-affinity blocks per (request, group), random page permutation.
-  * cfg3  block-major sparse prefill: T=32768 causal, Hq=64, Hkv=8, D=128, k=16 with
+  * causal_prefill (block-major sparse prefill): T=32768 causal, Hq=64, Hkv=8, D=128, k=16 with
           clustered selections (~75% of the queries of a 128-query span share 12 blocks).
-  * cfg4  paged sparse decode: B=64, context ~U[8K,128K], Hq=64, Hkv=8, D=128, k=16.
-  * cfg5  1M-token layer: 4 decode requests at 1,048,576 tokens (k=32) and a 32768-token
+  * paged_decode: B=64, context ~U[8K,128K], Hq=64, Hkv=8, D=128, k=16.
+  * long_context_decode / long_context_prefill (1M-token layer): 4 decode requests at 1,048,576 tokens (k=32) and a 32768-token
           prefill chunk after a 1,048,576-token prefix (k=32).
 """
 from __future__ import annotations
@@ -237,51 +237,51 @@ def layer_workload(T: int, Hq: int, Hkv: int, D: int, Di: int, seed: int, device
 
 # ----------------------------------------------------------------------------- named configs
 
-def cfg_pr1(device, seed: int = 0):
+def tiny_layer(device, seed: int = 0):
     """Tiny layer: 2048 tokens (16 blocks), Hq=8, Hkv=2, D=128, Di=64, k=4, 16 decode steps."""
     w = layer_workload(2048, 8, 2, 128, 64, seed, device, decode_steps=16)
     w["topk"] = 4
     return w
 
 
-CFG2 = dict(B=8, seq_len=60032, Hkv=8, Di=128, topk=16, n_planted=8)
+DECODE_SCORING = dict(B=8, seq_len=60032, Hkv=8, Di=128, topk=16, n_planted=8)
 
 
-def cfg2(device, seed: int = 2, B: int | None = None, seq_len: int | None = None):
+def decode_scoring(device, seed: int = 2, B: int | None = None, seq_len: int | None = None):
     """Decode index scoring: 8 requests x 60032 tokens (469 blocks), Hkv=8, Di=128, k=16."""
-    B = B or CFG2["B"]
-    seq_len = seq_len or CFG2["seq_len"]
-    w = index_workload([seq_len] * B, 1, CFG2["Hkv"], CFG2["Di"], seed, device,
-                       n_planted=CFG2["n_planted"])
-    w["topk"] = CFG2["topk"]
+    B = B or DECODE_SCORING["B"]
+    seq_len = seq_len or DECODE_SCORING["seq_len"]
+    w = index_workload([seq_len] * B, 1, DECODE_SCORING["Hkv"], DECODE_SCORING["Di"], seed, device,
+                       n_planted=DECODE_SCORING["n_planted"])
+    w["topk"] = DECODE_SCORING["topk"]
     return w
 
 
-CFG3 = dict(T=32768, Hq=64, Hkv=8, D=128, topk=16)
+CAUSAL_PREFILL = dict(T=32768, Hq=64, Hkv=8, D=128, topk=16)
 
 
-def cfg3(device, seed: int = 3, T: int | None = None):
+def causal_prefill(device, seed: int = 3, T: int | None = None):
     """Block-major sparse prefill: 32768-token causal chunk, Hq=64, Hkv=8, D=128, k=16."""
-    T = T or CFG3["T"]
-    return prefill_workload(T, T, CFG3["Hq"], CFG3["Hkv"], CFG3["D"], CFG3["topk"], seed, device)
+    T = T or CAUSAL_PREFILL["T"]
+    return prefill_workload(T, T, CAUSAL_PREFILL["Hq"], CAUSAL_PREFILL["Hkv"], CAUSAL_PREFILL["D"], CAUSAL_PREFILL["topk"], seed, device)
 
 
-CFG4 = dict(B=64, lo=8192, hi=131072, Hq=64, Hkv=8, D=128, topk=16)
+PAGED_DECODE = dict(B=64, lo=8192, hi=131072, Hq=64, Hkv=8, D=128, topk=16)
 
 
-def cfg4_seq_lens(seed: int, B: int, lo: int, hi: int):
+def paged_decode_seq_lens(seed: int, B: int, lo: int, hi: int):
     g = _gen(seed, "cpu")
     return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
 
 
-def cfg4(device, seed: int = 4, B: int | None = None):
+def paged_decode(device, seed: int = 4, B: int | None = None):
     """Paged sparse decode: 64 requests, context ~U[8192, 131072], Hq=64, Hkv=8, D=128, k=16."""
-    B = B or CFG4["B"]
-    lens = cfg4_seq_lens(seed, B, CFG4["lo"], CFG4["hi"])
-    return decode_workload(lens, 1, CFG4["Hq"], CFG4["Hkv"], CFG4["D"], CFG4["topk"], seed, device)
+    B = B or PAGED_DECODE["B"]
+    lens = paged_decode_seq_lens(seed, B, PAGED_DECODE["lo"], PAGED_DECODE["hi"])
+    return decode_workload(lens, 1, PAGED_DECODE["Hq"], PAGED_DECODE["Hkv"], PAGED_DECODE["D"], PAGED_DECODE["topk"], seed, device)
 
 
-CFG5 = dict(B=4, seq_len=1 << 20, Hq=64, Hkv=8, D=128, Di=128, topk=32, T_prefill=32768)
+LONG_CONTEXT = dict(B=4, seq_len=1 << 20, Hq=64, Hkv=8, D=128, Di=128, topk=32, T_prefill=32768)
 
 
 def paged_layer_workload(seq_lens, Hq: int, Hkv: int, D: int, Di: int, seed: int, device,
@@ -321,18 +321,18 @@ def chunk_prefill_workload(prefix: int, T: int, Hq: int, Hkv: int, D: int, Di: i
             "page_table": torch.arange(P, dtype=torch.int32, device=device)[None, :]}
 
 
-def cfg5_decode(device, seed: int = 5, B: int | None = None, seq_len: int | None = None):
+def long_context_decode(device, seed: int = 5, B: int | None = None, seq_len: int | None = None):
     """1M-token decode: 4 requests x 1,048,576 tokens, Hq 64, Hkv 8, D 128, Di 128, k 32."""
-    c = CFG5
+    c = LONG_CONTEXT
     w = paged_layer_workload([seq_len or c["seq_len"]] * (B or c["B"]), c["Hq"], c["Hkv"], c["D"],
                              c["Di"], seed, device)
     w["topk"] = c["topk"]
     return w
 
 
-def cfg5_prefill(device, seed: int = 6, T: int | None = None, prefix: int | None = None):
+def long_context_prefill(device, seed: int = 6, T: int | None = None, prefix: int | None = None):
     """32768-token prefill chunk after a 1,048,576-token prefix, Hq 64, Hkv 8, D 128, Di 128, k 32."""
-    c = CFG5
+    c = LONG_CONTEXT
     w = chunk_prefill_workload(prefix if prefix is not None else c["seq_len"], T or c["T_prefill"],
                                c["Hq"], c["Hkv"], c["D"], c["Di"], seed, device)
     w["topk"] = c["topk"]
