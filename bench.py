@@ -305,15 +305,18 @@ def run_ours(args, ws, rank, local):
                 "traffic": recorded_traffic("score_decode_kernel", h_score),
                 "algorithmic_bytes": wsc["bytes"], "peak_source": pk["source"]}
     stages = {
-        "index_score_topk": {"config": "8 x 60032 tokens, Hkv 8, Di 128, k 16", "ms": round(score_ms, 4),
+        "index_score_topk": {"config": f"{wsc['B']} x {wsc['max_seq_len']} tokens, Hkv {wsc['Hkv']}, "
+                                       f"Di {wsc['Di']}, k {wsc['topk']}", "ms": round(score_ms, 4),
                              "GB/s": round(score_gbs, 1), "frac_hbm": round(score_gbs / pk["hbm_gbs"], 4),
                              "bytes": wsc["bytes"]},
-        "sparse_decode": {"config": "64 req, ctx U[8K,128K], Hq 64, Hkv 8, D 128, k 16",
+        "sparse_decode": {"config": f"{wdc['B']} req, ctx U[8K,128K], Hq {wdc['Hq']}, Hkv {wdc['Hkv']}, "
+                                    f"D {wdc['D']}, k {wdc['topk']}",
                           "ms_page_table": round(pt_ms, 4), "ms_decode": round(dec_ms, 4),
                           "GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
                           "bytes": wdc["bytes"], "kv_bytes": wdc["kv_bytes"],
                           "traffic": recorded_traffic("paged_decode_kernel", src_hash("decode.cu"))},
-        "sparse_prefill": {"config": "T 32768 causal, Hq 64, Hkv 8, D 128, k 16", "ms": round(pre_ms, 4),
+        "sparse_prefill": {"config": f"T {wpf['T']} causal, Hq {wpf['Hq']}, Hkv {wpf['Hkv']}, D {wpf['D']}, "
+                                     f"k {wpf['topk']}", "ms": round(pre_ms, 4),
                            "TFLOP/s": round(pre_tflops, 1),
                            "frac_bf16": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
                            "kernels": "query-major selection + attention for blocks shared by a "
@@ -340,16 +343,19 @@ def run_ours(args, ws, rank, local):
                                "block-major sparse prefill (32768 tokens)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
-        # kernels of this library per step: scorer (1); page table, decode, merge (3); dense
-        # selection, bucket count, two scans, scatter, tile descriptors, block-major attention,
-        # query-major attention, merge (9). Memsets not counted.
+        # kernels of this library per step: scorer (1); page table, decode, merge (3); query
+        # ordering, dense selection, bucket count, two scans, scatter, tile descriptors,
+        # block-major attention, query-major attention, merge (10). Memsets not counted.
         "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
-                                      + ("prefill" in run) * 9),
+                                      + ("prefill" in run) * 10),
         "clocks": clk.summary(), "device_error_word": err,
     }
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
         if key not in run:
             stages[name] = None
+    if "score" not in run:  # the headline is the scorer's: nothing to report without it
+        line["value"] = None
+        line["roofline"] = None
     if args.long_context:
         line["long_context"] = run_long_context(args, local)
     if args.small or run != {"score", "decode", "prefill"}:

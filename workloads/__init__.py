@@ -155,6 +155,7 @@ def index_workload(seq_lens, N: int, Hkv: int, Di: int, seed: int, device,
         "q_idx": q_idx, "k_idx_pages": k_idx, "page_table": page_table,
         "seq_lens": torch.tensor([int(s) for s in seq_lens], dtype=torch.int32, device=device),
         "num_pages": num_pages, "B": B, "N": N, "Hkv": Hkv, "Di": Di, "planted": planted,
+        "max_seq_len": max(int(s) for s in seq_lens),
     }
 
 
