@@ -6,8 +6,9 @@ HBM (all larger than the 129 MB L2, so no flush is needed between steps):
                             (8 planted high-affinity blocks per request and group)
   * sparse page table + paged sparse decode: 64 requests, context ~U[8K, 128K], Hq 64,
                             Hkv 8, D 128, k 16 (KV groups flattened into 512 rows)
-  * block-major sparse prefill (bucketing, attention partials, LSE merge): 32768-token
-                            causal chunk, Hq 64, Hkv 8, D 128, k 16, clustered selections
+  * sparse prefill (query ordering and shared-block selection, bucketing, query-major and
+                            block-major attention partials, LSE merge): 32768-token causal
+                            chunk, Hq 64, Hkv 8, D 128, k 16, clustered selections
 The headline `value` is the index-score + top-k HBM throughput (GB/s of K-index scanned);
 `stages` carries every stage's throughput and roofline fraction.
 
