@@ -34,21 +34,18 @@ namespace msa {
 namespace {
 
 // ------------------------------------------------------------------------------ bucketing
-__device__ __forceinline__ int64_t list_of(int64_t idx, int32_t Hkv, int32_t topk, int32_t nblk,
-                                           int32_t win, int32_t nwin, int32_t j) {
-  const int64_t t = idx / ((int64_t)topk * Hkv);
-  const int g = (int)((idx / topk) % Hkv);
-  return ((int64_t)g * nwin + t / win) * nblk + j;
-}
+// Rows are (query, group) pairs, row = t*Hkv + g; the host checks that T*Hkv*topk fits in
+// int32, so row and entry arithmetic is 32-bit. List indices ((g*nwin + t/win)*nblk + j) stay
+// 64-bit.
 
 // One thread per (query, group) row: counts every valid selection into its list.
-__global__ void bucket_count_kernel(const int32_t* __restrict__ block_ids, int64_t rows,
+__global__ void bucket_count_kernel(const int32_t* __restrict__ block_ids, int32_t rows,
                                     int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
                                     int32_t nwin, int32_t* __restrict__ counts) {
-  for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < rows;
-       row += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = row / Hkv;
-    const int g = (int)(row % Hkv);
+  for (int32_t row = blockIdx.x * blockDim.x + threadIdx.x; row < rows;
+       row += gridDim.x * blockDim.x) {
+    const int32_t t = row / Hkv;
+    const int32_t g = row - t * Hkv;
     const int64_t list0 = ((int64_t)g * nwin + t / win) * nblk;
     for (int s = 0; s < topk; ++s) {
       const int32_t j = block_ids[row * topk + s];
@@ -149,21 +146,26 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-__global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int64_t n,
+// One thread per (query, group) row: places each valid selection (t, slot) at its list's next
+// free entry.
+__global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int32_t rows,
                                       int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
                                       int32_t nwin, const int32_t* __restrict__ offsets,
                                       const int32_t* __restrict__ group_base,
                                       int32_t* __restrict__ cursor, int32_t* __restrict__ entries) {
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t j = block_ids[idx];
-    if (j < 0 || j >= nblk) continue;
-    const int64_t t = idx / ((int64_t)topk * Hkv);
-    const int slot = (int)(idx % topk);
-    const int64_t list = list_of(idx, Hkv, topk, nblk, win, nwin, j);
-    const int64_t seg = list / nblk;  // (group, window) segment
-    const int pos = group_base[seg] + offsets[seg * (nblk + 1) + j] + atomicAdd(&cursor[list], 1);
-    entries[pos] = (int32_t)(t * topk + slot);
+  for (int32_t row = blockIdx.x * blockDim.x + threadIdx.x; row < rows;
+       row += gridDim.x * blockDim.x) {
+    const int32_t t = row / Hkv;
+    const int32_t g = row - t * Hkv;
+    const int64_t seg = (int64_t)g * nwin + t / win;  // (group, window) segment
+    const int32_t base = group_base[seg];
+    const int32_t* off = offsets + seg * (nblk + 1);
+    int32_t* cur = cursor + seg * nblk;
+    for (int s = 0; s < topk; ++s) {
+      const int32_t j = block_ids[(int64_t)row * topk + s];
+      if (j < 0 || j >= nblk) continue;
+      entries[base + off[j] + atomicAdd(&cur[j], 1)] = t * topk + s;
+    }
   }
 }
 
@@ -618,9 +620,7 @@ cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int3
   const int32_t nseg = Hkv * nwin;  // (group, window) segments
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)nseg * nblk, stream);
   if (e != cudaSuccess) return e;
-  const int64_t n = (int64_t)T * Hkv * topk;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8));
-  const int64_t rows = (int64_t)T * Hkv;
+  const int32_t rows = T * Hkv;  // T*Hkv*topk fits in int32 (checked by the callers)
   const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)sm_count() * 8));
   bucket_count_kernel<<<rgrid, 256, 0, stream>>>(block_ids, rows, Hkv, topk, nblk, win, nwin,
                                                  counts);
@@ -631,8 +631,8 @@ cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int3
   bucket_scan_kernel<<<nseg, 1024, 0, stream>>>(counts, nblk, qpt, offsets, tile_local);
   bucket_seg_scan_kernel<<<1, 1024, 0, stream>>>(offsets, tile_local, nseg, nblk, group_base,
                                                  seg_tile_base);
-  bucket_scatter_kernel<<<grid, 256, 0, stream>>>(block_ids, n, Hkv, topk, nblk, win, nwin, offsets,
-                                                  group_base, counts, entries);
+  bucket_scatter_kernel<<<rgrid, 256, 0, stream>>>(block_ids, rows, Hkv, topk, nblk, win, nwin,
+                                                   offsets, group_base, counts, entries);
   return cudaGetLastError();
 }
 
