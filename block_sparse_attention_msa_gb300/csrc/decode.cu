@@ -348,7 +348,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.num_pages = a.num_pages;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  if (a.nsplit != a.topk) return cudaErrorInvalidValue;  // one slot per selected page
+  if (a.nslots != a.topk) return cudaErrorInvalidValue;  // one slot per selected page
   const size_t smem = 1024 + (size_t)kWarps * kStages * kStep;
   cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -358,7 +358,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   paged_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_lse_merge(a.part_o, false, a.part_lse, nullptr, p.rows, a.nsplit, p.G, a.D,
+  return launch_lse_merge(a.part_o, false, a.part_lse, nullptr, p.rows, a.nslots, p.G, a.D,
                           a.o, a.lse, stream);
 }
 }  // namespace msa

@@ -48,9 +48,9 @@ struct DecodeArgs {
   int64_t num_pages;
   uint16_t* o;                 // [R, Hq, D]
   float* lse;                  // [R, Hq] or null
-  float* part_o;               // workspace [R*Hkv, nsplit, G, D]
-  float* part_lse;             // workspace [R*Hkv, nsplit, G]
-  int32_t nsplit;              // partial slots per flattened row: decode_slots(topk)
+  float* part_o;               // workspace [R*Hkv, nslots, G, D]
+  float* part_lse;             // workspace [R*Hkv, nslots, G]
+  int32_t nslots;              // partial slots per flattened row: decode_slots(topk)
 };
 // One partial slot per selected page: a warp whose unit range starts a row segment at page i
 // writes slot i.

@@ -242,8 +242,8 @@ int msa_paged_sparse_decode(const uint16_t* q, const uint16_t* k_cache, const ui
   a.num_pages = num_pages;
   a.o = o;
   a.lse = lse;
-  a.nsplit = msa::decode_slots(topk);
-  const size_t units = (size_t)R * Hq * a.nsplit;
+  a.nslots = msa::decode_slots(topk);
+  const size_t units = (size_t)R * Hq * a.nslots;
   a.part_o = reinterpret_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         msa::ws_align(units * 128 * sizeof(float)));
