@@ -226,11 +226,11 @@ MSA_API int msa_paged_sparse_decode(const uint16_t* q, const uint16_t* k_cache, 
  * (-1 entries ignored). Steps, all on the GPU: (a) invert the selections into per-(group,
  * block) query lists, (b) block-major attention writing one partial (O, lse) per
  * (query, group, slot), (c) merge the partials of each (query, head). With G = Hq/Hkv of 8
- * or 16, the queries of each 128-query span are first ranked by how many of their blocks
- * the span shares, and consecutive ranks form pairs of 128/G-query tiles; the blocks that at
- * least half of a pair chose are taken out and computed query-major (one partial per
- * (query, head) for all of them); (a)-(b) run on the remaining selections and (c) merges
- * both. Every selection is computed exactly once.
+ * or 16, the queries of each 128-query span are first ranked by how many of their blocks at
+ * least half of the span chose, and consecutive ranks form pairs of 128/G-query tiles; the
+ * blocks that at least half of a pair chose are taken out and computed query-major (one
+ * partial per (query, head) for all of them); (a)-(b) run on the remaining selections and
+ * (c) merges both. Every selection is computed exactly once.
  *
  *   q     [T, Hq, D] bf16; k, v [S_kv, Hkv, D] bf16 (contiguous K/V of the sequence)
  *   block_ids [T, Hkv, topk] int32, each id -1 or a causal block of its query
