@@ -73,3 +73,22 @@ def test_one_rank_is_the_identity():
     import bench
     assert bench.max_over_ranks([3, 4.5], 1, torch.device("cpu")) == [3.0, 4.5]
     assert bench.job_throughput(10.0, 5.0, 1) == 2000.0
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` on one rank: the oracle timed on the host cores, one JSON
+    line with the keys the benchmark contract asks of the reference arm."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
