@@ -33,9 +33,13 @@
  *  - Return value: MSA_OK (0) or a negative MSA_ERR_* code. Argument checks run on the host
  *    before anything is queued; on error nothing is queued and msa_last_error() returns a
  *    thread-local message. A CUDA launch failure returns MSA_ERR_CUDA.
- *  - Device-side checks: page ids and block ids read from device tables are range-checked
- *    inside the kernels; an out-of-range id is skipped (never dereferenced) and recorded
- *    in a device error word that msa_device_error() reads back (that call synchronises).
+ *  - Device-side checks: page ids, block ids and sequence lengths read from device tables
+ *    are range-checked inside the kernels before any address is formed from them. A bad
+ *    value is never dereferenced: a page id out of range is read as page 0 (page 0, group
+ *    0 for a virtual page of the strided view), a sequence length above max_blocks*128 is
+ *    clamped to it, and a sparse page-table entry whose block or page is invalid becomes
+ *    -1. Each case sets a bit of a device error word that msa_device_error() reads back
+ *    (that call synchronises).
  *
  * Supported values: D = 128; Di in {64, 128}; G in {1, 2, 4, 8, 16} with Hkv*G = Hq;
  * Hkv in {1, 2, 4, 8, 16}; 2 <= topk <= 64.
@@ -323,8 +327,11 @@ MSA_API int msa_lse_merge(const void* o_parts, int32_t parts_bf16, const float* 
  *  - Limit: the call needs msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks)
  *    <= MSA_NOALLOC_SCRATCH_BYTES, i.e. about B*N*Hkv*max_blocks <= 2 million block
  *    scores. Larger calls return MSA_ERR_UNSUPPORTED before anything is queued.
- *  - First call on a device: it looks up the array's device address (cudaGetSymbolAddress)
- *    with that device current and caches it. Make that first call on each device before
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it; every later call whose
+ *    stream is not being captured looks it up again, so that a device reset (which unloads
+ *    the module; the array may move when it is loaded again) leaves no stale address behind.
+ *    Make the first call on each device, and the first call after a device reset, before
  *    any stream capture begins.
  *  - Sharing: every call on a device uses the same array, which keeps the previous call's
  *    contents. Each call clears the counters it needs at zero (an asynchronous memset on

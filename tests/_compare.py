@@ -46,6 +46,19 @@ def check_selection(ids_gpu: np.ndarray, ids_ref: np.ndarray, scores_ref: np.nda
     Returns the number of (row, group) lists that differ only by near-tie swaps.
     """
     assert ids_gpu.shape == ids_ref.shape
+    # The sink block 0 and the query's local block are always kept. The local block is the
+    # last block with a finite oracle score: blocks past the query's position score -inf, and
+    # the local block holds at least the query's own token. A dropped forced block must fail
+    # here, before the near-tie rule below could excuse it.
+    fin = np.isfinite(scores_ref)
+    R, H = ids_gpu.shape[:2]
+    local = fin.shape[2] - 1 - np.argmax(fin[:, :, ::-1], axis=2)      # [R, Hkv]
+    has_any = fin.any(axis=2)
+    for forced, what in ((np.zeros((R, H), dtype=np.int64), "sink block 0"), (local, "local block")):
+        kept = (ids_gpu == forced[:, :, None]).any(axis=2)
+        bad = np.nonzero(has_any & ~kept)
+        assert bad[0].size == 0, (
+            f"{what} missing in row {bad[0][0]} group {bad[1][0]}: {ids_gpu[bad[0][0], bad[1][0]]}")
     swaps = 0
     diff = np.nonzero((ids_gpu != ids_ref).any(axis=2))
     for r, g in zip(*diff):

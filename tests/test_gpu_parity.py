@@ -263,7 +263,8 @@ def test_sparse_prefill_paged_equals_contiguous(T, prefix, Hq, Hkv, topk, n_shar
 def test_staged_kv_decode_equals_decode_on_the_full_cache(host):
     """Selected blocks' K/V copied from the paged caches (pinned host memory or device) to a
     staging cache: the paged decode on it equals the decode on the full caches bit for bit (the
-    same values in the same order, and the decode's sums do not depend on warp timing)."""
+    same values in the same order, and the decode's sums do not depend on warp timing), and
+    the oracle's sparse decode within the attention tolerances."""
     w = workloads.decode_workload([517, 1500, 129, 9000], 2, 32, 8, 128, 7, seed=9, device="cpu")
     kc = w["k_cache"].pin_memory() if host else w["k_cache"].to(DEV)
     vc = w["v_cache"].pin_memory() if host else w["v_cache"].to(DEV)
@@ -277,6 +278,10 @@ def test_staged_kv_decode_equals_decode_on_the_full_cache(host):
     assert torch.equal(lse_s, lse_f)
     assert torch.equal(o_s, o_f)
     assert torch.equal(spt < 0, fpt < 0)
+    # and both equal the oracle's sparse decode on the same inputs
+    ref = oracle.sparse_decode(u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"]), w["page_table"].numpy(),
+                               w["seq_lens"].numpy(), w["block_ids"].numpy(), 2)
+    check_attention(o_s, lse_s, ref, what=f"staged decode (host={host})")
     assert msa.device_error() == 0
 
 
