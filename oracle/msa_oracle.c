@@ -138,13 +138,17 @@ typedef struct {
   float* scores;
 } score_ctx;
 
-static void score_row(void* p, int64_t slot) {
+/* One work item = one (listed row, group): item = slot*Hkv + g, so that a few long rows
+ * (decode: one row per request) still spread over every host thread. */
+static void score_row(void* p, int64_t item) {
   score_ctx* c = (score_ctx*)p;
+  int64_t slot = item / c->Hkv;
+  int g = (int)(item % c->Hkv);
   int64_t r = c->rows ? c->rows[slot] : slot;
   int64_t b = r / c->N;
   int64_t i = r % c->N;
   int64_t q_pos = (int64_t)c->seq_lens[b] - c->N + i;
-  for (int g = 0; g < c->Hkv; ++g) {
+  {
     const uint16_t* q = c->q_idx + (r * c->Hkv + g) * c->Di;
     float* out = c->scores + (slot * c->Hkv + g) * c->max_blocks;
     for (int j = 0; j < c->max_blocks; ++j) {
@@ -173,7 +177,7 @@ int oracle_block_scores(const uint16_t* q_idx, const uint16_t* k_idx_pages,
   if (B <= 0 || N <= 0 || Hkv <= 0 || Di <= 0 || max_blocks <= 0) return -1;
   if (!rows) nrows = (int64_t)B * N;
   score_ctx c = {q_idx, k_idx_pages, page_table, seq_lens, N, Hkv, Di, max_blocks, rows, scores};
-  parallel_rows(nrows, nthreads, score_row, &c);
+  parallel_rows(nrows * Hkv, nthreads, score_row, &c);
   return 0;
 }
 
