@@ -203,7 +203,10 @@ constexpr int kRegsHigh = 208;
 constexpr uint32_t kOffQ = 0;                    // Q_A, Q_B
 constexpr uint32_t kOffKV = 2 * kTileBytes;      // {K, V}[2]
 constexpr uint32_t kOffBar = 6 * kTileBytes;
-constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+// blocks of the CTA's pair in each round (0: no pair or no shared block), one byte per round
+constexpr int kMaxRounds = 8192;
+constexpr uint32_t kOffCnt = kOffBar + 256;
+constexpr size_t kSmemBytes = 1024 + kOffCnt + kMaxRounds;
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -221,6 +224,7 @@ struct DenseKParams {
   const uint32_t* dmask;
   int32_t T, Hkv, G, qpt, ppg, q_atoms;
   int64_t npairs, q_start;
+  int64_t pair0;              // first pair of this launch (launches cover kMaxRounds rounds)
   const int32_t* page_table;  // null: contiguous K/V; else the page of each block
   int64_t num_pages;
   uint16_t* part_o;   // chunk-major [16][part_rows][8] bf16
@@ -240,8 +244,8 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
 // CTA's place in it moves by one each round: pairs are ordered by span and the ordered spans
 // put light pairs (few shared blocks) at fixed positions, which a fixed place would hand to
 // the same CTAs every round.
-__device__ __forceinline__ int64_t cta_pair(int64_t r, int64_t npairs) {
-  const int64_t pr = r * gridDim.x + (blockIdx.x + r) % gridDim.x;
+__device__ __forceinline__ int64_t cta_pair(int64_t r, int64_t pair0, int64_t npairs) {
+  const int64_t pr = pair0 + r * gridDim.x + (blockIdx.x + r) % gridDim.x;
   return pr < npairs ? pr : -1;
 }
 
@@ -276,13 +280,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  {
+    const int nr = (int)min((int64_t)kMaxRounds, (p.npairs - p.pair0 + gridDim.x - 1) / gridDim.x);
+    for (int r = tid; r < nr; r += kThreads) {
+      const int64_t pr = cta_pair(r, p.pair0, p.npairs);
+      const int c = pr < 0 ? 0 : p.dcnt[pr];
+      smem[kOffCnt + r] = (uint8_t)(c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c));
+    }
+  }
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
   const uint32_t tmem = B.tmem_base;
   const uint32_t sbase = smem_u32(smem);
   const int G = p.G, qpt = p.qpt;
-  const int64_t rounds = (p.npairs + gridDim.x - 1) / gridDim.x;
+  const int rounds = (int)min((int64_t)kMaxRounds, (p.npairs - p.pair0 + gridDim.x - 1) / gridDim.x);
+  uint8_t* rcnt = smem + kOffCnt;  // blocks of this CTA's pair of round r
 
   static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
   if (warp < 4) {
@@ -296,15 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&vmap);
       }
       int pairs_done = 0, kv_loads = 0;
-      for (int64_t r = 0; r < rounds && !*fail; ++r) {
-        const int64_t pr = cta_pair(r, p.npairs);
-        if (pr < 0) continue;
-        const int L = p.dcnt[pr];
-        if (L <= 0) continue;
+      for (int r = 0; r < rounds && !*fail; ++r) {
+        const int L = rcnt[r];
+        if (L == 0) continue;
+        const int64_t pr = cta_pair(r, p.pair0, p.npairs);
         const int g = (int)(pr / p.ppg);
         const int64_t t0 = (pr % p.ppg) * 2 * qpt;  // first pair slot
         const int64_t tq = lane < 2 * qpt ? slot_query(p.qperm, p.npos, g, t0 + lane, p.T) : -1;
         const int nvalid = __popc(__ballot_sync(0xffffffffu, tq >= 0));
+        // the pair's block ids, one per lane (read before any wait)
+        const int32_t blk_l = lane < L ? p.dblk[pr * kMaxDense + lane] : 0;
+        const int32_t blk_h = lane + 32 < L ? p.dblk[pr * kMaxDense + lane + 32] : 0;
         if (pairs_done > 0 && !wait_or_fail(&B.q_empty, (pairs_done - 1) & 1, fail)) break;
         if (lane == 0) mbar_expect_tx(&B.q_full, (uint32_t)(nvalid * G * 256));
         __syncwarp();
@@ -321,12 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < L; ++j) {
           const int c = kv_loads & 1;
+          const int32_t blk = __shfl_sync(0xffffffffu, j < 32 ? blk_l : blk_h, j & 31);
           if (lane == 0) {
             // load kv_loads goes to buffer kv_loads & 1, free once both O MMAs of load
             // kv_loads - 2 have completed
             if (kv_loads < 2 || wait_or_fail(&B.kv_empty[c], ((kv_loads - 2) >> 1) & 1, fail)) {
               bool bad = false;
-              const int tok = kv_block_row(p.page_table, p.num_pages, p.dblk[pr * kMaxDense + j], bad);
+              const int tok = kv_block_row(p.page_table, p.num_pages, blk, bad);
               if (bad) msa_record_error(kErrBadPage);
               uint8_t* kvb = smem + kOffKV + c * 2 * kTileBytes;
               mbar_expect_tx(&B.kv_full[c], 4 * kBox);
@@ -345,102 +361,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ============================================================== MMA issuer
       // Per warpgroup X (tile A = 0, B = 1) and block n of the CTA's block sequence:
-      //   S_X(n) needs K/V(n), the pair's queries and O_X(n-1) complete (P_X(n-1) lives in
-      //   S_X's columns); O_X(n) needs P_X(n) and, on a pair's first block, the epilogue of
-      //   the previous pair done with O_X. K/V buffer n%2 is released after both O(n), the
-      //   query tiles after both S of a pair's last block.
-      if (lane == 0) {
+      //   O_X(n) needs P_X(n) and, on a pair's first block, the epilogue of the previous pair
+      //   done with O_X; S_X(n+1) needs K/V(n+1), the pair's queries and O_X(n) issued.
+      //   S_X(n+1) overwrites the tensor memory from which O_X(n) reads P_X(n): it is issued
+      //   after O_X(n) from this one warp, and the tensor pipe runs the MMAs of one thread in
+      //   issue order, so O_X(n) has read P_X(n) before S_X(n+1) writes there (the results are
+      //   checked against the oracle); the commit that signals S_X(n+1) also covers O_X(n), so
+      //   a softmax that sees S_X(n+1) may rescale O_X. K/V buffer n%2 is released after both
+      //   O(n), the query tiles after both S of a pair's last block. A ready O goes first.
+      // The whole warp runs this loop in lockstep (barrier states agreed by a vote) and one
+      // elected lane issues each MMA and commit. The tensor pipe takes one group at a time,
+      // holding the warp inside an MMA issue until it has room, so the decision between two
+      // issues must be short: pair boundaries come from the per-round block counts in shared
+      // memory and every other piece of state lives in registers.
+      {
         const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);
         const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);
-        // the CTA's block sequence: total count, and the pair boundaries as they come
+        const uint32_t qhalf = p.q_atoms ? 1024 : kBox;
+        const uint32_t qsbo = p.q_atoms ? 2048 : 1024;
         int total = 0;
-        for (int64_t r = 0; r < rounds; ++r) {
-          const int64_t pr = cta_pair(r, p.npairs);
-          if (pr >= 0) total += max(p.dcnt[pr], 0);
-        }
-        int sN[2] = {0, 0}, oN[2] = {0, 0};
-        // per X: pair index and first/last block index of the pair that block sN[X] / oN[X]
-        // belongs to (advanced lazily)
-        int64_t s_rd[2] = {0, 0}, o_rd[2] = {0, 0};  // rounds of the pairs of blocks sN / oN
-        int s_end[2] = {0, 0}, s_pairs[2] = {-1, -1};
-        int o_first[2] = {0, 0}, o_end[2] = {0, 0}, o_pairs[2] = {-1, -1};
+        for (int r = 0; r < rounds; ++r) total += rcnt[r];
+        // per X: blocks issued, blocks left in the current pair, pair ordinal, round cursor
+        int sN[2] = {0, 0}, s_left[2] = {0, 0}, s_pi[2] = {-1, -1}, s_r[2] = {-1, -1};
+        int oN[2] = {0, 0}, o_left[2] = {0, 0}, o_pi[2] = {-1, -1}, o_r[2] = {-1, -1};
+        bool o_first[2] = {true, true};
+        auto ready = [&](uint64_t* bar, uint32_t parity) {
+          return __all_sync(0xffffffffu, mbar_test(bar, parity));
+        };
+        auto next_round = [&](int r) {
+          do { ++r; } while (r < rounds && rcnt[r] == 0);
+          return r;
+        };
         uint32_t idle = 0;
-        while ((oN[0] < total || oN[1] < total) && !*fail) {
+        while (oN[0] < total || oN[1] < total) {
           bool progress = false;
 #pragma unroll
           for (int X = 0; X < 2; ++X) {
             // ---- O_X(oN[X])
             if (oN[X] < sN[X]) {
+              if (o_left[X] == 0) {  // block oN[X] starts the next pair
+                o_r[X] = next_round(o_r[X]);
+                o_left[X] = o_r[X] < rounds ? rcnt[o_r[X]] : 0;
+                ++o_pi[X];
+                o_first[X] = true;
+              }
               const int n = oN[X];
-              while (n >= o_end[X] && o_rd[X] < rounds) {  // advance to the pair of block n
-                if (o_pairs[X] >= 0) ++o_rd[X];
-                while (o_rd[X] < rounds && (cta_pair(o_rd[X], p.npairs) < 0 ||
-                                            p.dcnt[cta_pair(o_rd[X], p.npairs)] <= 0))
-                  ++o_rd[X];
-                if (o_rd[X] >= rounds) break;
-                o_first[X] = o_end[X];
-                o_end[X] += p.dcnt[cta_pair(o_rd[X], p.npairs)];
-                ++o_pairs[X];
-              }
-              if (n >= o_end[X]) {  // block sequence inconsistent with the pair counts
-                msa_record_error(kErrBadBlock);
-                *fail = 1;
-                break;
-              }
-              const bool first = n == o_first[X];
-              if (mbar_test(&B.p_full[X], n & 1) &&
-                  (!first || o_pairs[X] == 0 || mbar_test(&B.o_free[X], (o_pairs[X] - 1) & 1))) {
+              if (ready(&B.p_full[X], n & 1) &&
+                  (!o_first[X] || o_pi[X] == 0 || ready(&B.o_free[X], (o_pi[X] - 1) & 1))) {
                 tmem_fence_after();
                 const int c = n & 1;
-                const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
+                const uint64_t bd0 =
+                    umma_desc_sw128(sbase + kOffKV + c * 2 * kTileBytes + kTileBytes, kBox, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                  const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-                  umma_bf16_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, bd, idesc_o,
-                               (!first || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(&B.o_full[X]);
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_bf16_ts_elect(tmem + 256 + X * 128, tmem + X * 128 + kk * 8,
+                                     bd0 + kk * (2048 >> 4), idesc_o,
+                                     (!o_first[X] || kk > 0) ? 1u : 0u);
+                umma_commit_elect(&B.o_full[X]);
                 ++oN[X];
-                if (oN[1 - X] >= oN[X]) umma_commit(&B.kv_empty[c]);  // both O(n) issued
+                if (oN[1 - X] >= oN[X]) umma_commit_elect(&B.kv_empty[c]);  // both O(n) issued
+                --o_left[X];
+                o_first[X] = false;
                 progress = true;
               }
             }
             // ---- S_X(sN[X])
             if (sN[X] < total && oN[X] >= sN[X]) {
+              if (s_left[X] == 0) {
+                s_r[X] = next_round(s_r[X]);
+                s_left[X] = s_r[X] < rounds ? rcnt[s_r[X]] : 0;
+                ++s_pi[X];
+              }
               const int n = sN[X];
-              while (n >= s_end[X] && s_rd[X] < rounds) {
-                if (s_pairs[X] >= 0) ++s_rd[X];
-                while (s_rd[X] < rounds && (cta_pair(s_rd[X], p.npairs) < 0 ||
-                                            p.dcnt[cta_pair(s_rd[X], p.npairs)] <= 0))
-                  ++s_rd[X];
-                if (s_rd[X] >= rounds) break;
-                s_end[X] += p.dcnt[cta_pair(s_rd[X], p.npairs)];
-                ++s_pairs[X];
-              }
-              if (n >= s_end[X]) {
-                msa_record_error(kErrBadBlock);
-                *fail = 1;
-                break;
-              }
-              if (mbar_test(&B.kv_full[n & 1], (n >> 1) & 1) &&
-                  mbar_test(&B.q_full, s_pairs[X] & 1) &&
-                  (n == 0 || mbar_test(&B.o_full[X], (n - 1) & 1))) {
+              if (ready(&B.kv_full[n & 1], (n >> 1) & 1) && ready(&B.q_full, s_pi[X] & 1)) {
                 tmem_fence_after();
-                const uint32_t qa = sbase + kOffQ + X * kTileBytes;
-                const uint32_t ka = sbase + kOffKV + (n & 1) * 2 * kTileBytes;
+                const uint64_t qd0 = umma_desc_sw128(sbase + kOffQ + X * kTileBytes, 16, qsbo);
+                const uint64_t kd0 = umma_desc_sw128(sbase + kOffKV + (n & 1) * 2 * kTileBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                  const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
-                                                  : (kk >> 2) * kBox + (kk & 3) * 32;
+                  const uint32_t qoff = (kk >> 2) * qhalf + (kk & 3) * 32;
                   const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                  umma_bf16(tmem + X * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
-                            umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                  umma_bf16_elect(tmem + X * 128, qd0 + (qoff >> 4), kd0 + (off >> 4), idesc_s,
+                                  kk > 0);
                 }
-                umma_commit(&B.s_full[X]);
+                umma_commit_elect(&B.s_full[X]);
                 ++sN[X];
                 // the pair's last block: once both tiles' S of it are issued (the two tiles run
                 // the same block sequence) the query tiles are free
-                if (sN[X] == s_end[X] && sN[1 - X] >= sN[X]) umma_commit(&B.q_empty);
+                if (--s_left[X] == 0 && sN[1 - X] >= sN[X]) umma_commit_elect(&B.q_empty);
                 progress = true;
               }
             }
@@ -451,9 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int X = oN[0] <= oN[1] ? 0 : 1;
             if (oN[X] < sN[X]) mbar_try_wait_hint(&B.p_full[X], oN[X] & 1, kIssuerNap);
             else __nanosleep(32);
-            if (++idle > kWaitLimit) {
-              msa_record_error(kErrTimeout);
+            // every lane leaves together: the flag is agreed by a vote
+            const bool failed = __any_sync(0xffffffffu, *fail != 0);
+            if (++idle > kWaitLimit || failed) {
+              if (!failed && lane == 0) msa_record_error(kErrTimeout);
               *fail = 1;
+              break;
             }
           }
         }
@@ -471,11 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tmem = tmem + lane_addr + 256 + X * 128;
     const uint32_t qbit = 1u << (X * qpt + qi);
     int n = 0, pairs_done = 0;
-    for (int64_t r = 0; r < rounds && !*fail; ++r) {
-      const int64_t pr = cta_pair(r, p.npairs);
-      if (pr < 0) continue;
-      const int L = p.dcnt[pr];
-      if (L <= 0) continue;
+    for (int r = 0; r < rounds && !*fail; ++r) {
+      const int L = rcnt[r];
+      if (L == 0) continue;
+      const int64_t pr = cta_pair(r, p.pair0, p.npairs);
       const int g = (int)(pr / p.ppg);
       const int64_t t = slot_query(p.qperm, p.npos, g, (pr % p.ppg) * 2 * qpt + X * qpt + qi, p.T);
       const bool valid = t >= 0;
@@ -499,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, v + c * 32);
         tmem_wait_ld();
-        // a row whose query did not choose this block is masked entirely; otherwise only the
-        // keys after the query on its own block
-        const int64_t lim64 = sel ? pos - (int64_t)blk * 128 : -1;  // last visible column
-        if (lim64 < 127) {
+        // causal mask on the query's own block; a row whose query did not choose this block
+        // gets P = 0 through its exponent (scale 0, offset -inf) instead of a mask
+        const int64_t lim64 = pos - (int64_t)blk * 128;  // last visible column
+        if (sel && lim64 < 127) {
           const int lim = lim64 < -1 ? -1 : (int)lim64;
 #pragma unroll
           for (int x = 0; x < 128; ++x)
@@ -511,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
         for (int x = 4; x < 128; x += 2) m4[(x >> 1) & 3] = max3(m4[(x >> 1) & 3], v[x], v[x + 1]);
-        const float m2 = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]) * kLog2e;
+        const float m2 = sel ? fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]) * kLog2e : -INFINITY;
         if (m_run == -INFINITY) {
           m_run = m2;  // the row's O is still zero
         } else if (m2 > m_run + kRescale) {
@@ -520,11 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m2;
           l *= factor;
         }
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;  // masked rows: 2^-inf = 0
+        const float sc = sel ? kLog2e : 0.f;
+        const float off = sel ? -m_run : -INFINITY;
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int x = 0; x < 128; x += 2) {
-          fma2(v[x], v[x + 1], v[x], v[x + 1], kLog2e, kLog2e, -m_use, -m_use);
+          fma2(v[x], v[x + 1], v[x], v[x + 1], sc, sc, off, off);
           v[x] = ex2(v[x]);
           v[x + 1] = ex2(v[x + 1]);
           add2(l8[(x >> 1) & 3], l8[4 + ((x >> 1) & 3)], v[x], v[x + 1]);
@@ -670,8 +681,14 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int64_t grid = std::min<int64_t>(p.npairs, sm_count());
-  prefill_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
-  return cudaGetLastError();
+  // one launch per kMaxRounds rounds of pairs (the per-round counts live in shared memory)
+  for (int64_t pair0 = 0; pair0 < p.npairs; pair0 += grid * kMaxRounds) {
+    p.pair0 = pair0;
+    prefill_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace msa
