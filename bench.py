@@ -163,6 +163,72 @@ def visible_keys(block_ids: torch.Tensor, q_pos: torch.Tensor) -> torch.Tensor:
     return n.sum(dim=2)
 
 
+def prefill_split(block_ids: torch.Tensor, S_kv: int, G: int, D: int) -> dict:
+    """FLOPs of the two attention passes of msa_sparse_prefill, for reporting.
+
+    Restates the selection rule of the query-major pass (G 8 / 16, key range <= 16384 blocks):
+    the queries of each 128-query span are ranked by how many of their blocks at least half of
+    the span chose (stable, descending); 2*128/G consecutive ranks form a pair; a block at
+    least half of the pair's slots chose (at most 64 per pair, ascending) is computed
+    query-major for the whole pair, every other selection block-major. Returns algorithmic
+    FLOPs of each pass and the FLOPs the query-major pass executes (masked rows included)."""
+    T, Hkv, k = block_ids.shape
+    dev = block_ids.device
+    pos = torch.arange(S_kv - T, S_kv, device=dev)
+    ids = block_ids.long()
+    valid = ids >= 0
+    local = (pos // BLOCK)[:, None, None]
+    vis = torch.where(ids < local, torch.full_like(ids, BLOCK), (pos % BLOCK + 1)[:, None, None].expand_as(ids))
+    vis = torch.where(valid & (ids <= local), vis, torch.zeros_like(vis))
+    flops_sel = 4 * D * G * vis                                  # per (t, g, slot)
+    total = int(flops_sel.sum())
+    nb = (S_kv + BLOCK - 1) // BLOCK
+    if G not in (8, 16) or nb > 16384:
+        return {"flops_total": total, "flops_block_major": total, "flops_query_major": 0,
+                "flops_query_major_executed": 0, "query_major_items": 0}
+    qpt = 128 // G
+    nq = 2 * qpt
+    nspan = (T + 127) // 128
+    Tp = nspan * 128
+    idp = torch.full((Tp, Hkv, k), -1, dtype=torch.long, device=dev)
+    idp[:T] = ids
+    vp = idp >= 0
+    span = torch.arange(Tp, device=dev) // 128
+    g_idx = torch.arange(Hkv, device=dev)[None, :, None].expand(Tp, Hkv, k)
+    s_idx = span[:, None, None].expand(Tp, Hkv, k)
+    col = torch.where(vp, idp, torch.full_like(idp, nb))        # invalid -> trash column nb
+    key = (g_idx * nspan + s_idx) * (nb + 1) + col
+    cnt = torch.zeros(Hkv * nspan * (nb + 1), dtype=torch.long, device=dev)
+    cnt.scatter_add_(0, key.reshape(-1), vp.reshape(-1).long())
+    nvalid = torch.clamp(T - torch.arange(nspan, device=dev) * 128, max=128)
+    cnt3 = cnt.view(Hkv, nspan, nb + 1)
+    pop = 2 * cnt3 >= nvalid[None, :, None]
+    pop[:, :, nb] = False
+    sel_pop = pop.view(-1)[key.reshape(-1)].view(Tp, Hkv, k) & vp
+    score = sel_pop.sum(dim=2)                                   # [Tp, Hkv]
+    score = torch.where(torch.arange(Tp, device=dev)[:, None] < T, score, torch.full_like(score, -1))
+    sc = score.view(nspan, 128, Hkv).permute(2, 0, 1)            # [Hkv, nspan, 128]
+    order = torch.sort(-sc, dim=2, stable=True).indices          # slot -> query within span
+    rank = torch.empty_like(order)
+    rank.scatter_(2, order, torch.arange(128, device=dev).expand_as(order))
+    pair = (rank // nq).permute(1, 2, 0).reshape(Tp, Hkv)        # pair within span per (t, g)
+    npp = 128 // nq
+    pkey = ((g_idx * nspan + s_idx) * npp + pair[:, :, None]) * (nb + 1) + col
+    pc = torch.zeros(Hkv * nspan * npp * (nb + 1), dtype=torch.long, device=dev)
+    pc.scatter_add_(0, pkey.reshape(-1), vp.reshape(-1).long())
+    pc = pc.view(-1, nb + 1)
+    pc[:, nb] = 0
+    thr = max(2, (nq + 1) // 2)
+    dense = pc >= thr
+    dense &= torch.cumsum(dense.long(), dim=1) <= 64             # kMaxDense per pair
+    items = int(dense.sum())
+    in_qm = dense.view(-1)[pkey.reshape(-1)].view(Tp, Hkv, k) & vp
+    qm = int(flops_sel[in_qm[:T]].sum())
+    return {"flops_total": total, "flops_query_major": qm, "flops_block_major": total - qm,
+            "flops_query_major_executed": items * 2 * 2 * 2 * 128 * 128 * 128,
+            "query_major_items": items}
+
+
 def build_workloads(dev, seed_offset: int, small: bool = False):
     # --small (profiling captures only): 8 decode requests and an 8192-token prefill chunk
     wsc = workloads.decode_scoring(dev, seed=2 + seed_offset)
@@ -186,8 +252,51 @@ def build_workloads(dev, seed_offset: int, small: bool = False):
     # bf16 partial rows (G per selection, D channels) written once and read once, + fp32 LSE
     nsel3 = int((wpf["block_ids"] >= 0).sum().item())
     wpf["partial_bytes"] = nsel3 * Gpf * (2 * wpf["D"] * 2 + 4 * 2)
+    # bytes a perfect prefill must move: q read, each K/V row of the sequence read once, o
+    # written, lse written
+    wpf["algorithmic_bytes"] = (wpf["q"].numel() * 2 + wpf["k"].numel() * 2 * 2
+                                + wpf["T"] * wpf["Hq"] * (wpf["D"] * 2 + 4))
+    wpf["split"] = prefill_split(wpf["block_ids"], wpf["S_kv"], Gpf, wpf["D"])
     del Gdc
     return wsc, wdc, wpf
+
+
+def prefill_stage(wpf, pre_ms, pk):
+    """The prefill call's line: end-to-end TFLOP/s against the burst bf16 peak (the call is timed
+    alone per step, a few ms, not a seconds-long loop), its FLOP split between the query-major and
+    block-major passes, and its DRAM traffic against the bytes a perfect call must move."""
+    eps = 1e-9
+    tfl = wpf["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
+    sp = wpf["split"]
+    traffic = prefill_traffic()
+    return {"config": f"T {wpf['T']} causal, Hq {wpf['Hq']}, Hkv {wpf['Hkv']}, D {wpf['D']}, "
+                      f"k {wpf['topk']}", "ms": round(pre_ms, 4),
+            "TFLOP/s": round(tfl, 1),
+            "frac_bf16": round(tfl / pk["bf16_tflops"], 4),
+            "peak": pk["bf16_tflops"], "peak_kind": "burst (measured)",
+            "frac_bf16_sustained": round(tfl / pk["bf16_tflops_sustained"], 4),
+            "kernels": "query-major selection + attention for blocks shared by a query pair; "
+                       "bucketing + block-major attention for the rest; LSE merge "
+                       "(per-kernel times: profiles/launches_bench_default.md)",
+            "flops": wpf["flops"],
+            # algorithmic FLOPs per pass, and what the query-major pass executes (its pairs'
+            # rows that did not choose a block ride through the MMAs masked)
+            "flops_query_major": sp["flops_query_major"],
+            "flops_block_major": sp["flops_block_major"],
+            "flops_query_major_executed": sp["flops_query_major_executed"],
+            "query_major_items": sp["query_major_items"],
+            # a purely block-major prefill writes one bf16 partial of G rows per (query, block)
+            # selection and reads it back: that traffic alone takes block_major_floor_ms at the
+            # measured HBM bandwidth
+            "block_major_partials_bytes": wpf["partial_bytes"],
+            "block_major_floor_ms": round(wpf["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
+            # q in, each K/V row once, o and lse out
+            "algorithmic_bytes": wpf["algorithmic_bytes"],
+            # DRAM bytes of every kernel of the call, from per-kernel captures (null when any
+            # kernel's source changed since it was captured)
+            "traffic_total": traffic,
+            "traffic_over_algorithmic": (round(traffic / wpf["algorithmic_bytes"], 3)
+                                         if traffic else None)}
 
 
 def src_hash(*names):
@@ -211,10 +320,25 @@ def recorded_traffic(kernel: str, source_hash: str):
     return rec.get("bytes_per_launch")
 
 
+# Every kernel of one msa_sparse_prefill call and the source file it is built from.
+PREFILL_KERNELS = (("pair_order_kernel", "prefill_dense.cu"), ("dense_select_kernel", "prefill_dense.cu"),
+                   ("bucket_count_kernel", "prefill.cu"), ("bucket_scan_kernel", "prefill.cu"),
+                   ("bucket_seg_scan_kernel", "prefill.cu"), ("bucket_scatter_kernel", "prefill.cu"),
+                   ("tile_desc_kernel", "prefill.cu"), ("prefill_block_tc_kernel", "prefill.cu"),
+                   ("prefill_dense_tc_kernel", "prefill_dense.cu"),
+                   ("lse_merge_chunked_kernel", "page_table_merge.cu"))
+
+
 def prefill_traffic():
-    blk = recorded_traffic("prefill_block_tc_kernel", src_hash("prefill.cu"))
-    dense = recorded_traffic("prefill_dense_tc_kernel", src_hash("prefill_dense.cu"))
-    return None if blk is None or dense is None else blk + dense
+    """DRAM bytes of one prefill call: the sum over its kernels' recorded captures (null while
+    any of them is missing or its source changed since it was captured)."""
+    tot = 0
+    for name, src in PREFILL_KERNELS:
+        b = recorded_traffic(name, src_hash(src))
+        if b is None:
+            return None
+        tot += b
+    return tot
 
 
 # --------------------------------------------------------------------------- our arm
@@ -296,8 +420,17 @@ def run_ours(args, ws, rank, local):
     pre_tflops = wpf["flops"] / (max(pre_ms, eps) * 1e-3) / 1e12
     value = job_throughput(wsc["bytes"], max(score_ms, eps), ws) / 1e9
 
-    # e2e through host buffers for the headline stage
+    # e2e through host buffers for the headline stage, and for the decode stage
     e2e = e2e_score(msa, wsc, wsp, dev, args.steps, ws) if "score" in run else None
+    e2e_dec = e2e_decode(msa, wdc, wsp, dev, args.steps, ws) if "decode" in run else None
+    # multi-token decode / verify rows, and decode from host-resident K/V caches (outside the
+    # timed step: each is its own configuration)
+    extra = {}
+    if not args.no_extra and {"score", "decode"} <= run:
+        extra.update(multi_token_stages(msa, wsc, wdc, wsp, dev, max(10, args.steps), pk))
+        if not args.no_host_stage:
+            extra["sparse_decode_host_kv"] = staged_host_decode(msa, wdc, fpt_dc, len4, wsp, dev,
+                                                                max(10, args.steps), pk)
 
     h_score = src_hash("score_topk.cu")
     roofline = {"kernel": "score_decode_kernel (msa_index_score_topk)", "bound": "hbm",
@@ -315,24 +448,9 @@ def run_ours(args, ws, rank, local):
                           "ms_page_table": round(pt_ms, 4), "ms_decode": round(dec_ms, 4),
                           "GB/s": round(dec_gbs, 1), "frac_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
                           "bytes": wdc["bytes"], "kv_bytes": wdc["kv_bytes"],
-                          "traffic": recorded_traffic("paged_decode_kernel", src_hash("decode.cu"))},
-        "sparse_prefill": {"config": f"T {wpf['T']} causal, Hq {wpf['Hq']}, Hkv {wpf['Hkv']}, D {wpf['D']}, "
-                                     f"k {wpf['topk']}", "ms": round(pre_ms, 4),
-                           "TFLOP/s": round(pre_tflops, 1),
-                           "frac_bf16": round(pre_tflops / pk["bf16_tflops_sustained"], 4),
-                           "kernels": "query-major selection + attention for blocks shared by a "
-                                      "query pair; bucketing + block-major attention for the "
-                                      "rest; LSE merge (per-kernel shares: profiles/)",
-                           "flops": wpf["flops"],
-                           # a purely block-major prefill writes one bf16 partial of G rows per
-                           # (query, block) selection and reads it back: that traffic alone takes
-                           # block_major_floor_ms at the measured HBM bandwidth (the query-major
-                           # pass removes most of it for shared blocks)
-                           "block_major_partials_bytes": wpf["partial_bytes"],
-                           "block_major_floor_ms": round(wpf["partial_bytes"] / pk["hbm_gbs"] / 1e6, 4),
-                           # DRAM bytes of the two attention kernels per call (null when either
-                           # source changed since it was profiled)
-                           "traffic": prefill_traffic()},
+                          "traffic": recorded_traffic("paged_decode_kernel", src_hash("decode.cu")),
+                          "e2e": e2e_dec},
+        "sparse_prefill": prefill_stage(wpf, pre_ms, pk),
     }
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
@@ -354,6 +472,7 @@ def run_ours(args, ws, rank, local):
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
         if key not in run:
             stages[name] = None
+    stages.update(extra)
     if "score" not in run:  # the headline is the scorer's: nothing to report without it
         line["value"] = None
         line["roofline"] = None
@@ -361,8 +480,14 @@ def run_ours(args, ws, rank, local):
         line["long_context"] = run_long_context(args, local)
     if args.small or run != {"score", "decode", "prefill"}:
         line["config"]["partial_run"] = f"stages={sorted(run)} small={args.small} (profiling only)"
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and "score" in run:
-        line["cpu_baseline"] = cpu_baseline(wsc, args.cpu_seconds)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        if "score" in run:
+            line["cpu_baseline"] = cpu_baseline(wsc, args.cpu_seconds)
+            stages["index_score_topk"]["cpu_baseline"] = line["cpu_baseline"]
+        if "decode" in run:
+            stages["sparse_decode"]["cpu_baseline"] = cpu_baseline_decode(wdc)
+        if "prefill" in run:
+            stages["sparse_prefill"]["cpu_baseline"] = cpu_baseline_prefill(wpf)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -411,6 +536,185 @@ def e2e_score(msa, wsc, wsp, dev, steps: int, ws: int):
             "note": "per-step inputs copied from pinned host memory; paged K-index resident"}
 
 
+# --------------------------------------------------------------------------- extra stages
+
+def _timed(fn, reps: int) -> float:
+    """Mean ms per call of fn on the current stream, after 3 untimed calls."""
+    for _ in range(3):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def multi_token_stages(msa, wsc, wdc, wsp, dev, reps: int, pk) -> dict:
+    """Multi-token decode / speculative verify: N query rows per request.
+
+    * index score + top-k for N = 2, 4, 8 rows per request on the decode-scoring K-index (8
+      requests x 60032 tokens): the streaming scorer reads the K-index once for all N rows;
+    * sparse page table + paged decode for N = 2, 4 rows per request on the paged-decode caches
+      (64 requests): each row reads its own selection (rows are not deduplicated)."""
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    B, Hkv, Di, k = wsc["B"], wsc["Hkv"], wsc["Di"], wsc["topk"]
+    kidx_bytes = int(wsc["seq_lens"].to(torch.int64).sum()) * Hkv * Di * 2 + wsc["page_table"].numel() * 4
+    for N in (2, 4, 8):
+        q_idx = workloads.randn_bf16((B * N, Hkv, Di), gen, dev)
+        ids = torch.empty((B * N, Hkv, k), dtype=torch.int32, device=dev)
+        sc = torch.empty((B * N, Hkv, k), dtype=torch.float32, device=dev)
+        ms = _timed(lambda: msa.index_score_topk(q_idx, wsc["k_idx_pages"], wsc["page_table"],
+                                                 wsc["seq_lens"], N, k, workspace=wsp,
+                                                 out=(ids, sc)), reps)
+        nbytes = kidx_bytes + q_idx.numel() * 2 + ids.numel() * 8
+        gbs = nbytes / ms / 1e6
+        out[f"index_score_topk_N{N}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                         "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "bytes": nbytes}
+    Bd, Hq, Hkvd, D, kd = wdc["B"], wdc["Hq"], wdc["Hkv"], wdc["D"], wdc["topk"]
+    sl = wdc["seq_lens"].to(torch.int64)
+    for N in (2, 4):
+        q = workloads.randn_bf16((Bd * N, Hq, D), gen, dev, scale=D ** -0.5)
+        q_pos = (sl[:, None] - N + torch.arange(N, device=dev)[None, :]).reshape(-1)
+        ids = workloads.sample_selection(q_pos, Hkvd, kd, gen)
+        fpt = torch.empty((Bd * N * Hkvd, kd), dtype=torch.int32, device=dev)
+        lens = torch.empty((Bd * N * Hkvd,), dtype=torch.int32, device=dev)
+        o = torch.empty((Bd * N, Hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((Bd * N, Hq), dtype=torch.float32, device=dev)
+
+        def f():
+            msa.build_sparse_page_table(ids, wdc["page_table"], wdc["seq_lens"], N, wdc["num_pages"],
+                                        out=(fpt, lens))
+            msa.paged_sparse_decode(q, wdc["k_cache"], wdc["v_cache"], fpt, lens, workspace=wsp,
+                                    out=(o, lse))
+        ms = _timed(f, reps)
+        kv = int(visible_keys(ids, q_pos).sum()) * D * 2 * 2
+        nbytes = kv + q.numel() * 2 * 2 + lse.numel() * 4
+        gbs = nbytes / ms / 1e6
+        out[f"sparse_decode_N{N}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "bytes": nbytes,
+                                      "kv_bytes": kv}
+    return out
+
+
+def staged_host_decode(msa, wdc, fpt_dc, len4, wsp, dev, reps: int, pk) -> dict:
+    """KV residency split at the paged-decode workload: the K/V caches live in pinned host
+    memory; per step the selected blocks' K/V rows are staged onto the device (read by the
+    kernel over the host link) and the paged decode runs on the staging cache."""
+    t0 = time.perf_counter()
+    hk = torch.empty(wdc["k_cache"].shape, dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty(wdc["v_cache"].shape, dtype=torch.bfloat16, pin_memory=True)
+    hk.copy_(wdc["k_cache"])
+    hv.copy_(wdc["v_cache"])
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t0
+    R, Hkv, D, k = wdc["B"], wdc["Hkv"], wdc["D"], wdc["topk"]
+    ks = torch.empty((R * k, BLOCK, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    spt = torch.empty_like(fpt_dc)
+    o = torch.empty((R, wdc["Hq"], D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, wdc["Hq"]), dtype=torch.float32, device=dev)
+    ms_stage = _timed(lambda: msa.stage_selected_kv(hk, hv, fpt_dc, out=(ks, vs, spt)), reps)
+
+    def f():
+        msa.stage_selected_kv(hk, hv, fpt_dc, out=(ks, vs, spt))
+        msa.paged_sparse_decode(wdc["q"], ks, vs, spt, len4, workspace=wsp, out=(o, lse))
+    ms = _timed(f, reps)
+    staged = int((fpt_dc >= 0).sum()) * BLOCK * D * 2 * 2       # whole pages of one group, K + V
+    del hk, hv
+    return {"config": "paged-decode workload with K/V caches in pinned host memory",
+            "ms_stage": round(ms_stage, 4), "ms_stage_and_decode": round(ms, 4),
+            "staged_bytes": staged, "GB/s_staging": round(staged / ms_stage / 1e6, 1),
+            "host_cache_bytes": 2 * wdc["k_cache"].numel() * 2, "setup_s": round(setup_s, 1)}
+
+
+def e2e_decode(msa, wdc, wsp, dev, steps: int, ws: int) -> dict:
+    """Sparse page table + paged decode through the public API from pinned host buffers: per
+    step the queries, selections, lengths and page table go host->device and the output and
+    LSE come back; the K/V caches are resident state."""
+    R, Hq, D, Hkv, k = wdc["B"], wdc["Hq"], wdc["D"], wdc["Hkv"], wdc["topk"]
+    hq = wdc["q"].cpu().pin_memory()
+    hids = wdc["block_ids"].cpu().pin_memory()
+    hsl = wdc["seq_lens"].cpu().pin_memory()
+    hpt = wdc["page_table"].cpu().pin_memory()
+    ho = torch.empty((R, Hq, D), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((R, Hq), dtype=torch.float32).pin_memory()
+    dq, dids, dsl, dpt = (torch.empty_like(x, device=dev) for x in (hq, hids, hsl, hpt))
+    fpt = torch.empty((R * Hkv, k), dtype=torch.int32, device=dev)
+    lens = torch.empty((R * Hkv,), dtype=torch.int32, device=dev)
+    o = torch.empty((R, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, Hq), dtype=torch.float32, device=dev)
+
+    def one():
+        for d, h in ((dq, hq), (dids, hids), (dsl, hsl), (dpt, hpt)):
+            d.copy_(h, non_blocking=True)
+        msa.build_sparse_page_table(dids, dpt, dsl, 1, wdc["num_pages"], out=(fpt, lens))
+        msa.paged_sparse_decode(dq, wdc["k_cache"], wdc["v_cache"], fpt, lens, workspace=wsp,
+                                out=(o, lse))
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    ms = max_over_ranks([_timed(one, steps)], ws, dev)[0]
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hids, hsl, hpt))
+    d2h = ho.numel() * 2 + hlse.numel() * 4
+    return {"value": round(job_throughput(wdc["bytes"], ms, ws) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "per-step inputs copied from pinned host memory; K/V caches resident"}
+
+
+# --------------------------------------------------------------------------- CPU oracle, per stage
+
+def cpu_baseline_decode(wdc, n_req: int = 16) -> dict:
+    """The oracle's sparse decode on the first n_req requests of the paged-decode workload (all
+    their rows and heads), GB/s over their selected K/V bytes."""
+    import numpy as np
+    import oracle
+    u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    ids = wdc["block_ids"][:n_req]
+    pt = wdc["page_table"][:n_req]
+    sel_pages = torch.gather(pt, 1, ids.clamp(min=0).long().reshape(n_req, -1))[ids.reshape(n_req, -1) >= 0]
+    pages = torch.unique(sel_pages).long()
+    remap = torch.zeros(wdc["num_pages"], dtype=torch.int32, device=pt.device)
+    remap[pages] = torch.arange(pages.numel(), dtype=torch.int32, device=pt.device)
+    pt_small = remap[pt.long()]                      # pages never selected map to 0, never read
+    kc, vc = u16(wdc["k_cache"][pages]), u16(wdc["v_cache"][pages])
+    q = u16(wdc["q"][:n_req])
+    sl = wdc["seq_lens"][:n_req].cpu().numpy()
+    ids_np = ids.cpu().numpy()
+    kv = int(visible_keys(ids, (wdc["seq_lens"][:n_req].to(torch.int64) - 1)).sum()) * wdc["D"] * 4
+    t0 = time.perf_counter()
+    oracle.sparse_decode(q, kc, vc, pt_small.cpu().numpy(), sl, ids_np, 1)
+    dt = time.perf_counter() - t0
+    return {"value": round(kv / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": f"{n_req} of {wdc['B']} requests, all heads, in {dt:.2f} s"}
+
+
+def cpu_baseline_prefill(wpf, n_rows: int = 128) -> dict:
+    """The oracle's sparse prefill on n_rows query rows spread over the chunk (all heads),
+    TFLOP/s over their algorithmic FLOPs."""
+    import numpy as np
+    import oracle
+    u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    T, Hq, D = wpf["T"], wpf["Hq"], wpf["D"]
+    G = Hq // wpf["Hkv"]
+    rows = torch.linspace(0, T - 1, n_rows).round().long().unique()
+    units = (rows[:, None] * Hq + torch.arange(Hq)[None, :]).reshape(-1).numpy()
+    q_pos = (wpf["S_kv"] - T + rows).to(wpf["block_ids"].device)
+    flops = 4 * D * G * int(visible_keys(wpf["block_ids"][rows.to(q_pos.device)], q_pos).sum())
+    q, k, v = u16(wpf["q"]), u16(wpf["k"]), u16(wpf["v"])
+    ids = wpf["block_ids"].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.sparse_prefill(q, k, v, ids, units=units)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": f"{rows.numel()} of {T} query rows (all {Hq} heads) in {dt:.2f} s"}
+
+
 # --------------------------------------------------------------------------- CPU oracle
 
 def _oracle_score_step(oracle, h):
@@ -443,8 +747,8 @@ def cpu_baseline(wsc, seconds: float):
             break
     dt = time.perf_counter() - t0
     gbs = n * B * per_row / dt / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": min(os.cpu_count() or 1, B),
-            "kind": "oracle",
+    return {"value": round(gbs, 3), "unit": "GB/s",
+            "cores": min(oracle.default_threads(), B * wsc["Hkv"]), "kind": "oracle",
             "sample": f"{n} full passes of all {B} requests (scores + top-k) in {dt:.1f} s"}
 
 
@@ -551,7 +855,7 @@ def run_reference(args, ws, rank, local):
     dt = time.perf_counter() - t0
     ms = dt / args.steps * 1e3
     gbs = wsc["bytes"] / (ms * 1e-3) / 1e9
-    cores = min(os.cpu_count() or 1, B)
+    cores = min(oracle.default_threads(), B * wsc["Hkv"])
     line = {"metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "impl": "reference",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -579,6 +883,10 @@ def main():
                     help="also report the 1M-token layer's stages (takes about a minute)")
     ap.add_argument("--small", action="store_true",
                     help="smaller decode/prefill workloads (profiling captures only)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the multi-token and host-resident K/V stages")
+    ap.add_argument("--no-host-stage", action="store_true",
+                    help="skip the decode from host-resident K/V caches")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_info()

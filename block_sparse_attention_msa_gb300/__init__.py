@@ -206,12 +206,13 @@ def build_sparse_page_table(block_ids, page_table, seq_lens, N: int, num_pages: 
 
 # ------------------------------------------------------------------------------ stage 2
 
-def stage_selected_kv(k_cache, v_cache, flat_page_table):
+def stage_selected_kv(k_cache, v_cache, flat_page_table, out=None):
     """Copy the selected blocks' K/V to a device staging cache (``msa_stage_selected_kv``).
 
     k_cache, v_cache [P, 128, Hkv, D] bf16: CUDA tensors or pinned host tensors (read by the
     device directly); flat_page_table [R*Hkv, topk] int32 (CUDA). Returns (k_stage, v_stage
-    [R*topk, 128, Hkv, D] bf16, stage_page_table [R*Hkv, topk] int32) for ``paged_sparse_decode``.
+    [R*topk, 128, Hkv, D] bf16, stage_page_table [R*Hkv, topk] int32) for ``paged_sparse_decode``,
+    written into ``out`` when given.
     """
     for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
@@ -225,9 +226,18 @@ def stage_selected_kv(k_cache, v_cache, flat_page_table):
         raise ValueError("stage_selected_kv: inconsistent shapes")
     R = RH // Hkv
     dev = flat_page_table.device
-    k_stage = torch.empty((R * topk, BLOCK, Hkv, D), dtype=torch.bfloat16, device=dev)
-    v_stage = torch.empty_like(k_stage)
-    spt = torch.empty_like(flat_page_table)
+    if out is None:
+        k_stage = torch.empty((R * topk, BLOCK, Hkv, D), dtype=torch.bfloat16, device=dev)
+        v_stage = torch.empty_like(k_stage)
+        spt = torch.empty_like(flat_page_table)
+    else:
+        k_stage, v_stage, spt = out
+        _need(k_stage, "k_stage", torch.bfloat16, 4)
+        _need(v_stage, "v_stage", torch.bfloat16, 4)
+        _need(spt, "stage_page_table", torch.int32, 2)
+        if (k_stage.shape != (R * topk, BLOCK, Hkv, D) or v_stage.shape != k_stage.shape
+                or spt.shape != flat_page_table.shape):
+            raise ValueError("stage_selected_kv: output shapes do not match")
     rc = load().msa_stage_selected_kv(k_cache.data_ptr(), v_cache.data_ptr(), P,
                                       _ptr(flat_page_table), R, Hkv, D, topk, _ptr(k_stage),
                                       _ptr(v_stage), _ptr(spt), _stream(dev))
