@@ -413,7 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // serves is usually still in its own epilogue. An idle issuer blocks in hardware on the
       // next O's barrier for at most kIssuerNap ns before re-checking, so it reacts to either
       // within a few hundred cycles. All state stays in registers.
-      if (lane == 0) {
+      // The whole warp runs the loop in lockstep (barrier states agreed by a vote) and one
+      // elected lane issues each MMA and commit: a converged warp keeps the MMA operands in
+      // uniform registers, where a lone lane would move them over before every instruction.
+      {
+        auto ready = [&](uint64_t* bar, uint32_t parity) {
+          return __all_sync(0xffffffffu, mbar_test(bar, parity));
+        };
         const uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
         const uint32_t idesc_o = umma_idesc_bf16(128, 128, 0, 1);  // P (tmem) x V (MN-major)
         int kv_gj = -1, kv_loads = 0;
@@ -423,25 +429,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int after_gj = n > 1 ? load_desc(p, tile_of(1)).x : -2;
         int si = 0, oi = 0;
         uint32_t idle = 0;
-        while (oi < n && !*fail) {
+        while (oi < n && !__any_sync(0xffffffffu, *fail != 0)) {
           // ---- O(oi): needs P(oi) and the epilogue of oi-2 done with its O buffer
           if (oi < si) {
             const int b = oi & 1;
-            if (mbar_test(&B.p_full[b], (oi >> 1) & 1) &&
-                (oi < 2 || mbar_test(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
+            if (ready(&B.p_full[b], (oi >> 1) & 1) &&
+                (oi < 2 || ready(&B.o_free[b], ((oi - 2) >> 1) & 1))) {
               tmem_fence_after();
               const int c = b ? kvb1 : kvb0;
               const uint32_t va = sbase + kOffKV + c * 2 * kTileBytes + kTileBytes;
   #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t bd = umma_desc_sw128(va + kk * 2048, kBox, 1024);
-                umma_bf16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
+                umma_bf16_ts_elect(tmem + 256 + b * 128, tmem + b * 128 + kk * 8, bd, idesc_o, kk > 0);
               }
-              umma_commit(&B.o_full[b]);
+              umma_commit_elect(&B.o_full[b]);
               // the list of tile oi+1 (its S is issued, or it is the next S) tells whether tile
               // oi is the last one on this K/V load
               const int gj_after = oi + 1 < si ? (b ? gj0 : gj1) : (oi + 1 < n ? next_gj : -2);
-              if (gj_after != (b ? gj1 : gj0)) umma_commit(&B.kv_empty[c]);
+              if (gj_after != (b ? gj1 : gj0)) umma_commit_elect(&B.kv_empty[c]);
               ++oi;
               idle = 0;
               continue;
@@ -451,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (si < n && oi >= si - 1) {
             const int b = si & 1, qs = si % kQStages;
             const bool kv_new = next_gj != kv_gj;
-            if ((!kv_new || mbar_test(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
-                mbar_test(&B.q_full[qs], (si / kQStages) & 1) &&
-                (si < 2 || mbar_test(&B.o_full[b], ((si - 2) >> 1) & 1))) {
+            if ((!kv_new || ready(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
+                ready(&B.q_full[qs], (si / kQStages) & 1) &&
+                (si < 2 || ready(&B.o_full[b], ((si - 2) >> 1) & 1))) {
               tmem_fence_after();
               if (kv_new) {
                 ++kv_loads;
@@ -469,11 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qoff = p.q_atoms ? (kk >> 2) * 1024 + (kk & 3) * 32
                                                 : (kk >> 2) * kBox + (kk & 3) * 32;
                 const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                umma_bf16(tmem + b * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
-                          umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                umma_bf16_elect(tmem + b * 128, umma_desc_sw128(qa + qoff, 16, p.q_atoms ? 2048 : 1024),
+                                umma_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
               }
-              umma_commit(&B.s_full[b]);
-              umma_commit(&B.q_empty[qs]);
+              umma_commit_elect(&B.s_full[b]);
+              umma_commit_elect(&B.q_empty[qs]);
               if (b) {
                 gj1 = next_gj;
                 kvb1 = c;
