@@ -356,7 +356,7 @@ def prefill_bucket(block_ids, nblk: int, workspace: Workspace | None = None):
     offsets = torch.empty((Hkv, nblk + 1), dtype=torch.int32, device=dev)
     entries = torch.empty((max(T * Hkv * topk, 1),), dtype=torch.int32, device=dev)
     lib = load()
-    nbytes = lib.msa_prefill_bucket_workspace_size(Hkv, nblk)
+    nbytes = lib.msa_prefill_bucket_workspace_size(T, Hkv, topk, nblk)
     buf = _ws(workspace, dev).get("bucket", nbytes, dev)
     rc = lib.msa_prefill_bucket(_ptr(block_ids), T, Hkv, topk, nblk, _ptr(offsets), _ptr(entries),
                                 _ptr(buf), buf.numel(), _stream(dev))

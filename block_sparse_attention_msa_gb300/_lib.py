@@ -37,7 +37,7 @@ SIGNATURES = [
     ("msa_sparse_prefill", ctypes.c_int, [P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, SZ, P]),
     ("msa_sparse_prefill_paged", ctypes.c_int,
      [P, P, P, P, I64, P, I32, I64, I32, I32, I32, I32, P, P, P, SZ, P]),
-    ("msa_prefill_bucket_workspace_size", SZ, [I32, I32]),
+    ("msa_prefill_bucket_workspace_size", SZ, [I32, I32, I32, I32]),
     ("msa_prefill_bucket", ctypes.c_int, [P, I32, I32, I32, I32, P, P, P, SZ, P]),
     ("msa_lse_merge", ctypes.c_int, [P, I32, P, I64, I32, I32, I32, P, P, P]),
     ("msa_last_error", ctypes.c_char_p, []),

@@ -26,6 +26,11 @@ struct ScoreArgs {
 // Streaming scorer for N <= kDecodeMaxN with the top-k fused into the last CTA per request.
 constexpr int kDecodeMaxN = 8;
 cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream);
+// Multi-token decode scorer (2 <= N <= kDecodeTcMaxN) on the tensor cores, writing every
+// visible block score (the top-k kernel follows).
+constexpr int kDecodeTcMaxN = 16;
+cudaError_t launch_score_tc_decode(const ScoreArgs& a, cudaStream_t stream);
+int score_tc_decode_stages(int Hkv, int Di);
 // Generic scorer (any N) writing every block score, followed by the top-k kernel.
 cudaError_t launch_score_rows(const ScoreArgs& a, cudaStream_t stream);
 cudaError_t launch_topk_rows(const ScoreArgs& a, cudaStream_t stream);
@@ -94,7 +99,7 @@ inline int64_t prefill_pairs(int64_t T, int32_t Hkv, int32_t G) {
 // Pair slots per group: the chunk's queries in 128-query spans (a pair never crosses a span).
 inline int64_t prefill_qpos(int64_t T) { return (T + 127) / 128 * 128; }
 struct PrefillWorkspace {
-  size_t counts, group_base, tile_offsets, offsets, entries, part_o, part_lse, tile_desc;
+  size_t counts, group_base, tile_offsets, offsets, entries, epos, part_o, part_lse, tile_desc;
   size_t residual, dcnt, dblk, dmask, dense_o, dense_lse, qperm, total;  // query-major (G 8, 16)
 };
 inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
@@ -127,8 +132,9 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
   w.counts = off;       off = ws_align(off + 4 * lists);
   w.group_base = off;   off = ws_align(off + 4 * (groups + 1));
   w.tile_offsets = off; off = ws_align(off + 4 * (groups * (nblk + 1) + groups + 1));
+  const size_t sel = (size_t)T * Hkv * topk;
+  w.epos = off;         off = ws_align(off + 4 * sel);
   if (attention) {
-    const size_t sel = (size_t)T * Hkv * topk;
     w.offsets = off;    off = ws_align(off + 4 * groups * (nblk + 1));
     w.entries = off;    off = ws_align(off + 4 * sel);
     w.part_o = off;     off = ws_align(off + 2 * sel * G * 128);
@@ -171,8 +177,13 @@ __device__ __forceinline__ int32_t kv_block_row(const int32_t* page_table, int64
   bad = pg < 0 || pg >= num_pages;
   return (bad ? 0 : pg) * 128;
 }
-cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
-                                int32_t G, int32_t topk, const DenseWorkspace& w,
+// (a) of the prefill in one kernel per (group, 128-query span): the query order and the shared
+// blocks of each pair (G 8 / 16, when w.residual is set), then the count of every remaining
+// selection into its (group, query window, block) list, with its place in the list in `epos`.
+// `counts` [Hkv * nwin, nblk] must be zero on entry.
+cudaError_t launch_select_count(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
+                                int32_t G, int32_t topk, int32_t nblk, int32_t win,
+                                const DenseWorkspace& w, int32_t* counts, int32_t* epos,
                                 cudaStream_t stream);
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
@@ -183,10 +194,17 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
 // (a) bucketing; tiles of `qpt` queries are laid out for the attention kernel.
 // List of selection (t, slot) of group g: ((g * nwin + t / win) * nblk + j); the per-list
 // offsets are relative to their (group, window) segment, segments in (g, w) order.
+// launch_bucket_lists finishes lists counted by launch_select_count (offsets, tile descriptors
+// when `desc` is set, entries); launch_bucket runs all of it on plain selections.
+cudaError_t launch_bucket_lists(const int32_t* ids, const int32_t* epos, int32_t T, int32_t Hkv,
+                                int32_t topk, int32_t nblk, int32_t win, int32_t qpt,
+                                const int32_t* counts, int32_t* offsets, int32_t* entries,
+                                int32_t* group_base, int32_t* tile_offsets, int4* desc,
+                                cudaStream_t stream);
 cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
                           int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,
                           int32_t* entries, int32_t* counts, int32_t* group_base,
-                          int32_t* tile_offsets, cudaStream_t stream);
+                          int32_t* tile_offsets, int32_t* epos, cudaStream_t stream);
 struct PrefillArgs {
   const uint16_t* q;           // [T, Hq, D]
   const uint16_t* k;           // [S_kv, Hkv, D], or paged [num_pages, 128, Hkv, D]

@@ -118,13 +118,20 @@ static int index_score_topk_impl(const char* name, const uint16_t* q_idx,
                                       msa::ws_align((size_t)B * sizeof(int32_t)));
   int nstage = 0;
   msa::score_decode_smem_bytes(N, Hkv, Di, &nstage);
-  if (N <= msa::kDecodeMaxN && nstage >= 2) {
+  // one query row per request: the CUDA-core streaming scorer, with the top-k (and the page
+  // table) fused into its last CTA per request; 2..16 rows: the tensor-core decode scorer (the
+  // key index read once for all rows); longer chunks: the multi-row scorer. The last two are
+  // followed by the top-k kernel (one warp per row) and, when asked for, the page-table kernel.
+  const bool streaming = N == 1 && nstage >= 2;
+  const bool tc_decode = N >= 2 && N <= msa::kDecodeTcMaxN && msa::score_tc_decode_stages(Hkv, Di) >= 2;
+  if (streaming) {
     // the fused top-k counts finished pages per request from zero
     cudaError_t e = cudaMemsetAsync(a.tickets, 0, (size_t)B * sizeof(int32_t), as_stream(stream));
-    if (e == cudaSuccess) e = msa::launch_score_decode(a, as_stream(stream));  // + page table
+    if (e == cudaSuccess) e = msa::launch_score_decode(a, as_stream(stream));
     return cuda_status(e, name);
   }
-  cudaError_t e = msa::launch_score_rows(a, as_stream(stream));
+  cudaError_t e = tc_decode ? msa::launch_score_tc_decode(a, as_stream(stream))
+                            : msa::launch_score_rows(a, as_stream(stream));
   if (e == cudaSuccess) e = msa::launch_topk_rows(a, as_stream(stream));
   if (e == cudaSuccess && fpt)
     e = msa::launch_build_page_table(block_ids, page_table, seq_lens, B, N, Hkv, topk, max_blocks,
@@ -318,9 +325,9 @@ int msa_sparse_prefill_paged(const uint16_t* q, const uint16_t* k_cache, const u
                              workspace_bytes, stream);
 }
 
-size_t msa_prefill_bucket_workspace_size(int32_t Hkv, int32_t nblk) {
-  if (Hkv <= 0 || nblk <= 0) return 0;
-  return msa::prefill_ws_layout(0, Hkv, 1, nblk, 1, false).total;
+size_t msa_prefill_bucket_workspace_size(int32_t T, int32_t Hkv, int32_t topk, int32_t nblk) {
+  if (T < 0 || Hkv <= 0 || topk <= 0 || nblk <= 0) return 0;
+  return msa::prefill_ws_layout(T, Hkv, topk, nblk, 1, false).total;
 }
 
 int msa_prefill_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
@@ -332,17 +339,22 @@ int msa_prefill_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t
     return fail(MSA_ERR_ARG, "msa_prefill_bucket: T=%d Hkv=%d topk=%d nblk=%d", T, Hkv, topk, nblk);
   if ((int64_t)T * Hkv * topk > kInt32Max)
     return fail(MSA_ERR_UNSUPPORTED, "msa_prefill_bucket: T*Hkv*topk exceeds int32");
-  const size_t need = msa_prefill_bucket_workspace_size(Hkv, nblk);
+  if (T == 0)  // every list is empty
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)Hkv * (nblk + 1),
+                                       as_stream(stream)),
+                       "msa_prefill_bucket");
+  const size_t need = msa_prefill_bucket_workspace_size(T, Hkv, topk, nblk);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(MSA_ERR_WORKSPACE, "msa_prefill_bucket: workspace of %zu bytes (need %zu)",
                 workspace_bytes, need);
-  const msa::PrefillWorkspace W = msa::prefill_ws_layout(0, Hkv, 1, nblk, 1, false);
+  const msa::PrefillWorkspace W = msa::prefill_ws_layout(T, Hkv, topk, nblk, 1, false);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return cuda_status(
-      msa::launch_bucket(block_ids, T, Hkv, topk, nblk, T > 0 ? T : 1, 128, offsets, entries,
+      msa::launch_bucket(block_ids, T, Hkv, topk, nblk, T, 128, offsets, entries,
                          reinterpret_cast<int32_t*>(ws + W.counts),
                          reinterpret_cast<int32_t*>(ws + W.group_base),
-                         reinterpret_cast<int32_t*>(ws + W.tile_offsets), as_stream(stream)),
+                         reinterpret_cast<int32_t*>(ws + W.tile_offsets),
+                         reinterpret_cast<int32_t*>(ws + W.epos), as_stream(stream)),
       "msa_prefill_bucket");
 }
 
@@ -363,8 +375,9 @@ int msa_lse_merge(const void* o_parts, int32_t parts_bf16, const float* lse_part
 // a caller workspace
 //
 // Scratch of msa_index_score_topk_noalloc: one fixed array in device memory, created when
-// the library is loaded on a device and held until the process exits. Host code only sees a
-// host-side stand-in for it, so its device address is looked up once per device (below).
+// the library's module is first used on a device (CUDA loads modules lazily) and held until
+// the process exits or the device is reset. Host code only sees a host-side stand-in for it,
+// so its device address is looked up per device (below).
 static __device__ __align__(256) unsigned char g_noalloc_score_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -372,15 +385,21 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, resolved on first use.
-int noalloc_scratch(void** out) {
+// Device address of the scratch array on the current device. It is resolved on the first
+// call on a device, and again on every call whose stream is not being captured: a device
+// reset (cudaDeviceReset) unloads the module, and the array may sit elsewhere once the module
+// is loaded again. During a capture the address cached by the last call outside one is used.
+int noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e, "msa_index_score_topk_noalloc: cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return fail(MSA_ERR_UNSUPPORTED, "msa_index_score_topk_noalloc: device %d", dev);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_status(e, "msa_index_score_topk_noalloc: cudaStreamIsCapturing");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_score_scratch);
     if (e != cudaSuccess || !p)
@@ -407,7 +426,7 @@ int msa_index_score_topk_noalloc(const uint16_t* q_idx, const uint16_t* k_idx_pa
                 "msa_index_score_topk with a workspace instead",
                 need, (size_t)MSA_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
-  const int rc = noalloc_scratch(&scratch);
+  const int rc = noalloc_scratch(as_stream(stream), &scratch);
   if (rc != MSA_OK) return rc;
   // Same checks, kernels and per-call clearing of the ticket counters as the workspace
   // entry point; the scratch array simply stands in for the workspace.

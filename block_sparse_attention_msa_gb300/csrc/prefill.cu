@@ -34,30 +34,11 @@ namespace msa {
 namespace {
 
 // ------------------------------------------------------------------------------ bucketing
-// Rows are (query, group) pairs, row = t*Hkv + g; the host checks that T*Hkv*topk fits in
-// int32, so row and entry arithmetic is 32-bit. List indices ((g*nwin + t/win)*nblk + j) stay
-// 64-bit.
-
-// One thread per (query, group) row: counts every valid selection into its list.
-__global__ void bucket_count_kernel(const int32_t* __restrict__ block_ids, int32_t rows,
-                                    int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
-                                    int32_t nwin, int32_t* __restrict__ counts) {
-  for (int32_t row = blockIdx.x * blockDim.x + threadIdx.x; row < rows;
-       row += gridDim.x * blockDim.x) {
-    const int32_t t = row / Hkv;
-    const int32_t g = row - t * Hkv;
-    const int64_t list0 = ((int64_t)g * nwin + t / win) * nblk;
-    for (int s = 0; s < topk; ++s) {
-      const int32_t j = block_ids[row * topk + s];
-      if (j < 0) continue;
-      if (j >= nblk) {
-        msa_record_error(kErrBadBlock);
-        continue;
-      }
-      atomicAdd(&counts[list0 + j], 1);
-    }
-  }
-}
+// The selections were counted into their lists by the selection kernel (prefill_dense.cu),
+// which also kept each selection's place in its list (epos). Two kernels finish the lists:
+// offsets per (group, window) segment with the tile descriptors, then the placement of every
+// entry at its list's offset plus its place, with no atomics. Rows are (query, group) pairs,
+// row = t*Hkv + g; the host checks that T*Hkv*topk fits in int32.
 
 // Block-wide exclusive scan of one int per thread; returns the block total via *total.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -88,16 +69,58 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return out;
 }
 
-// One CTA per (group, window) segment: exclusive offsets of the segment's lists, the
-// segment-local tile prefix (tiles of `qpt` queries per list) with the segment totals at
-// index nblk, and counts reset to zero for the scatter.
-__global__ void __launch_bounds__(1024)
-    bucket_scan_kernel(int32_t* __restrict__ counts, int32_t nblk, int32_t qpt,
-                       int32_t* __restrict__ offsets, int32_t* __restrict__ tile_local) {
+constexpr int kListThreads = 1024;
+
+// One CTA per (group, window) segment. Every CTA sums the counts of all segments (a few
+// thousand lists) to find its own segment's first entry and first tile, so no CTA waits for
+// another; then it scans its own lists: offsets (relative to the segment) and tiles of `qpt`
+// queries, and writes one descriptor (list, first entry, valid queries) per tile when `desc`
+// is given. CTA 0 also writes the grand totals at index nseg.
+__global__ void __launch_bounds__(kListThreads)
+    bucket_lists_kernel(const int32_t* __restrict__ counts, int32_t nseg, int32_t nblk,
+                        int32_t qpt, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ tile_local, int32_t* __restrict__ group_base,
+                        int32_t* __restrict__ seg_tile_base, int4* __restrict__ desc) {
+  extern __shared__ int32_t seg_tot[];  // [2 * nseg]: entries, tiles per segment
   __shared__ int warp_sums[33];
-  const int seg = blockIdx.x;
+  __shared__ int32_t s_base[2];
+  const int seg = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int sg = warp; sg < nseg; sg += kListThreads / 32) {
+    int c = 0, t = 0;
+    for (int j = lane; j < nblk; j += 32) {
+      const int v = counts[(int64_t)sg * nblk + j];
+      c += v;
+      t += (v + qpt - 1) / qpt;
+    }
+    c = __reduce_add_sync(0xffffffffu, c);
+    t = __reduce_add_sync(0xffffffffu, t);
+    if (lane == 0) {
+      seg_tot[sg] = c;
+      seg_tot[nseg + sg] = t;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bc = 0, bt = 0, ac = 0, at = 0;
+    for (int sg = 0; sg < nseg; ++sg) {
+      if (sg == seg) {
+        bc = ac;
+        bt = at;
+      }
+      ac += seg_tot[sg];
+      at += seg_tot[nseg + sg];
+    }
+    s_base[0] = bc;
+    s_base[1] = bt;
+    group_base[seg] = bc;
+    seg_tile_base[seg] = bt;
+    if (seg == 0) {
+      group_base[nseg] = ac;
+      seg_tile_base[nseg] = at;
+    }
+  }
   int carry = 0, tile_carry = 0;
-  for (int j0 = 0; j0 < nblk; j0 += blockDim.x) {
+  for (int j0 = 0; j0 < nblk; j0 += kListThreads) {
     const int j = j0 + threadIdx.x;
     const int c = j < nblk ? counts[(int64_t)seg * nblk + j] : 0;
     const int nt = (c + qpt - 1) / qpt;
@@ -107,7 +130,6 @@ __global__ void __launch_bounds__(1024)
     if (j < nblk) {
       offsets[(int64_t)seg * (nblk + 1) + j] = carry + ex_c;
       tile_local[(int64_t)seg * (nblk + 1) + j] = tile_carry + ex_t;
-      counts[(int64_t)seg * nblk + j] = 0;
     }
     carry += tot_c;
     tile_carry += tot_t;
@@ -116,43 +138,26 @@ __global__ void __launch_bounds__(1024)
     offsets[(int64_t)seg * (nblk + 1) + nblk] = carry;
     tile_local[(int64_t)seg * (nblk + 1) + nblk] = tile_carry;
   }
-}
-
-// One CTA: exclusive scan of the segment totals -> entry base per segment (group_base) and
-// tile base per segment; the grand totals at index nseg.
-__global__ void __launch_bounds__(1024)
-    bucket_seg_scan_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_local,
-                           int32_t nseg, int32_t nblk, int32_t* __restrict__ group_base,
-                           int32_t* __restrict__ seg_tile_base) {
-  __shared__ int warp_sums[33];
-  int carry = 0, tile_carry = 0;
-  for (int s0 = 0; s0 < nseg; s0 += blockDim.x) {
-    const int sg = s0 + threadIdx.x;
-    const int c = sg < nseg ? offsets[(int64_t)sg * (nblk + 1) + nblk] : 0;
-    const int t = sg < nseg ? tile_local[(int64_t)sg * (nblk + 1) + nblk] : 0;
-    int tot_c, tot_t;
-    const int ex_c = block_exclusive_scan(c, warp_sums, &tot_c);
-    const int ex_t = block_exclusive_scan(t, warp_sums, &tot_t);
-    if (sg < nseg) {
-      group_base[sg] = carry + ex_c;
-      seg_tile_base[sg] = tile_carry + ex_t;
-    }
-    carry += tot_c;
-    tile_carry += tot_t;
-  }
-  if (threadIdx.x == 0) {
-    group_base[nseg] = carry;
-    seg_tile_base[nseg] = tile_carry;
+  if (!desc) return;
+  __syncthreads();  // this CTA's offsets are visible to all its threads
+  // one warp per list, lanes over the list's tiles
+  for (int j = warp; j < nblk; j += kListThreads / 32) {
+    const int32_t* off = offsets + (int64_t)seg * (nblk + 1) + j;
+    const int32_t* tl = tile_local + (int64_t)seg * (nblk + 1) + j;
+    const int first = s_base[0] + off[0], lcnt = off[1] - off[0];
+    const int t0 = s_base[1] + tl[0], nt = tl[1] - tl[0];
+    for (int q = lane; q < nt; q += 32)
+      desc[t0 + q] = make_int4(seg * nblk + j, first + q * qpt, min(qpt, lcnt - q * qpt), 0);
   }
 }
 
-// One thread per (query, group) row: places each valid selection (t, slot) at its list's next
-// free entry.
-__global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int32_t rows,
-                                      int32_t Hkv, int32_t topk, int32_t nblk, int32_t win,
-                                      int32_t nwin, const int32_t* __restrict__ offsets,
-                                      const int32_t* __restrict__ group_base,
-                                      int32_t* __restrict__ cursor, int32_t* __restrict__ entries) {
+// One thread per (query, group) row: each counted selection (t, slot) goes to its list's first
+// entry plus its place in the list.
+__global__ void bucket_place_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ epos,
+                                    int32_t rows, int32_t Hkv, int32_t topk, int32_t nblk,
+                                    int32_t win, int32_t nwin, const int32_t* __restrict__ offsets,
+                                    const int32_t* __restrict__ group_base,
+                                    int32_t* __restrict__ entries) {
   for (int32_t row = blockIdx.x * blockDim.x + threadIdx.x; row < rows;
        row += gridDim.x * blockDim.x) {
     const int32_t t = row / Hkv;
@@ -160,33 +165,12 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ block_ids, int
     const int64_t seg = (int64_t)g * nwin + t / win;  // (group, window) segment
     const int32_t base = group_base[seg];
     const int32_t* off = offsets + seg * (nblk + 1);
-    int32_t* cur = cursor + seg * nblk;
     for (int s = 0; s < topk; ++s) {
-      const int32_t j = block_ids[(int64_t)row * topk + s];
+      const int32_t j = ids[row * topk + s];
       if (j < 0 || j >= nblk) continue;
-      entries[base + off[j] + atomicAdd(&cur[j], 1)] = t * topk + s;
+      entries[base + off[j] + epos[row * topk + s]] = t * topk + s;
     }
   }
-}
-
-// Compact descriptor of every work tile: (list, first entry, valid queries). One warp per
-// list; lanes over the list's tiles. nseg = number of (group, window) segments.
-__global__ void __launch_bounds__(256)
-    tile_desc_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ group_base,
-                     const int32_t* __restrict__ tile_local,
-                     const int32_t* __restrict__ seg_tile_base, int32_t nseg, int32_t nblk,
-                     int32_t qpt, int4* __restrict__ desc) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gj = blockIdx.x * 8 + warp;
-  if (gj >= nseg * nblk) return;
-  const int seg = gj / nblk, j = gj % nblk;
-  const int32_t* off = offsets + (int64_t)seg * (nblk + 1) + j;
-  const int lbeg = off[0], lcnt = off[1] - off[0];
-  const int first = group_base[seg] + lbeg;
-  const int32_t* tl = tile_local + (int64_t)seg * (nblk + 1) + j;
-  const int t0 = seg_tile_base[seg] + tl[0], nt = tl[1] - tl[0];
-  for (int c = lane; c < nt; c += 32)
-    desc[t0 + c] = make_int4(gj, first + c * qpt, min(qpt, lcnt - c * qpt), 0);
 }
 
 // ------------------------------------------------------------------------------ attention
@@ -453,13 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               continue;
             }
           }
-          // ---- S(si): needs O(si-2) issued and completed, its queries and its K/V block
+          // ---- S(si): needs O(si-2) issued (this warp issues in order, and the tensor pipe runs
+          // one thread's MMAs in issue order, so O(si-2) has read P(si-2) before S(si) writes
+          // there; the commit that signals S(si) covers O(si-2)), its queries and its K/V block
           if (si < n && oi >= si - 1) {
             const int b = si & 1, qs = si % kQStages;
             const bool kv_new = next_gj != kv_gj;
             if ((!kv_new || ready(&B.kv_full[kv_loads & 1], (kv_loads >> 1) & 1)) &&
-                ready(&B.q_full[qs], (si / kQStages) & 1) &&
-                (si < 2 || ready(&B.o_full[b], ((si - 2) >> 1) & 1))) {
+                ready(&B.q_full[qs], (si / kQStages) & 1)) {
               tmem_fence_after();
               if (kv_new) {
                 ++kv_loads;
@@ -540,7 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // causal mask: key j*128 + col is visible to the query iff it is <= the query position
       const int64_t qpos = ent >= 0 ? p.q_start + ent / p.topk : -1;
       const int64_t lim64 = qpos - (int64_t)j * 128;  // last visible column
-      if (lim64 < 127) {
+      // an empty query slot of the tile gets P = 0 through its exponent (scale 0, offset -inf)
+      if (ent >= 0 && lim64 < 127) {
         const int lim = lim64 < -1 ? -1 : (int)lim64;
 #pragma unroll
         for (int x = 0; x < 128; ++x)
@@ -550,13 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
       for (int x = 4; x < 128; x += 2) m4[(x >> 1) & 3] = max3(m4[(x >> 1) & 3], v[x], v[x + 1]);
-      const float mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+      const float mx = ent >= 0 ? fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]) : -INFINITY;
       const float mscaled = (mx == -INFINITY ? 0.f : mx) * kLog2e;
+      const float sc = ent >= 0 ? kLog2e : 0.f;
+      const float off = ent >= 0 ? -mscaled : -INFINITY;
       // p = 2^(s*log2e - max*log2e): the scaling in packed pairs, the exponent on the SFU
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int x = 0; x < 128; x += 2) {
-        fma2(v[x], v[x + 1], v[x], v[x + 1], kLog2e, kLog2e, -mscaled, -mscaled);
+        fma2(v[x], v[x + 1], v[x], v[x + 1], sc, sc, off, off);
         v[x] = ex2(v[x]);
         v[x + 1] = ex2(v[x + 1]);
         add2(l8[(x >> 1) & 3], l8[4 + ((x >> 1) & 3)], v[x], v[x + 1]);
@@ -618,28 +606,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
-                          int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,
-                          int32_t* entries, int32_t* counts, int32_t* group_base,
-                          int32_t* tile_offsets, cudaStream_t stream) {
-  const int32_t nwin = (T + win - 1) / win > 0 ? (T + win - 1) / win : 1;
+cudaError_t launch_bucket_lists(const int32_t* ids, const int32_t* epos, int32_t T, int32_t Hkv,
+                                int32_t topk, int32_t nblk, int32_t win, int32_t qpt,
+                                const int32_t* counts, int32_t* offsets, int32_t* entries,
+                                int32_t* group_base, int32_t* tile_offsets, int4* desc,
+                                cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const int32_t nwin = (T + win - 1) / win;
   const int32_t nseg = Hkv * nwin;  // (group, window) segments
-  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)nseg * nblk, stream);
-  if (e != cudaSuccess) return e;
-  const int32_t rows = T * Hkv;  // T*Hkv*topk fits in int32 (checked by the callers)
-  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)sm_count() * 8));
-  bucket_count_kernel<<<rgrid, 256, 0, stream>>>(block_ids, rows, Hkv, topk, nblk, win, nwin,
-                                                 counts);
   // tile_offsets holds the segment-local tile prefix [nseg][nblk+1], then the segment tile
   // bases [nseg+1]
   int32_t* tile_local = tile_offsets;
   int32_t* seg_tile_base = tile_offsets + (size_t)nseg * (nblk + 1);
-  bucket_scan_kernel<<<nseg, 1024, 0, stream>>>(counts, nblk, qpt, offsets, tile_local);
-  bucket_seg_scan_kernel<<<1, 1024, 0, stream>>>(offsets, tile_local, nseg, nblk, group_base,
-                                                 seg_tile_base);
-  bucket_scatter_kernel<<<rgrid, 256, 0, stream>>>(block_ids, rows, Hkv, topk, nblk, win, nwin,
-                                                   offsets, group_base, counts, entries);
+  const size_t smem = 8 * (size_t)nseg;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(bucket_lists_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  bucket_lists_kernel<<<nseg, kListThreads, smem, stream>>>(counts, nseg, nblk, qpt, offsets,
+                                                            tile_local, group_base, seg_tile_base,
+                                                            desc);
+  const int32_t rows = T * Hkv;  // T*Hkv*topk fits in int32 (checked by the callers)
+  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)sm_count() * 8));
+  bucket_place_kernel<<<rgrid, 256, 0, stream>>>(ids, epos, rows, Hkv, topk, nblk, win, nwin,
+                                                 offsets, group_base, entries);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
+                          int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,
+                          int32_t* entries, int32_t* counts, int32_t* group_base,
+                          int32_t* tile_offsets, int32_t* epos, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const int32_t nwin = (T + win - 1) / win;
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)Hkv * nwin * nblk, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_select_count(block_ids, T, (int64_t)nblk * 128, Hkv, 1, topk, nblk, win,
+                          DenseWorkspace{}, counts, epos, stream);
+  if (e != cudaSuccess) return e;
+  return launch_bucket_lists(block_ids, epos, T, Hkv, topk, nblk, win, qpt, counts, offsets,
+                             entries, group_base, tile_offsets, nullptr, stream);
 }
 
 cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
@@ -654,6 +661,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   uint16_t* part_o = reinterpret_cast<uint16_t*>(a.workspace + W.part_o);
   float* part_lse = reinterpret_cast<float*>(a.workspace + W.part_lse);
   int4* tile_desc = reinterpret_cast<int4*>(a.workspace + W.tile_desc);
+  int32_t* epos = reinterpret_cast<int32_t*>(a.workspace + W.epos);
   const int32_t win = prefill_window(a.T, a.nblk, a.topk, G);
   const int32_t nwin = prefill_nwin(a.T, a.nblk, a.topk, G);
   // G 8 / 16: the slots shared by many queries of a query pair are computed query-major; the
@@ -661,7 +669,6 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const bool hybrid = prefill_hybrid(G);
   DenseWorkspace dw{};
   const int32_t* ids = a.block_ids;
-  cudaError_t e = cudaSuccess;
   if (hybrid) {
     dw.qperm = reinterpret_cast<int32_t*>(a.workspace + W.qperm);
     dw.residual = reinterpret_cast<int32_t*>(a.workspace + W.residual);
@@ -670,12 +677,17 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
     dw.dmask = reinterpret_cast<uint32_t*>(a.workspace + W.dmask);
     dw.part_o = reinterpret_cast<uint16_t*>(a.workspace + W.dense_o);
     dw.part_lse = reinterpret_cast<float*>(a.workspace + W.dense_lse);
-    e = launch_dense_select(a.block_ids, a.T, a.S_kv, a.Hkv, G, a.topk, dw, stream);
-    if (e != cudaSuccess) return e;
     ids = dw.residual;
   }
-  e = launch_bucket(ids, a.T, a.Hkv, a.topk, a.nblk, win, qpt,
-                                offsets, entries, counts, group_base, tile_offsets, stream);
+  // (a) selection (query order, shared blocks) and the count of the block-major selections in
+  // one kernel; the lists' offsets with the tile descriptors; the placement of the entries
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)a.Hkv * nwin * a.nblk, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_select_count(a.block_ids, a.T, a.S_kv, a.Hkv, G, a.topk, a.nblk, win, dw, counts,
+                          epos, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_bucket_lists(ids, epos, a.T, a.Hkv, a.topk, a.nblk, win, qpt, counts, offsets,
+                          entries, group_base, tile_offsets, tile_desc, stream);
   if (e != cudaSuccess) return e;
 
   CUtensorMap qmap, kmap, vmap;
@@ -701,12 +713,6 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
       !encode_bf16_map(&kmap, a.k, 3, dims, strides, box, true) ||
       !encode_bf16_map(&vmap, a.v, 3, dims, strides, box, true))
     return cudaErrorInvalidValue;
-  const int32_t nseg = a.Hkv * nwin;
-  tile_desc_kernel<<<(unsigned)((nseg * a.nblk + 7) / 8), 256, 0, stream>>>(
-      offsets, group_base, tile_offsets, tile_offsets + (size_t)nseg * (a.nblk + 1), nseg, a.nblk,
-      qpt, tile_desc);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   PreKParams p;
   p.entries = entries;
   p.desc = tile_desc;

@@ -41,13 +41,11 @@ namespace msa {
 namespace {
 
 // ------------------------------------------------------------------------------ selection
-constexpr int kSelThreads = 256;
-// One CTA per pair of 128/G-query tiles (nq = 2*128/G <= 32 consecutive queries of group g).
-// The ids a pair can choose are at most the local block of its last query (nb blocks); they are
-// counted in windows of hw <= kHistBlocks blocks (hw: the chunk's block count, capped): a query
-// mask per block in shared memory, filled with
-// shared atomics (a block's count is its mask's popcount: a query chooses a block at most once),
-// then a prefix scan over the window ranks the dense blocks in ascending order.
+// The ids a pair can choose are at most the local block of its span's last query (nb blocks);
+// they are counted in windows of hw <= kHistBlocks blocks (hw: the chunk's block count, capped):
+// a query mask per block in shared memory, filled with shared atomics (a block's count is its
+// mask's popcount: a query chooses a block at most once), then a prefix scan over the window
+// ranks the dense blocks in ascending order.
 constexpr int kHistBlocks = 16384;
 
 // Query of pair slot `pos` of group g (-1: past the chunk). Without an order, slot = query.
@@ -58,132 +56,322 @@ __device__ __forceinline__ int64_t slot_query(const int32_t* qperm, int64_t npos
 }
 
 constexpr int kSpan = 128;
-// One CTA per (128-query span, group): block counts of the span's selections in shared memory
-// (nb_max = blocks of the whole key range), each query's number of selections among the blocks
-// chosen by at least half of the span's queries, then a stable rank by that number descending.
-__global__ void __launch_bounds__(kSpan)
-    pair_order_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv,
-                      int32_t topk, int32_t nb_max, int64_t npos, int32_t* __restrict__ qperm) {
-  extern __shared__ uint32_t span_cnt[];  // [nb_max]
-  __shared__ int32_t score[kSpan];
-  const int r = threadIdx.x;
-  const int g = (int)(blockIdx.x % Hkv);
-  const int64_t span = blockIdx.x / Hkv;
-  const int64_t t = span * kSpan + r;
-  const bool valid = t < T;
-  const int nvalid = (int)min((int64_t)kSpan, (int64_t)T - span * kSpan);
-  for (int j = r; j < nb_max; j += kSpan) span_cnt[j] = 0u;
-  __syncthreads();
-  const int32_t* sel = block_ids + (t * Hkv + g) * topk;
-  if (valid)
-    for (int k = 0; k < topk; ++k) {
-      const int32_t j = sel[k];
-      if (j >= 0 && j < nb_max) atomicAdd(&span_cnt[j], 1u);
-    }
-  __syncthreads();
-  int sc = -1;  // slots past the chunk sort last
-  if (valid) {
-    sc = 0;
-    for (int k = 0; k < topk; ++k) {
-      const int32_t j = sel[k];
-      if (j >= 0 && j < nb_max && 2 * (int)span_cnt[j] >= nvalid) ++sc;
-    }
-  }
-  score[r] = sc;
-  __syncthreads();
-  int rank = 0;
-  for (int q = 0; q < kSpan; ++q) {
-    const int s2 = score[q];
-    rank += (s2 > sc || (s2 == sc && q < r)) ? 1 : 0;
-  }
-  qperm[(int64_t)g * npos + span * kSpan + rank] = valid ? (int32_t)t : -1;
-}
 
-__global__ void __launch_bounds__(kSelThreads)
-    dense_select_kernel(const int32_t* __restrict__ block_ids, int32_t T, int32_t Hkv, int32_t G,
-                        int32_t topk, int32_t qpt, int32_t ppg, int32_t thr, int64_t q_start,
-                        int32_t hw, const int32_t* __restrict__ qperm, int64_t npos,
-                        int32_t* __restrict__ residual, int32_t* __restrict__ dcnt,
-                        int32_t* __restrict__ dblk, uint32_t* __restrict__ dmask,
-                        float* __restrict__ part_lse) {
-  extern __shared__ __align__(16) uint8_t hist_smem[];
-  uint32_t* msk = reinterpret_cast<uint32_t*>(hist_smem);          // [hw]
-  int16_t* rnk = reinterpret_cast<int16_t*>(hist_smem + 4 * hw);   // [hw] dense rank or -1
-  __shared__ int32_t warp_sum[kSelThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t pair = blockIdx.x;
-  const int g = (int)(pair / ppg);
-  const int64_t t0 = (pair % ppg) * 2 * qpt;  // first pair slot
-  const int nq = 2 * qpt, n = nq * topk;
-  // the pair's queries lie in the 128-query span of its slots
-  const int64_t t_last = min((int64_t)T - 1, qperm ? t0 / kSpan * kSpan + kSpan - 1 : t0 + nq - 1);
-  const int64_t nb = (q_start + t_last) / 128 + 1;  // blocks the pair can have chosen
-  for (int r = tid; r < nq * G; r += kSelThreads) {
-    const int64_t t = slot_query(qperm, npos, g, t0 + r / G, T);
-    if (t >= 0) part_lse[(t * Hkv + g) * G + r % G] = -INFINITY;
+struct SelectParams {
+  const int32_t* block_ids;  // [T, Hkv, topk]
+  int32_t T, Hkv, topk;
+  int64_t q_start;
+  // query-major selection (G 8 / 16)
+  bool hybrid, ordered;
+  int32_t nb_max;            // blocks of the whole key range (ordering histogram)
+  int32_t qpt, ppg, thr, hw;
+  int64_t npos;
+  int32_t* qperm;            // [Hkv, npos]
+  int32_t* residual;         // [T, Hkv, topk]
+  int32_t* dcnt;             // [pairs]
+  int32_t* dblk;             // [pairs, kMaxDense]
+  uint32_t* dmask;           // [pairs, kMaxDense]
+  float* part_lse;           // [T*Hkv*G] query-major LSE, -inf until written
+  int32_t G;
+  // bucketing of the remaining (block-major) selections
+  int32_t nblk, win, nwin;
+  int32_t ph;                // per-warp pair histogram length (0: windowed CTA-wide selection)
+  int32_t* counts;           // [Hkv*nwin, nblk], zero on entry
+  int32_t* epos;             // [T, Hkv, topk]: place of each counted selection in its list
+};
+
+// Blocks per pair histogram for the one-warp-per-pair selection (smaller key ranges); longer
+// key ranges take the CTA-wide windowed selection.
+constexpr int kPairHist = 1024;
+
+// One CTA per (group g, 128-query span), one thread per query of the span. The span's ids are
+// staged in shared memory once.
+//  (o) [hybrid, ordered] the span's block histogram; each query's number of selections among
+//      the blocks chosen by at least half of the span; a stable rank by that number descending
+//      gives the slot order (qperm): consecutive slots form the pairs of 2*128/G queries.
+//  (a) [hybrid] per pair of the span: the blocks chosen by at least half of the pair's queries
+//      (at most kMaxDense, ascending) with a query bit mask each; the pair's selections of those
+//      blocks are replaced by -1 in `residual`. One warp per pair (key ranges of at most
+//      kPairHist blocks), else the whole CTA per pair in windows of hw blocks.
+//  (c) each remaining selection (t, slot) of block j is counted into list (g, t/win, j), and its
+//      place in that list is kept in `epos` (the bucketing places it there once the lists'
+//      offsets are known).
+__global__ void __launch_bounds__(kSpan)
+    select_count_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  __shared__ __align__(16) int32_t score[kSpan];
+  __shared__ int32_t s_query[kSpan];   // query of each slot of the span (-1: none)
+  __shared__ int16_t s_row[kSpan];     // span row (t - span start) of each slot
+  __shared__ int32_t warp_sum[kSpan / 32];
+  const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+  const int g = (int)(blockIdx.x % p.Hkv);
+  const int64_t span = blockIdx.x / p.Hkv;
+  const int64_t t_me = span * kSpan + r;
+  const bool valid = t_me < p.T;
+  const int nvalid = (int)min((int64_t)kSpan, (int64_t)p.T - span * kSpan);
+  const int64_t row_me = t_me * p.Hkv + g;
+  if (!p.hybrid) {
+    // (c) only: count the selections of this thread's query
+    if (!valid) return;
+    const int64_t list0 = ((int64_t)g * p.nwin + t_me / p.win) * p.nblk;
+    for (int k = 0; k < p.topk; ++k) {
+      const int32_t j = p.block_ids[row_me * p.topk + k];
+      if (j < 0) continue;
+      if (j >= p.nblk) {
+        msa_record_error(kErrBadBlock);
+        continue;
+      }
+      p.epos[row_me * p.topk + k] = atomicAdd(&p.counts[list0 + j], 1);
+    }
+    return;
   }
-  int ranked = 0;  // dense blocks ranked in earlier windows
-  for (int64_t base = 0; base < nb; base += hw) {
-    const int w = (int)min((int64_t)hw, nb - base);
-    for (int j = tid; j < w; j += kSelThreads) msk[j] = 0u;
+  // the span's selections [topk][kSpan] (slot-major: a warp's rows fall in distinct banks;
+  // residuals are written over them in (a)), then the histograms of (o) and (a)
+  int32_t* s_ids = reinterpret_cast<int32_t*>(sel_smem);
+  uint8_t* hist = sel_smem + (size_t)kSpan * p.topk * 4;
+  for (int k = 0; k < p.topk; ++k)
+    s_ids[k * kSpan + r] = valid ? p.block_ids[row_me * p.topk + k] : -1;
+  // ---------------- (o) slot order of the span
+  if (p.ordered) {
+    uint32_t* span_cnt = reinterpret_cast<uint32_t*>(hist);  // [nb_max]
+    for (int j = r; j < p.nb_max; j += kSpan) span_cnt[j] = 0u;
     __syncthreads();
-    for (int e = tid; e < n; e += kSelThreads) {
-      const int q = e / topk;
-      const int64_t t = slot_query(qperm, npos, g, t0 + q, T);
-      if (t < 0) continue;
-      const int64_t id = block_ids[(t * Hkv + g) * topk + e % topk];
-      if (id >= base && id < base + w) atomicOr(&msk[id - base], 1u << q);
+    for (int k = 0; k < p.topk; ++k) {
+      const int32_t j = s_ids[k * kSpan + r];
+      if (j >= 0 && j < p.nb_max) atomicAdd(&span_cnt[j], 1u);
     }
     __syncthreads();
-    const int per = (w + kSelThreads - 1) / kSelThreads;
-    const int j0 = tid * per, j1 = min(w, j0 + per);
-    int local = 0;
-    for (int j = j0; j < j1; ++j) local += __popc(msk[j]) >= thr ? 1 : 0;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    int sc = -1;  // slots past the chunk sort last
+    if (valid) {
+      sc = 0;
+      for (int k = 0; k < p.topk; ++k) {
+        const int32_t j = s_ids[k * kSpan + r];
+        if (j >= 0 && j < p.nb_max && 2 * (int)span_cnt[j] >= nvalid) ++sc;
+      }
     }
-    if (lane == 31) warp_sum[warp] = incl;
+    score[r] = sc;
     __syncthreads();
-    int rank = ranked + incl - local, total = 0;
-    for (int v = 0; v < kSelThreads / 32; ++v) {
-      if (v < warp) rank += warp_sum[v];
-      total += warp_sum[v];
+    int rank = 0;
+#pragma unroll 4
+    for (int q = 0; q < kSpan; q += 4) {
+      const int4 s4 = *reinterpret_cast<const int4*>(score + q);
+      rank += (s4.x > sc || (s4.x == sc && q < r)) ? 1 : 0;
+      rank += (s4.y > sc || (s4.y == sc && q + 1 < r)) ? 1 : 0;
+      rank += (s4.z > sc || (s4.z == sc && q + 2 < r)) ? 1 : 0;
+      rank += (s4.w > sc || (s4.w == sc && q + 3 < r)) ? 1 : 0;
     }
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t m = msk[j];
-      int16_t rk = -1;
-      if (__popc(m) >= thr) {
-        if (rank < kMaxDense) {
-          dblk[pair * kMaxDense + rank] = (int32_t)(base + j);
-          dmask[pair * kMaxDense + rank] = m;
+    s_query[rank] = valid ? (int32_t)t_me : -1;
+    s_row[rank] = (int16_t)r;
+    p.qperm[(int64_t)g * p.npos + span * kSpan + rank] = valid ? (int32_t)t_me : -1;
+  } else {
+    s_query[r] = valid ? (int32_t)t_me : -1;
+    s_row[r] = (int16_t)r;
+  }
+  __syncthreads();  // slot order and staged ids (the histogram space is reused below)
+  // ---------------- (a) shared blocks of each pair of the span
+  const int nq = 2 * p.qpt;
+  const int pairs = kSpan / nq;
+  const int64_t nb = (p.q_start + span * kSpan + nvalid - 1) / 128 + 1;  // blocks the span sees
+  for (int rr = r; rr < kSpan * p.G; rr += kSpan) {
+    const int32_t t = s_query[rr / p.G];
+    if (t >= 0) p.part_lse[((int64_t)t * p.Hkv + g) * p.G + rr % p.G] = -INFINITY;
+  }
+  if (p.ph > 0 && nb <= p.ph) {
+    // one warp per pair (pairs of 32 slots) or per two pairs (16 slots): lane = slot of the pair
+    const int ppw = pairs / (kSpan / 32);  // pairs per warp: 1 or 2
+    uint32_t* msk = reinterpret_cast<uint32_t*>(hist) + warp * p.ph;
+    int16_t* rnk = reinterpret_cast<int16_t*>(hist + (kSpan / 32) * p.ph * 4) + warp * p.ph;
+    for (int i = 0; i < ppw; ++i) {
+      const int pi = warp * ppw + i;  // pair within the span
+      const int64_t pslot = span * pairs + pi;
+      const bool live = pslot < p.ppg;  // uniform for the warp
+      if (!live) break;
+      const int64_t pair = (int64_t)g * p.ppg + pslot;
+      for (int j = lane; j < nb; j += 32) msk[j] = 0u;
+      __syncwarp();
+      const bool mine = lane < nq;
+      const int slot = pi * nq + lane;
+      const int srow = mine ? s_row[slot] : 0;
+      const bool qv = mine && s_query[slot] >= 0;
+      if (qv)
+        for (int k = 0; k < p.topk; ++k) {
+          const int32_t id = s_ids[k * kSpan + srow];
+          if (id >= 0 && id < nb) atomicOr(&msk[id], 1u << lane);
+        }
+      __syncwarp();
+      // ascending ranks of the dense blocks, 32 blocks per step
+      int ranked = 0;
+      for (int j0 = 0; j0 < nb; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t m = j < nb ? msk[j] : 0u;
+        const bool dense = __popc(m) >= p.thr;
+        const uint32_t bal = __ballot_sync(0xffffffffu, dense);
+        const int rank = ranked + __popc(bal & ((1u << lane) - 1u));
+        int16_t rk = -1;
+        if (dense && rank < kMaxDense) {
+          p.dblk[pair * kMaxDense + rank] = j;
+          p.dmask[pair * kMaxDense + rank] = m;
           rk = (int16_t)rank;
         }
-        ++rank;
+        if (j < nb) rnk[j] = rk;
+        ranked += __popc(bal);
       }
-      rnk[j] = rk;
+      if (lane == 0) p.dcnt[pair] = ranked < kMaxDense ? ranked : kMaxDense;
+      __syncwarp();
+      // the pair's residual selections: the dense ones leave, the others stay
+      if (qv)
+        for (int k = 0; k < p.topk; ++k) {
+          const int32_t id = s_ids[k * kSpan + srow];
+          if (id >= 0 && id < nb && rnk[id] >= 0) s_ids[k * kSpan + srow] = -1;
+        }
+      __syncwarp();
     }
-    __syncthreads();
-    // residual selections of this window: the dense ones leave, the others stay; ids outside
-    // every window (negative or past the causal range) are copied once, with the first window
-    for (int e = tid; e < n; e += kSelThreads) {
-      const int q = e / topk;
-      const int64_t t = slot_query(qperm, npos, g, t0 + q, T);
-      if (t < 0) continue;
-      const int64_t at = (t * Hkv + g) * topk + e % topk;
-      const int32_t id = block_ids[at];
-      if (id >= base && id < base + w)
-        residual[at] = rnk[id - base] >= 0 ? -1 : id;
-      else if (base == 0 && (id < 0 || id >= nb))
-        residual[at] = id;
+  } else {
+    uint32_t* msk = reinterpret_cast<uint32_t*>(hist);           // [hw]
+    int16_t* rnk = reinterpret_cast<int16_t*>(hist + 4 * p.hw);  // [hw] dense rank or -1
+    const int n = nq * p.topk;
+    for (int i = 0; i < pairs; ++i) {
+      const int64_t pslot = span * pairs + i;
+      if (pslot >= p.ppg) break;
+      const int64_t pair = (int64_t)g * p.ppg + pslot;
+      int ranked = 0;  // dense blocks ranked in earlier windows
+      for (int64_t base = 0; base < nb; base += p.hw) {
+        const int w = (int)min((int64_t)p.hw, nb - base);
+        for (int j = r; j < w; j += kSpan) msk[j] = 0u;
+        __syncthreads();
+        for (int e = r; e < n; e += kSpan) {
+          const int q = e / p.topk, slot = i * nq + q;
+          if (s_query[slot] < 0) continue;
+          const int64_t id = s_ids[(e % p.topk) * kSpan + s_row[slot]];
+          if (id >= base && id < base + w) atomicOr(&msk[id - base], 1u << q);
+        }
+        __syncthreads();
+        const int per = (w + kSpan - 1) / kSpan;
+        const int j0 = r * per, j1 = min(w, j0 + per);
+        int local = 0;
+        for (int j = j0; j < j1; ++j) local += __popc(msk[j]) >= p.thr ? 1 : 0;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        int rank = ranked + incl - local, total = 0;
+        for (int v = 0; v < kSpan / 32; ++v) {
+          if (v < warp) rank += warp_sum[v];
+          total += warp_sum[v];
+        }
+        for (int j = j0; j < j1; ++j) {
+          const uint32_t m = msk[j];
+          int16_t rk = -1;
+          if (__popc(m) >= p.thr) {
+            if (rank < kMaxDense) {
+              p.dblk[pair * kMaxDense + rank] = (int32_t)(base + j);
+              p.dmask[pair * kMaxDense + rank] = m;
+              rk = (int16_t)rank;
+            }
+            ++rank;
+          }
+          rnk[j] = rk;
+        }
+        __syncthreads();
+        for (int e = r; e < n; e += kSpan) {
+          const int q = e / p.topk, slot = i * nq + q;
+          if (s_query[slot] < 0) continue;
+          int32_t* at = &s_ids[(e % p.topk) * kSpan + s_row[slot]];
+          const int32_t id = *at;
+          if (id >= base && id < base + w && rnk[id - base] >= 0) *at = -1;
+        }
+        ranked += total;
+        __syncthreads();  // the window's arrays are reused by the next window / pair
+      }
+      if (r == 0) p.dcnt[pair] = ranked < kMaxDense ? ranked : kMaxDense;
     }
-    ranked += total;
-    __syncthreads();  // the window's arrays are reused by the next window
   }
-  if (tid == 0) dcnt[pair] = ranked < kMaxDense ? ranked : kMaxDense;
+  __syncthreads();  // every pair's residuals are in s_ids
+  // ---------------- (c) count the remaining selections of this thread's query into their lists
+  if (!valid) return;
+  const int64_t list0 = ((int64_t)g * p.nwin + t_me / p.win) * p.nblk;
+  for (int k = 0; k < p.topk; ++k) {
+    const int32_t j = s_ids[k * kSpan + r];
+    p.residual[row_me * p.topk + k] = j;
+    if (j < 0) continue;
+    if (j >= p.nblk) {
+      msa_record_error(kErrBadBlock);
+      continue;
+    }
+    p.epos[row_me * p.topk + k] = atomicAdd(&p.counts[list0 + j], 1);
+  }
 }
+
+}  // namespace
+
+// Per-warp pair histogram length: the chunk's key blocks, when they are few enough.
+int32_t pair_hist_len(int64_t S_kv) {
+  const int64_t nbk = (S_kv + 127) / 128;
+  return nbk <= kPairHist ? (int32_t)((nbk + 7) / 8 * 8) : 0;
+}
+
+// Shared memory of select_count_kernel: the span's ids, then the larger of the ordering
+// histogram and the pair histograms.
+size_t select_count_smem_bytes(int64_t S_kv, int32_t G, int32_t topk) {
+  const int64_t nbk = (S_kv + 127) / 128;
+  const int64_t hw = std::min<int64_t>(kHistBlocks, nbk);
+  const int64_t nb_max = std::min<int64_t>(nbk, INT32_MAX);
+  if (!prefill_hybrid(G)) return 16;
+  const int32_t ph = pair_hist_len(S_kv);
+  size_t h = ph > 0 ? (size_t)(kSpan / 32) * ph * 6 : (size_t)6 * hw;
+  if (nb_max <= kHistBlocks) h = std::max(h, (size_t)4 * nb_max);
+  return (size_t)kSpan * topk * 4 + (h + 15) / 16 * 16;
+}
+
+cudaError_t launch_select_count(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
+                                int32_t G, int32_t topk, int32_t nblk, int32_t win,
+                                const DenseWorkspace& w, int32_t* counts, int32_t* epos,
+                                cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  SelectParams p{};
+  p.block_ids = block_ids;
+  p.T = T;
+  p.Hkv = Hkv;
+  p.topk = topk;
+  p.q_start = S_kv - T;
+  p.hybrid = prefill_hybrid(G) && w.residual != nullptr;
+  p.G = G;
+  p.qpt = 128 / G;
+  p.ppg = (int32_t)((T + 2 * p.qpt - 1) / (2 * p.qpt));
+  p.thr = std::max(2, (2 * p.qpt + 1) / 2);  // at least half of the pair's queries
+  const int64_t nbk = (S_kv + 127) / 128;
+  // the window covers every block of the chunk when it fits (one pass), else kHistBlocks
+  p.hw = (int32_t)std::min<int64_t>(kHistBlocks, nbk);
+  // pair order: while the key range's block counts fit in shared memory, else slot = query
+  p.nb_max = (int32_t)std::min<int64_t>(nbk, INT32_MAX);
+  p.ordered = p.nb_max <= kHistBlocks;
+  p.npos = prefill_qpos(T);
+  p.qperm = w.qperm;
+  p.residual = w.residual;
+  p.dcnt = w.dcnt;
+  p.dblk = w.dblk;
+  p.dmask = w.dmask;
+  p.part_lse = w.part_lse;
+  p.nblk = nblk;
+  p.win = win;
+  p.nwin = (T + win - 1) / win;
+  p.counts = counts;
+  p.epos = epos;
+  p.ph = pair_hist_len(S_kv);
+  const size_t smem = p.hybrid ? select_count_smem_bytes(S_kv, G, topk) : 16;
+  cudaError_t e = cudaFuncSetAttribute(select_count_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t nspan = (T + kSpan - 1) / kSpan;
+  select_count_kernel<<<(unsigned)(Hkv * nspan), kSpan, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+namespace {
 
 // ------------------------------------------------------------------------------ attention
 constexpr int kThreads = 384;
@@ -459,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int X = oN[0] <= oN[1] ? 0 : 1;
             if (oN[X] < sN[X]) mbar_try_wait_hint(&B.p_full[X], oN[X] & 1, kIssuerNap);
             else __nanosleep(32);
-            // every lane leaves together: the flag is agreed by a vote
+            // every lane leaves together: the flag is agreed by a vote (read now and then: it
+            // is only set when another role's wait has timed out)
             const bool failed = __any_sync(0xffffffffu, *fail != 0);
             if (++idle > kWaitLimit || failed) {
               if (!failed && lane == 0) msa_record_error(kErrTimeout);
@@ -611,42 +800,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-
-cudaError_t launch_dense_select(const int32_t* block_ids, int32_t T, int64_t S_kv, int32_t Hkv,
-                                int32_t G, int32_t topk, const DenseWorkspace& w,
-                                cudaStream_t stream) {
-  const int32_t qpt = 128 / G;
-  const int32_t ppg = (int32_t)((T + 2 * qpt - 1) / (2 * qpt));
-  const int32_t nq = 2 * qpt;
-  const int32_t thr = std::max(2, (nq + 1) / 2);  // at least half of the pair's queries
-  const int64_t npairs = (int64_t)Hkv * ppg;
-  if (npairs <= 0) return cudaSuccess;
-  // the window covers every block of the chunk when it fits (one pass), else kHistBlocks
-  const int32_t hw = (int32_t)std::min<int64_t>(kHistBlocks, (S_kv + 127) / 128);
-  const size_t smem = (6 * (size_t)hw + 15) / 16 * 16;
-  // pair order: while the key range's block counts fit in shared memory, else slot = query
-  const int32_t nb_max = (int32_t)std::min<int64_t>((S_kv + 127) / 128, INT32_MAX);
-  const bool ordered = nb_max <= kHistBlocks;
-  const int64_t npos = prefill_qpos(T);
-  if (ordered) {
-    const size_t osmem = 4 * (size_t)nb_max;
-    cudaError_t e0 = cudaFuncSetAttribute(pair_order_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem);
-    if (e0 != cudaSuccess) return e0;
-    pair_order_kernel<<<(unsigned)(Hkv * (npos / kSpan)), kSpan, osmem, stream>>>(
-        block_ids, T, Hkv, topk, nb_max, npos, w.qperm);
-    e0 = cudaGetLastError();
-    if (e0 != cudaSuccess) return e0;
-  }
-  cudaError_t e = cudaFuncSetAttribute(dense_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dense_select_kernel<<<(unsigned)npairs, kSelThreads, smem, stream>>>(
-      block_ids, T, Hkv, G, topk, qpt, ppg, thr, S_kv - T, hw, ordered ? w.qperm : nullptr, npos,
-      w.residual, w.dcnt, w.dblk, w.dmask,
-      w.part_lse);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,

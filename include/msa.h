@@ -285,9 +285,10 @@ MSA_API int msa_sparse_prefill_paged(const uint16_t* q, const uint16_t* k_cache,
  *
  *   block_ids [T, Hkv, topk] int32; offsets [Hkv, nblk+1] int32 (out);
  *   entries   [T*Hkv*topk] int32 (out; only the first sum-of-totals entries are written)
- *   workspace >= msa_prefill_bucket_workspace_size(Hkv, nblk) bytes (no zero-fill needed)
+ *   workspace >= msa_prefill_bucket_workspace_size(T, Hkv, topk, nblk) bytes (no zero-fill
+ *             needed)
  * ------------------------------------------------------------------------------------ */
-MSA_API size_t msa_prefill_bucket_workspace_size(int32_t Hkv, int32_t nblk);
+MSA_API size_t msa_prefill_bucket_workspace_size(int32_t T, int32_t Hkv, int32_t topk, int32_t nblk);
 
 MSA_API int msa_prefill_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
                        int32_t nblk, int32_t* offsets, int32_t* entries, void* workspace,

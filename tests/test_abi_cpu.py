@@ -43,7 +43,7 @@ def test_workspace_sizes(lib):
     assert lib.msa_index_score_topk_workspace_size(0, 1, 8, 469) == 0
     assert lib.msa_paged_sparse_decode_workspace_size(64, 64, 8, 16) >= 64 * 64 * 4 * 128 * 4
     assert lib.msa_sparse_prefill_workspace_size(32768, 32768, 64, 8, 16) > 32768 * 8 * 16 * 8 * 128 * 2
-    assert lib.msa_prefill_bucket_workspace_size(8, 256) >= 8 * 256 * 4
+    assert lib.msa_prefill_bucket_workspace_size(1000, 8, 16, 256) >= 8 * 256 * 4 + 1000 * 8 * 16 * 4
 
 
 def _err(lib):
