@@ -782,6 +782,356 @@ __global__ void __launch_bounds__(256) topk_rows_kernel(const ScoreArgs a) {
             a.sel_scores ? a.sel_scores + item * a.topk : nullptr, ws[warp]);
 }
 
+// ---------------------------------------------------------------------------------------
+// Multi-token decode scorer (2 <= N <= 16 query rows per request) on the tensor cores.
+//
+// The pages' AB-swapped tile: the 128-token key-index block is the MMA's M side and the
+// request's query rows, padded to 16, its N side. Every (page, group) of the K-index is one
+// 128 x Di tile, brought by TMA ({64 channels, 1 group, 128 tokens} boxes, 128-byte swizzle)
+// into a ring of stages and read once from HBM whatever N is; one MMA group of Di/16 steps
+// (M 128, N 16) writes its 128 x 16 fp32 scores into a slot of tensor memory. An epilogue
+// warpgroup (one token per thread) applies the causal mask of the request's last block and
+// reduces each query row's column to the block max with a transposing butterfly (16 shuffles
+// per warp for 16 columns), and one score per (query row, group, block) is written. The
+// CUDA-core scorer re-reads every query row from shared memory for every key row, which caps
+// it at about a quarter of the HBM bandwidth at N = 8.
+//
+// Work: the batch's (request, page) list in contiguous ranges, one persistent CTA per SM, the
+// page's Hkv groups in order. Roles: warp 0 loads (TMA), warp 1 issues the MMAs (one elected
+// lane of the converged warp), warps 2-5 drain tensor memory. The top-k of the N*Hkv rows of
+// every request follows in the multi-row top-k kernel, one warp per row over the whole GPU:
+// left to the CTA that finishes a request's last page (as the one-row scorer does) the
+// N*Hkv top-ks of a request run on four warps of one SM while the others are idle.
+constexpr int kTdThreads = 192;
+constexpr int kTdEpi = 4;           // epilogue warps (128 tensor-memory lanes)
+constexpr int kTdAcc = 4;           // accumulator slots of 16 columns
+constexpr int kTdNPad = 16;         // query rows per MMA (N of the instruction)
+
+struct TdLayout {
+  uint32_t stage_bytes, q_bytes, off_q, off_red, off_bar, off_misc, total;
+  int nstage;
+};
+
+__host__ __device__ inline TdLayout td_layout(int Hkv, int Di, int nstage) {
+  TdLayout L;
+  L.nstage = nstage;
+  L.stage_bytes = (uint32_t)(128 * Di * 2);                   // one (page, group) tile
+  L.q_bytes = (uint32_t)(Hkv * (Di / 64) * kTdNPad * 128);    // 16 rows x 64 channels per box
+  uint32_t off = L.stage_bytes * (uint32_t)nstage;            // stages first (1024-aligned)
+  L.off_q = off;
+  off += L.q_bytes;
+  L.off_red = off;
+  off += (uint32_t)(2 * kTdEpi * kTdNPad * 4);                // per-warp column maxima, x2
+  off = (off + 7u) & ~7u;
+  L.off_bar = off;
+  off += (uint32_t)(8 * (2 * nstage + 2 + 2 * kTdAcc));
+  L.off_misc = off;
+  off += 64;
+  L.total = off + 1024;
+  return L;
+}
+
+struct TdParams {
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t B, N, Hkv, Di, max_blocks, nstage;
+  int64_t num_pages;
+  float* scores;
+};
+
+// Barrier of the epilogue warps, returning whether any epilogue thread passed `flag` (one decision for all).
+__device__ __forceinline__ bool td_epi_sync_or(bool flag) {
+  uint32_t any;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 2, %2, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(any)
+      : "r"((uint32_t)flag), "n"(kTdEpi * 32)
+      : "memory");
+  return any != 0;
+}
+
+// Max over the warp's 32 rows of each of 16 columns: afterwards lanes 2c and 2c+1 hold the max
+// of column c (each step halves the columns a lane keeps and exchanges the other half).
+__device__ __forceinline__ float warp_colmax16(float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float give = u16 ? v[c] : v[c + 8], keep = u16 ? v[c + 8] : v[c];
+    w8[c] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float give = u8 ? w8[c] : w8[c + 4], keep = u8 ? w8[c + 4] : w8[c];
+    w4[c] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const float give = u4 ? w4[c] : w4[c + 2], keep = u4 ? w4[c + 2] : w4[c];
+    w2[c] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+  }
+  const float give = u2 ? w2[0] : w2[1], keep = u2 ? w2[1] : w2[0];
+  float w = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 2));
+  return fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 1));
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kTdThreads, 1)
+    score_tc_decode_kernel(const __grid_constant__ CUtensorMap qmap,
+                           const __grid_constant__ CUtensorMap kmap, const TdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const TdLayout L = td_layout(p.Hkv, DI, p.nstage);
+  const int nstage = p.nstage, Hkv = p.Hkv, N = p.N;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  uint64_t* empty = full + nstage;
+  uint64_t* q_full = empty + nstage;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* acc_full = q_empty + 1;
+  uint64_t* acc_empty = acc_full + kTdAcc;
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.off_misc);
+  float* red = reinterpret_cast<float*>(smem + L.off_red);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- the CTA's contiguous range of (request, page) items: warp 0 scans the lengths
+  if (warp == 0) {
+    int total = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      bool bad = false;
+      const int nb = b < p.B ? (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128 : 0;
+      if (bad && blockIdx.x == 0) msa_record_error(kErrBadBlock);
+      total += __reduce_add_sync(0xffffffffu, nb);
+    }
+    const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int p0 = min(total, (int)blockIdx.x * per);
+    const int p1 = min(total, p0 + per);
+    int run = 0, b_start = p.B, j_start = 0;
+    for (int b0 = 0; b0 < p.B && b_start == p.B; b0 += 32) {
+      const int b = b0 + lane;
+      bool bad = false;
+      const int nb = b < p.B ? (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128 : 0;
+      int incl = nb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - nb;
+      const uint32_t hit = __ballot_sync(0xffffffffu, b < p.B && run + excl <= p0 && p0 < run + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        b_start = b0 + src;
+        j_start = p0 - run - __shfl_sync(0xffffffffu, excl, src);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      misc[0] = p0;
+      misc[1] = p1;
+      misc[2] = b_start;
+      misc[3] = j_start;
+      misc[5] = 0;  // set when a bounded wait gives up
+    }
+  }
+  if (tid == 32) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, kTdEpi);
+    for (int a = 0; a < kTdAcc; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kTdEpi);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(misc + 8)), "n"(kTdAcc * kTdNPad)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = (uint32_t)misc[8];
+  const int p0 = misc[0], p1 = misc[1];
+  const uint32_t sbase = smem_u32(smem);
+  volatile int32_t* fail = misc + 5;
+  auto wait_ok = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_wait(bar, parity)) return true;
+    msa_record_error(kErrTimeout);
+    *fail = 1;
+    return false;
+  };
+
+  if (p0 < p1) {
+    if (warp == 0) {
+      // ================================================================ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&qmap);
+        int b = misc[2], j = misc[3], qloads = 0;
+        bool bad = false;
+        int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = p0; item < p1 && ok; ++item) {
+          if (item == p0 || j == 0) {
+            // the request's query-index rows (16 from its first row; the MMA reads N of them)
+            if (qloads > 0 && !wait_ok(q_empty, (qloads - 1) & 1)) break;
+            mbar_expect_tx(q_full, L.q_bytes);
+            for (int g = 0; g < Hkv; ++g)
+              for (int h = 0; h < DI / 64; ++h)
+                tma_load_3d(smem + L.off_q + (g * (DI / 64) + h) * (kTdNPad * 128), &qmap, q_full,
+                            h * 64, g, b * N);
+            ++qloads;
+          }
+          int32_t page = p.page_table[(int64_t)b * p.max_blocks + j];
+          if (page < 0 || page >= p.num_pages) {
+            msa_record_error(kErrBadPage);
+            page = 0;
+          }
+          for (int g = 0; g < Hkv; ++g, ++it) {
+            const uint32_t s = it % nstage;
+            if (it >= (uint32_t)nstage && !wait_ok(&empty[s], ((it / nstage) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = smem + s * L.stage_bytes;
+            mbar_expect_tx(&full[s], L.stage_bytes);
+#pragma unroll
+            for (int h = 0; h < DI / 64; ++h)
+              tma_load_3d(dst + h * 16384, &kmap, &full[s], h * 64, g, page * 128);
+          }
+          if (++j == nb) {
+            j = 0;
+            ++b;
+            if (b < p.B) nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+          }
+        }
+        // the copies still in flight land before the CTA may exit
+        for (uint32_t k = it > (uint32_t)nstage ? it - nstage : 0; k < it; ++k)
+          mbar_wait(&empty[k % nstage], (k / nstage) & 1);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ================================================================ MMA issuer
+      const uint32_t idesc = umma_idesc_bf16(128, kTdNPad, 0, 0);
+      int b = misc[2], j = misc[3], qloads = 0;
+      bool bad = false;
+      int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = p0; item < p1 && ok; ++item) {
+        if (item == p0 || j == 0) {
+          ok = __all_sync(0xffffffffu, wait_ok(q_full, qloads & 1));
+          ++qloads;
+        }
+        for (int g = 0; g < Hkv && ok; ++g, ++it) {
+          const uint32_t s = it % nstage, a = it % kTdAcc;
+          ok = __all_sync(0xffffffffu, wait_ok(&full[s], (it / nstage) & 1)) &&
+               (it < (uint32_t)kTdAcc ||
+                __all_sync(0xffffffffu, wait_ok(&acc_empty[a], ((it / kTdAcc) - 1) & 1)));
+          if (!ok) break;
+          tmem_fence_after();
+          const uint64_t ad = umma_desc_sw128(sbase + s * L.stage_bytes, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(sbase + L.off_q + g * (DI / 64) * (kTdNPad * 128), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < DI / 16; ++kk) {
+            // 16 channels per step: 32 bytes into a 128-byte row, 16 KB (A) / 2 KB (B) per half
+            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * (kTdNPad * 128) + (kk & 3) * 32;
+            umma_bf16_elect(tmem + a * kTdNPad, ad + (aoff >> 4), bd + (boff >> 4), idesc, kk > 0);
+          }
+          umma_commit_elect(&acc_full[a]);
+          umma_commit_elect(&empty[s]);  // the stage is free once the group has read it
+        }
+        if (++j == nb) {
+          j = 0;
+          ++b;
+          if (b < p.B) nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+        }
+      }
+      __syncwarp();
+    } else {
+      // ================================================================ epilogue + top-k
+      // a warp reads the tensor-memory lanes of its sub-partition: 32 * (warp % 4) ..
+      const int ew = warp & 3;
+      const int erow = ew * 32 + lane;                // token of the block = accumulator row
+      const uint32_t lane_addr = (uint32_t)(32 * ew) << 16;
+      int b = misc[2], j = misc[3], cur_b = -1, par = 0, qloads = 0;
+      bool bad = false;
+      int nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+      uint32_t it = 0;
+      bool ok = true, failed = false;  // failed: agreed by all epilogue threads at a barrier
+      for (int item = p0; item < p1 && !failed; ++item) {
+        if (b != cur_b) {
+          cur_b = b;
+          if (qloads > 0 && lane == 0) mbar_arrive(q_empty);  // the previous request's rows
+          ++qloads;
+        }
+        bool bad_s = false;
+        const int seq = clamp_seq(p.seq_lens, b, N, p.max_blocks, bad_s);
+        const int pos = j * 128 + erow;
+        for (int g = 0; g < Hkv; ++g, ++it) {
+          const uint32_t a = it % kTdAcc;
+          // warp-uniform: the tensor-memory load below is warp-collective
+          ok = __all_sync(0xffffffffu, ok && wait_ok(&acc_full[a], (it / kTdAcc) & 1));
+          float v[16];
+          if (ok) {
+            tmem_fence_after();
+            uint32_t raw[16];
+            tmem_ld16(tmem + lane_addr + a * kTdNPad, raw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(raw[c]);
+          }
+          tmem_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+          // causal mask: row c sits at position seq - N + c
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (!ok || c >= N || pos > seq - N + c) v[c] = -INFINITY;
+          const float m = warp_colmax16(v, lane);
+          if ((lane & 1) == 0) red[(par * kTdEpi + ew) * kTdNPad + (lane >> 1)] = m;
+          // a wait that gave up is agreed here, so every epilogue warp leaves after the same item
+          failed = td_epi_sync_or(!ok);
+          const int tid_e = tid - 64;
+          if (!failed && tid_e < N) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kTdEpi; ++w) mx = fmaxf(mx, red[(par * kTdEpi + w) * kTdNPad + tid_e]);
+            const int64_t r = (int64_t)b * N + tid_e;
+            p.scores[(r * Hkv + g) * p.max_blocks + j] = mx;
+          }
+          par ^= 1;
+        }
+        if (failed) break;
+        if (++j == nb) {
+          j = 0;
+          ++b;
+          if (b < p.B) nb = (clamp_seq(p.seq_lens, b, N, p.max_blocks, bad) + 127) / 128;
+        }
+      }
+    }
+  }
+  // ------------------------------------------------------------------ teardown
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(kTdAcc * kTdNPad)
+                 : "memory");
+  }
+}
+
 constexpr size_t kSmemMax = 232448;  // opt-in shared memory per block on sm_100/sm_103
 
 }  // namespace
@@ -842,6 +1192,45 @@ cudaError_t launch_score_decode(const ScoreArgs& a, cudaStream_t stream) {
         : nq == 4 ? launch(score_decode_kernel<64, 4>) : launch(score_decode_kernel<64, 8>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+int score_tc_decode_stages(int Hkv, int Di) {
+  for (int ns = 6; ns >= 2; --ns)
+    if (td_layout(Hkv, Di, ns).total <= kSmemMax) return ns;
+  return 0;
+}
+
+cudaError_t launch_score_tc_decode(const ScoreArgs& a, cudaStream_t stream) {
+  const int nstage = score_tc_decode_stages(a.Hkv, a.Di);
+  if (nstage < 2 || a.N > kTdNPad) return cudaErrorInvalidValue;
+  CUtensorMap qmap, kmap;
+  const uint64_t qdims[3] = {(uint64_t)a.Di, (uint64_t)a.Hkv, (uint64_t)a.B * a.N};
+  const uint64_t kdims[3] = {(uint64_t)a.Di, (uint64_t)a.Hkv, (uint64_t)a.num_pages * 128};
+  const uint64_t strides[2] = {(uint64_t)a.Di * 2, (uint64_t)a.Hkv * a.Di * 2};
+  const uint32_t qbox[3] = {64, 1, (uint32_t)kTdNPad};
+  const uint32_t kbox[3] = {64, 1, 128};
+  if (!encode_bf16_map(&qmap, a.q_idx, 3, qdims, strides, qbox, true) ||
+      !encode_bf16_map(&kmap, a.k_idx, 3, kdims, strides, kbox, true))
+    return cudaErrorInvalidValue;
+  TdParams p;
+  p.page_table = a.page_table;
+  p.seq_lens = a.seq_lens;
+  p.B = a.B;
+  p.N = a.N;
+  p.Hkv = a.Hkv;
+  p.Di = a.Di;
+  p.max_blocks = a.max_blocks;
+  p.nstage = nstage;
+  p.num_pages = a.num_pages;
+  p.scores = a.scores;
+  const size_t smem = td_layout(a.Hkv, a.Di, nstage).total;
+  auto launch = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<sm_count(), kTdThreads, smem, stream>>>(qmap, kmap, p);
+    return cudaGetLastError();
+  };
+  return a.Di == 128 ? launch(score_tc_decode_kernel<128>) : launch(score_tc_decode_kernel<64>);
 }
 
 cudaError_t launch_score_rows(const ScoreArgs& a, cudaStream_t stream) {

@@ -56,8 +56,21 @@ def test_score_topk_streaming_path(seq_lens, N, Hkv, Di, topk):
 
 
 @pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
+    ([517, 3000, 129, 7000], 2, 8, 128, 16),        # two rows per request, ragged, one short request
+    ([2000, 4100, 260], 3, 2, 64, 6),               # odd row count, Di 64
+    ([6000, 5000, 999, 12000], 8, 16, 128, 8),      # Hkv 16 (the largest): 4 ring stages
+    ([3000, 16, 4097], 16, 1, 128, 5),              # 16 rows (a full MMA N), a request of 16 tokens
+    ([9000, 1500], 12, 4, 64, 32),                  # k 32, rows straddling a block boundary
+])
+def test_score_topk_multi_token_tensor_core_path(seq_lens, N, Hkv, Di, topk):
+    """2 <= N <= 16 query rows per request: the tensor-core scorer (128-token block as M, rows
+    padded to 16 as N) with the top-k fused into its last CTA per request."""
+    _score_case(seq_lens, N, Hkv, Di, topk, seed=hash((tuple(seq_lens), N, Di)) % 1000 + 3)
+
+
+@pytest.mark.parametrize("seq_lens,N,Hkv,Di,topk", [
     ([700], 300, 2, 64, 4),                         # prefill chunk, ragged row tile
-    ([2048, 1500], 33, 4, 128, 5),                  # two requests, N just above the streaming cap
+    ([2048, 1500], 33, 4, 128, 5),                  # two requests, N above the decode scorers' cap
     ([5000, 3000], 600, 2, 128, 8),                 # chunks after a prefix, several row tiles
     ([1300], 1300, 4, 128, 16),                     # whole sequence is the chunk, ragged tiles
     ([9000, 129, 4000], 129, 2, 64, 6),             # one request with seq == N, 4-block chunks
