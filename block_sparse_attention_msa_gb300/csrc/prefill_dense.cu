@@ -83,6 +83,27 @@ struct SelectParams {
 // Blocks per pair histogram for the one-warp-per-pair selection (smaller key ranges); longer
 // key ranges take the CTA-wide windowed selection.
 constexpr int kPairHist = 1024;
+// A row's ids are loaded, and its list counts taken, kIdBatch at a time: the loads (and the
+// atomics, whose returned place is stored) are all in flight before any result is used.
+constexpr int kIdBatch = 16;
+
+// Counts up to kIdBatch selections (ids j[], -1 = none; `n` of them valid slots) of one row into
+// their lists; each one's place in its list goes to epos[at + u].
+__device__ __forceinline__ void count_batch(const SelectParams& p, const int32_t (&j)[kIdBatch],
+                                            int64_t list0, int64_t at, int n) {
+  int32_t pos[kIdBatch];
+#pragma unroll
+  for (int u = 0; u < kIdBatch; ++u) {
+    pos[u] = -1;
+    if (u < n && j[u] >= 0) {
+      if (j[u] < p.nblk) pos[u] = atomicAdd(&p.counts[list0 + j[u]], 1);
+      else msa_record_error(kErrBadBlock);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kIdBatch; ++u)
+    if (pos[u] >= 0) p.epos[at + u] = pos[u];
+}
 
 // One CTA per (group g, 128-query span), one thread per query of the span. The span's ids are
 // staged in shared memory once.
@@ -114,14 +135,12 @@ __global__ void __launch_bounds__(kSpan)
     // (c) only: count the selections of this thread's query
     if (!valid) return;
     const int64_t list0 = ((int64_t)g * p.nwin + t_me / p.win) * p.nblk;
-    for (int k = 0; k < p.topk; ++k) {
-      const int32_t j = p.block_ids[row_me * p.topk + k];
-      if (j < 0) continue;
-      if (j >= p.nblk) {
-        msa_record_error(kErrBadBlock);
-        continue;
-      }
-      p.epos[row_me * p.topk + k] = atomicAdd(&p.counts[list0 + j], 1);
+    for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
+      int32_t j[kIdBatch];
+#pragma unroll
+      for (int u = 0; u < kIdBatch; ++u)
+        j[u] = k0 + u < p.topk ? p.block_ids[row_me * p.topk + k0 + u] : -1;
+      count_batch(p, j, list0, row_me * p.topk + k0, p.topk - k0);
     }
     return;
   }
@@ -129,8 +148,15 @@ __global__ void __launch_bounds__(kSpan)
   // residuals are written over them in (a)), then the histograms of (o) and (a)
   int32_t* s_ids = reinterpret_cast<int32_t*>(sel_smem);
   uint8_t* hist = sel_smem + (size_t)kSpan * p.topk * 4;
-  for (int k = 0; k < p.topk; ++k)
-    s_ids[k * kSpan + r] = valid ? p.block_ids[row_me * p.topk + k] : -1;
+  for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
+    int32_t j[kIdBatch];  // a row's ids requested together, then stored
+#pragma unroll
+    for (int u = 0; u < kIdBatch; ++u)
+      j[u] = valid && k0 + u < p.topk ? p.block_ids[row_me * p.topk + k0 + u] : -1;
+#pragma unroll
+    for (int u = 0; u < kIdBatch; ++u)
+      if (k0 + u < p.topk) s_ids[(k0 + u) * kSpan + r] = j[u];
+  }
   // ---------------- (o) slot order of the span
   if (p.ordered) {
     uint32_t* span_cnt = reinterpret_cast<uint32_t*>(hist);  // [nb_max]
@@ -294,15 +320,14 @@ __global__ void __launch_bounds__(kSpan)
   // ---------------- (c) count the remaining selections of this thread's query into their lists
   if (!valid) return;
   const int64_t list0 = ((int64_t)g * p.nwin + t_me / p.win) * p.nblk;
-  for (int k = 0; k < p.topk; ++k) {
-    const int32_t j = s_ids[k * kSpan + r];
-    p.residual[row_me * p.topk + k] = j;
-    if (j < 0) continue;
-    if (j >= p.nblk) {
-      msa_record_error(kErrBadBlock);
-      continue;
+  for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
+    int32_t j[kIdBatch];
+#pragma unroll
+    for (int u = 0; u < kIdBatch; ++u) {
+      j[u] = k0 + u < p.topk ? s_ids[(k0 + u) * kSpan + r] : -1;
+      if (k0 + u < p.topk) p.residual[row_me * p.topk + k0 + u] = j[u];
     }
-    p.epos[row_me * p.topk + k] = atomicAdd(&p.counts[list0 + j], 1);
+    count_batch(p, j, list0, row_me * p.topk + k0, p.topk - k0);
   }
 }
 
