@@ -275,8 +275,9 @@ def prefill_stage(wpf, pre_ms, pk):
             "frac_bf16": round(tfl / pk["bf16_tflops"], 4),
             "peak": pk["bf16_tflops"], "peak_kind": "burst (measured)",
             "frac_bf16_sustained": round(tfl / pk["bf16_tflops_sustained"], 4),
-            "kernels": "query-major selection + attention for blocks shared by a query pair; "
-                       "bucketing + block-major attention for the rest; LSE merge "
+            "kernels": "selection + counting; list offsets; placement; block-major attention "
+                       "for the scattered selections; query-major attention for blocks shared "
+                       "by a query pair; LSE merge "
                        "(per-kernel times: profiles/launches_bench_default.md)",
             "flops": wpf["flops"],
             # algorithmic FLOPs per pass, and what the query-major pass executes (its pairs'
@@ -321,10 +322,8 @@ def recorded_traffic(kernel: str, source_hash: str):
 
 
 # Every kernel of one msa_sparse_prefill call and the source file it is built from.
-PREFILL_KERNELS = (("pair_order_kernel", "prefill_dense.cu"), ("dense_select_kernel", "prefill_dense.cu"),
-                   ("bucket_count_kernel", "prefill.cu"), ("bucket_scan_kernel", "prefill.cu"),
-                   ("bucket_seg_scan_kernel", "prefill.cu"), ("bucket_scatter_kernel", "prefill.cu"),
-                   ("tile_desc_kernel", "prefill.cu"), ("prefill_block_tc_kernel", "prefill.cu"),
+PREFILL_KERNELS = (("select_count_kernel", "prefill_dense.cu"), ("bucket_lists_kernel", "prefill.cu"),
+                   ("bucket_place_kernel", "prefill.cu"), ("prefill_block_tc_kernel", "prefill.cu"),
                    ("prefill_dense_tc_kernel", "prefill_dense.cu"),
                    ("lse_merge_chunked_kernel", "page_table_merge.cu"))
 
@@ -462,11 +461,11 @@ def run_ours(args, ws, rank, local):
                                "block-major sparse prefill (32768 tokens)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
-        # kernels of this library per step: scorer (1); page table, decode, merge (3); query
-        # ordering, dense selection, bucket count, two scans, scatter, tile descriptors,
-        # block-major attention, query-major attention, merge (10). Memsets not counted.
+        # kernels of this library per step: scorer with its top-k (1); page table, decode,
+        # merge (3); selection with counting, list offsets, placement, block-major attention,
+        # query-major attention, merge (6). Memsets not counted.
         "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
-                                      + ("prefill" in run) * 10),
+                                      + ("prefill" in run) * 6),
         "clocks": clk.summary(), "device_error_word": err,
     }
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):
@@ -769,11 +768,15 @@ def run_long_context(args, local):
     ws_ = msa.Workspace()
 
     def timed(fn, reps):
+        # device time of `reps` back-to-back calls: a spin kernel queued first keeps the GPU
+        # busy while the host enqueues them, so calls shorter than their host-side cost are
+        # timed by their kernels, not by the launch rate
         for _ in range(2):
             fn()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        torch.cuda._sleep(int(4e6))
         a.record()
         for _ in range(reps):
             fn()

@@ -12,15 +12,13 @@
 // passes, and the merge (row a7) combines the query-major partial with the block-major ones.
 //
 // GB300 design.
-//  (o) pair_order_kernel, one CTA per (group, 128-query span): orders the span's queries so
-//      that those choosing the span's popular blocks (chosen by at least half of the span) come
-//      first. Pairs are consecutive slots of that order, so queries that share blocks fill the
-//      same tiles and fewer masked rows ride through the query-major MMAs.
-//  (a) dense_select_kernel, one CTA per pair of 128/G-query tiles (2*128/G slots of one
-//      group's order): counts the pair's selections per block in shared memory, keeps
-//      the blocks chosen by at least half of the pair's queries (at most kMaxDense, ascending)
-//      with a bit mask of the queries that chose each, and writes the residual selections (the
-//      dense ones replaced by -1) for the block-major pass.
+//  (o, a) select_count_kernel, one CTA per (group, 128-query span): orders the span's queries
+//      so that those choosing the span's popular blocks (chosen by at least half of the span)
+//      come first, so that queries sharing blocks fill the same tiles; then, per pair of
+//      128/G-query tiles (consecutive slots of that order), keeps the blocks chosen by at least
+//      half of the pair's queries (at most kMaxDense, ascending) with a bit mask of the queries
+//      that chose each, writes the residual selections (the shared ones replaced by -1) and
+//      counts each residual selection into its block-major list.
 //  (b) prefill_dense_tc_kernel, one persistent CTA per SM over the pairs: the two tiles of a
 //      pair share each K/V block load; per block S = Q K^T and O += P V run on tcgen05 with
 //      S, P and O in tensor memory; one softmax warpgroup per tile keeps a running row max and
