@@ -178,10 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKPar
   Steps cur, pf;
   cur.start(u0, u1);
   pf.start(u0, u1);
-  cur.advance(p, cap, lane);
-  pf.advance(p, cap, lane);
   RegWindow vw;
   vw.base = LLONG_MIN / 2;
+  // the range's first page ids are requested before the row lengths that the walk needs
+  // first, so the two round trips overlap
+  if (u0 < u1) (void)vw.get(p.fpt, p.units, u0, lane);
+  cur.advance(p, cap, lane);
+  pf.advance(p, cap, lane);
   // prefetch the first kStages - 1 steps (one commit group per step; empty groups past the
   // end keep the count uniform)
 #pragma unroll

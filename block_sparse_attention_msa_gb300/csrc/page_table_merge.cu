@@ -107,26 +107,52 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<uint4*>(o + orow + c * 8) = out;
     }
   } else {
-    // generic path: lanes own 4 consecutive channels, partials in sequence
+    // generic path: lanes own 4 consecutive channels; the partials that carry weight stream
+    // sixteen at a time with all their loads in flight (a row's partials are independent, so a
+    // warp pays one memory round trip per sixteen of them, not one per partial)
+    const uint64_t vm = (uint64_t)__ballot_sync(0xffffffffu, wts[0] != 0.f) |
+                        ((uint64_t)__ballot_sync(0xffffffffu, wts[1] != 0.f) << 32);
     for (int d0 = 0; d0 < D; d0 += 128) {
       const int d = d0 + lane * 4;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < S; ++s) {
-        const float w = __shfl_sync(0xffffffffu, s < 32 ? wts[0] : wts[1], s & 31);
-        if (w == 0.f || d >= D) continue;
-        const int64_t row = ((u * S + s) * G + e) * (int64_t)D;
-        if (BF16) {
-          const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(o_parts) + row + d);
-          acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
-          acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
-          acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
-          acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
-        } else {
-          const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o_parts) + row + d);
-          acc[0] = fmaf(w, v.x, acc[0]);
-          acc[1] = fmaf(w, v.y, acc[1]);
-          acc[2] = fmaf(w, v.z, acc[2]);
-          acc[3] = fmaf(w, v.w, acc[3]);
+      uint64_t rest = vm;
+      while (rest) {
+        constexpr int kBatch = 16;
+        int sl[kBatch];
+        float w8[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          sl[k] = -1;
+          if (rest) {
+            sl[k] = __ffsll((long long)rest) - 1;
+            rest &= rest - 1;
+          }
+          const float wsel = sl[k] >= 32 ? wts[1] : wts[0];
+          w8[k] = __shfl_sync(0xffffffffu, wsel, sl[k] & 31);
+          if (sl[k] < 0) w8[k] = 0.f;
+        }
+        float4 v[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (sl[k] >= 0 && d < D) {
+            const int64_t row = ((u * S + sl[k]) * G + e) * (int64_t)D;
+            if (BF16) {
+              const uint2 b = __ldcs(reinterpret_cast<const uint2*>(
+                  reinterpret_cast<const uint16_t*>(o_parts) + row + d));
+              v[k] = make_float4(bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y));
+            } else {
+              v[k] = __ldcs(reinterpret_cast<const float4*>(
+                  reinterpret_cast<const float*>(o_parts) + row + d));
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          acc[0] = fmaf(w8[k], v[k].x, acc[0]);
+          acc[1] = fmaf(w8[k], v[k].y, acc[1]);
+          acc[2] = fmaf(w8[k], v[k].z, acc[2]);
+          acc[3] = fmaf(w8[k], v[k].w, acc[3]);
         }
       }
       if (d < D) {

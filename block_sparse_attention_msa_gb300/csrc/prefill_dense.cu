@@ -118,7 +118,11 @@ __device__ __forceinline__ void count_batch(const SelectParams& p, const int32_t
 __global__ void __launch_bounds__(kSpan)
     select_count_kernel(const SelectParams p) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
-  __shared__ __align__(16) int32_t score[kSpan];
+  // slot order: per warp, the number of its queries with each score key (score + 1, 0..topk+1),
+  // and per key the number of the span's queries with a larger key
+  constexpr int kKeys = 96;  // > topk + 1 for topk <= 64
+  __shared__ int32_t key_cnt[kSpan / 32][kKeys];
+  __shared__ int32_t key_above[kKeys];
   __shared__ int32_t s_query[kSpan];   // query of each slot of the span (-1: none)
   __shared__ int16_t s_row[kSpan];     // span row (t - span start) of each slot
   __shared__ int32_t warp_sum[kSpan / 32];
@@ -159,6 +163,7 @@ __global__ void __launch_bounds__(kSpan)
   if (p.ordered) {
     uint32_t* span_cnt = reinterpret_cast<uint32_t*>(hist);  // [nb_max]
     for (int j = r; j < p.nb_max; j += kSpan) span_cnt[j] = 0u;
+    for (int j = r; j < (kSpan / 32) * kKeys; j += kSpan) (&key_cnt[0][0])[j] = 0;
     __syncthreads();
     for (int k = 0; k < p.topk; ++k) {
       const int32_t j = s_ids[k * kSpan + r];
@@ -173,17 +178,37 @@ __global__ void __launch_bounds__(kSpan)
         if (j >= 0 && j < p.nb_max && 2 * (int)span_cnt[j] >= nvalid) ++sc;
       }
     }
-    score[r] = sc;
+    // stable rank by score, descending: the queries with a larger score, then those with the
+    // same score and a lower span row (earlier warps' counts, then lower lanes of this warp)
+    const int key = sc + 1;
+    const uint32_t same = __match_any_sync(0xffffffffu, key);
+    const int below = __popc(same & ((1u << lane) - 1u));
+    if (below == 0) key_cnt[warp][key] = __popc(same);
     __syncthreads();
-    int rank = 0;
-#pragma unroll 4
-    for (int q = 0; q < kSpan; q += 4) {
-      const int4 s4 = *reinterpret_cast<const int4*>(score + q);
-      rank += (s4.x > sc || (s4.x == sc && q < r)) ? 1 : 0;
-      rank += (s4.y > sc || (s4.y == sc && q + 1 < r)) ? 1 : 0;
-      rank += (s4.z > sc || (s4.z == sc && q + 2 < r)) ? 1 : 0;
-      rank += (s4.w > sc || (s4.w == sc && q + 3 < r)) ? 1 : 0;
+    if (warp == 0) {
+      // key_above[k] = number of queries with key > k (suffix sums over three 32-key groups)
+      int t3[3], x3[3];
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        const int k = lane + 32 * c;
+        t3[c] = 0;
+#pragma unroll
+        for (int w = 0; w < kSpan / 32; ++w) t3[c] += key_cnt[w][k];
+        x3[c] = t3[c];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, x3[c], o);
+          if (lane + o < 32) x3[c] += y;
+        }
+      }
+      const int tot1 = __shfl_sync(0xffffffffu, x3[1], 0), tot2 = __shfl_sync(0xffffffffu, x3[2], 0);
+      key_above[lane] = x3[0] - t3[0] + tot1 + tot2;
+      key_above[lane + 32] = x3[1] - t3[1] + tot2;
+      key_above[lane + 64] = x3[2] - t3[2];
     }
+    __syncthreads();
+    int rank = key_above[key] + below;
+    for (int w = 0; w < warp; ++w) rank += key_cnt[w][key];
     s_query[rank] = valid ? (int32_t)t_me : -1;
     s_row[rank] = (int16_t)r;
     p.qperm[(int64_t)g * p.npos + span * kSpan + rank] = valid ? (int32_t)t_me : -1;
