@@ -22,6 +22,8 @@
 //    LSE) into the slot of the first page it covered; the other slots of its range hold LSE
 //    -inf, and the LSE-merge kernel combines a row's slots. The result does not depend on warp
 //    timing.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <climits>
 
@@ -160,21 +162,16 @@ __device__ __forceinline__ void load_step(uint32_t st, const DecKParams& p, int3
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ring = smem_u32(smem) + warp * kStages * kStep;
+// One warp's walk over the units [u0, u1) through its ring of kStages step buffers (ring: the
+// shared-memory address of the warp's buffers). At the end of each row segment it calls
+// emit(f, slot_row, o, lrow, mrow, gid, tig) with the segment's unnormalised O fragments (rows
+// gid / gid + 8 = heads, columns nd*8 + tig*2 + {0, 1}), the row sums (already reduced over
+// the quad) and the row maxima; the walk's copies of that segment have all landed by then.
+template <class Emit>
+__device__ __forceinline__ void walk_units(const DecKParams& p, uint32_t ring, int64_t u0,
+                                           int64_t u1, int lane, Emit&& emit) {
   const int cap = p.topk * 128;
   const int G = p.G;
-  const int64_t nw = (int64_t)gridDim.x * kWarps, wg = (int64_t)blockIdx.x * kWarps + warp;
-  const int64_t u0 = p.units * wg / nw, u1 = p.units * (wg + 1) / nw;
-
-  // every slot of the range starts empty; a row segment's partial overwrites its first slot
-  for (int64_t i = u0 * G + lane; i < u1 * G; i += 32) p.part_lse[i] = -INFINITY;
-  __syncwarp();
-
   Steps cur, pf;
   cur.start(u0, u1);
   pf.start(u0, u1);
@@ -311,27 +308,122 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKPar
       cur.advance(p, cap, lane);
     } while (cur.valid && cur.f == f);
 
-    // ---- the segment's partial: normalised O and LSE per head, in its first page's slot
+    // ---- the segment's partial
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
       lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
     }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = gid + 8 * r;
-      if (row >= G) continue;
-      const float inv = lrow[r] > 0.f ? 1.0f / lrow[r] : 0.f;
-      float* dst = p.part_o + (slot_row * G + row) * 128;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd)
-        *reinterpret_cast<float2*>(dst + nd * 8 + tig * 2) =
-            make_float2(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
-      if (tig == 0)
-        p.part_lse[slot_row * G + row] = lrow[r] > 0.f ? mrow[r] + __logf(lrow[r]) : -INFINITY;
-    }
+    emit(f, slot_row, o, lrow, mrow, gid, tig);
   }
   cp_async_wait<0>();
+}
+
+// Writes a segment's partial as normalised fp32 rows dst[head][128] and its LSE per head.
+__device__ __forceinline__ void store_partial(float* dst, float* lse_dst, const float (&o)[16][4],
+                                              const float (&lrow)[2], const float (&mrow)[2],
+                                              int G, int gid, int tig) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = gid + 8 * r;
+    if (row >= G) continue;
+    const float inv = lrow[r] > 0.f ? 1.0f / lrow[r] : 0.f;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd)
+      *reinterpret_cast<float2*>(dst + row * 128 + nd * 8 + tig * 2) =
+          make_float2(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
+    if (tig == 0) lse_dst[row] = lrow[r] > 0.f ? mrow[r] + __logf(lrow[r]) : -INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const DecKParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ring = smem_u32(smem) + warp * kStages * kStep;
+  const int G = p.G;
+  const int64_t nw = (int64_t)gridDim.x * kWarps, wg = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t u0 = p.units * wg / nw, u1 = p.units * (wg + 1) / nw;
+
+  // every slot of the range starts empty; a row segment's partial overwrites its first slot
+  for (int64_t i = u0 * G + lane; i < u1 * G; i += 32) p.part_lse[i] = -INFINITY;
+  __syncwarp();
+  walk_units(p, ring, u0, u1, lane,
+             [&](int64_t, int64_t slot_row, const float (&o)[16][4], const float (&lrow)[2],
+                 const float (&mrow)[2], int gid, int tig) {
+               store_partial(p.part_o + slot_row * G * 128, p.part_lse + slot_row * G, o, lrow,
+                             mrow, G, gid, tig);
+             });
+}
+
+// Few rows (a small batch at long context): a cluster of kClusterCtas CTAs per flattened row.
+// Its 32 warps split the row's selected pages into contiguous ranges and walk them as above;
+// each warp then leaves its normalised partial and LSEs in its own (now idle) ring buffer, and
+// after a cluster barrier every CTA merges a share of the row's (head, channel) outputs from
+// all 32 partials through distributed shared memory. No partial goes to HBM and no merge
+// kernel follows.
+constexpr int kClusterCtas = 4;
+
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads, 1)
+    paged_decode_cluster_kernel(const DecKParams p, uint16_t* __restrict__ o_out,
+                                float* __restrict__ lse_out) {
+  namespace cg = cooperative_groups;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  cg::cluster_group cluster = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster.block_rank();
+  const int64_t f = blockIdx.x / kClusterCtas;  // flattened row (request, group)
+  const int G = p.G;
+  constexpr int kParts = kClusterCtas * kWarps;
+  const int wi = rank * kWarps + warp;
+  const int64_t u0 = f * p.topk + (int64_t)p.topk * wi / kParts;
+  const int64_t u1 = f * p.topk + (int64_t)p.topk * (wi + 1) / kParts;
+  // a warp's partial, once its walk is over: O [G][128] fp32, then its G LSEs
+  constexpr uint32_t kWarpBytes = kStages * kStep;
+  float* part = reinterpret_cast<float*>(smem + warp * kWarpBytes);
+  float* part_lse = part + 16 * 128;
+  bool emitted = false;
+  walk_units(p, smem_u32(smem) + warp * kWarpBytes, u0, u1, lane,
+             [&](int64_t, int64_t, const float (&o)[16][4], const float (&lrow)[2],
+                 const float (&mrow)[2], int gid, int tig) {
+               cp_async_wait<0>();
+               __syncwarp();  // the ring's last step is read: it becomes the partial's space
+               store_partial(part, part_lse, o, lrow, mrow, G, gid, tig);
+               emitted = true;
+             });
+  if (!emitted)  // no visible page in the range
+    for (int h = lane; h < G; h += 32) part_lse[h] = -INFINITY;
+  cluster.sync();  // every warp's partial is in its CTA's shared memory
+  // (head, channel) outputs of the row, dealt over the cluster's threads
+  for (int item = rank * kThreads + (int)threadIdx.x; item < G * 128;
+       item += kClusterCtas * kThreads) {
+    const int h = item >> 7, ch = item & 127;
+    float m = -INFINITY;
+    for (int j = 0; j < kParts; ++j) {
+      const float* pl = cluster.map_shared_rank(
+          reinterpret_cast<float*>(smem + (j % kWarps) * kWarpBytes) + 16 * 128, j / kWarps);
+      m = fmaxf(m, pl[h]);
+    }
+    float acc = 0.f, total = 0.f;
+    if (m != -INFINITY) {
+      for (int j = 0; j < kParts; ++j) {
+        const float* pj = cluster.map_shared_rank(
+            reinterpret_cast<float*>(smem + (j % kWarps) * kWarpBytes), j / kWarps);
+        const float l = pj[16 * 128 + h];
+        if (l == -INFINITY) continue;  // an empty range: its O was never written
+        const float w = __expf(l - m);
+        total += w;
+        acc = fmaf(w, pj[h * 128 + ch], acc);
+      }
+    }
+    const float inv = total > 0.f ? 1.0f / total : 0.f;
+    o_out[(f * G + h) * 128 + ch] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
+    if (lse_out && ch == 0) lse_out[f * G + h] = total > 0.f ? m + __logf(total) : -INFINITY;
+  }
+  cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
 }  // namespace
@@ -357,6 +449,15 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (p.units <= 0) return cudaSuccess;
+  if (p.rows * kClusterCtas <= sm_count()) {
+    // few rows: one cluster per row merges in distributed shared memory
+    e = cudaFuncSetAttribute(paged_decode_cluster_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    paged_decode_cluster_kernel<<<(unsigned)(p.rows * kClusterCtas), kThreads, smem, stream>>>(
+        p, a.o, a.lse);
+    return cudaGetLastError();
+  }
   const int64_t grid = std::min<int64_t>((p.units + kWarps - 1) / kWarps, sm_count());
   paged_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();

@@ -156,6 +156,26 @@ def test_paged_sparse_decode(seq_lens, N, Hq, Hkv, topk):
     check_attention(o, lse, ref, what="decode")
 
 
+def test_paged_sparse_decode_few_rows_cluster_merge():
+    """Few flattened rows (4 requests x 8 groups, the 1M-context batch shape at shorter
+    contexts): each row is owned by a cluster whose 32 warps take a page range each and merge
+    in distributed shared memory. Short requests leave some warps without a visible page."""
+    seq_lens = [40000, 9000, 700, 128]
+    N, Hq, Hkv, topk = 1, 64, 8, 32
+    w = workloads.decode_workload(seq_lens, N, Hq, Hkv, 128, topk, seed=9, device="cpu")
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    fpt, lens = msa.build_sparse_page_table(d["block_ids"], d["page_table"], d["seq_lens"], N,
+                                            w["num_pages"])
+    o, lse = msa.paged_sparse_decode(d["q"], d["k_cache"], d["v_cache"], fpt, lens)
+    o2, lse2 = msa.paged_sparse_decode(d["q"], d["k_cache"], d["v_cache"], fpt, lens)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    ref = oracle.sparse_decode(u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"]), w["page_table"].numpy(),
+                               w["seq_lens"].numpy(), w["block_ids"].numpy(), N)
+    check_attention(o, lse, ref, what="decode")
+    assert msa.device_error() == 0
+
+
 def test_paged_sparse_decode_ranges_cross_rows():
     """More (row, page) units than the grid has warps: each warp's range covers several pages
     and crosses row boundaries, so rows are split into segments merged through their slots;
