@@ -394,34 +394,42 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
                store_partial(part, part_lse, o, lrow, mrow, G, gid, tig);
                emitted = true;
              });
-  if (!emitted)  // no visible page in the range
+  if (!emitted) {  // no visible page in the range: O = 0, LSE -inf
+    cp_async_wait<0>();
+    __syncwarp();
+    for (int i = lane; i < G * 128; i += 32) part[i] = 0.f;
     for (int h = lane; h < G; h += 32) part_lse[h] = -INFINITY;
+  }
   cluster.sync();  // every warp's partial is in its CTA's shared memory
-  // (head, channel) outputs of the row, dealt over the cluster's threads
+  // the row's merge weights, one warp per head, lane j = partial j: w[h][j] = e^(lse_j - lse)
+  // (0 for an empty range), kept in this CTA (behind warp 0's partial, which stays readable)
+  float* wts = reinterpret_cast<float*>(smem + 12 * 1024);
+  static_assert(kParts == 32, "one lane per partial");
+  for (int h = warp; h < G; h += kWarps) {
+    const float* pl = cluster.map_shared_rank(
+        reinterpret_cast<float*>(smem + (lane % kWarps) * kWarpBytes) + 16 * 128, lane / kWarps);
+    const float l = pl[h];
+    const float m = warp_max(l);
+    const float e = (m == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - m);
+    const float total = warp_sum(e);
+    wts[h * 32 + lane] = total > 0.f ? e / total : 0.f;
+    if (lane == 0 && lse_out && rank == (h % kClusterCtas))
+      lse_out[f * G + h] = total > 0.f ? m + __logf(total) : -INFINITY;
+  }
+  __syncthreads();
+  // (head, channel) outputs of the row, dealt over the cluster's threads: 32 independent
+  // remote loads each
   for (int item = rank * kThreads + (int)threadIdx.x; item < G * 128;
        item += kClusterCtas * kThreads) {
     const int h = item >> 7, ch = item & 127;
-    float m = -INFINITY;
+    float acc = 0.f;
+#pragma unroll
     for (int j = 0; j < kParts; ++j) {
-      const float* pl = cluster.map_shared_rank(
-          reinterpret_cast<float*>(smem + (j % kWarps) * kWarpBytes) + 16 * 128, j / kWarps);
-      m = fmaxf(m, pl[h]);
+      const float* pj = cluster.map_shared_rank(
+          reinterpret_cast<float*>(smem + (j % kWarps) * kWarpBytes), j / kWarps);
+      acc = fmaf(wts[h * 32 + j], pj[h * 128 + ch], acc);
     }
-    float acc = 0.f, total = 0.f;
-    if (m != -INFINITY) {
-      for (int j = 0; j < kParts; ++j) {
-        const float* pj = cluster.map_shared_rank(
-            reinterpret_cast<float*>(smem + (j % kWarps) * kWarpBytes), j / kWarps);
-        const float l = pj[16 * 128 + h];
-        if (l == -INFINITY) continue;  // an empty range: its O was never written
-        const float w = __expf(l - m);
-        total += w;
-        acc = fmaf(w, pj[h * 128 + ch], acc);
-      }
-    }
-    const float inv = total > 0.f ? 1.0f / total : 0.f;
-    o_out[(f * G + h) * 128 + ch] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
-    if (lse_out && ch == 0) lse_out[f * G + h] = total > 0.f ? m + __logf(total) : -INFINITY;
+    o_out[(f * G + h) * 128 + ch] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
   }
   cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
