@@ -206,6 +206,9 @@ MSA_API int msa_stage_selected_kv(const uint16_t* k_cache, const uint16_t* v_cac
  *   o        [R, Hq, D] bf16 (out); lse [R, Hq] fp32 (out, may be NULL)
  *   workspace >= msa_paged_sparse_decode_workspace_size(R, Hq, Hkv, topk) bytes
  *             (one partial slot per selected page; no zero-fill needed)
+ * With few flattened rows (4 * R * Hkv <= the device's SM count, e.g. a small batch at long
+ * context) each row is computed by one cluster of 4 CTAs whose partials are merged in
+ * distributed shared memory; the workspace is then not touched.
  * The result depends only on the inputs (no run-to-run variation).
  * ------------------------------------------------------------------------------------ */
 MSA_API size_t msa_paged_sparse_decode_workspace_size(int32_t R, int32_t Hq, int32_t Hkv, int32_t topk);
