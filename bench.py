@@ -446,7 +446,17 @@ def run_ours(args, ws, rank, local):
     value = job_throughput(wsc["bytes"], max(score_ms, eps), ws) / 1e9
 
     # e2e through host buffers for the headline stage, and for the decode stage
-    e2e = e2e_score(msa, wsc, wsp, dev, args.steps, ws) if "score" in run else None
+    def rest_of_step():
+        if "decode" in run:
+            msa.build_sparse_page_table(wdc["block_ids"], wdc["page_table"], wdc["seq_lens"], 1,
+                                        wdc["num_pages"], out=(fpt_dc, len4))
+            msa.paged_sparse_decode(wdc["q"], wdc["k_cache"], wdc["v_cache"], fpt_dc, len4,
+                                    workspace=wsp, out=(o4, lse4))
+        if "prefill" in run:
+            msa.sparse_prefill(wpf["q"], wpf["k"], wpf["v"], wpf["block_ids"], workspace=wsp,
+                               out=(o3, lse3))
+
+    e2e = e2e_score(msa, wsc, wsp, dev, args.steps, ws, between=rest_of_step) if "score" in run else None
     e2e_dec = e2e_decode(msa, wdc, wsp, dev, args.steps, ws) if "decode" in run else None
     # multi-token decode / verify rows, and decode from host-resident K/V caches (outside the
     # timed step: each is its own configuration)
@@ -520,10 +530,12 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def e2e_score(msa, wsc, wsp, dev, steps: int, ws: int):
+def e2e_score(msa, wsc, wsp, dev, steps: int, ws: int, between=None):
     """Headline stage through the public API with pinned host buffers: per step the query
     index rows, page table and lengths go host->device and the selection comes back; the
-    paged K-index cache is resident state (it is written once per token, not per step)."""
+    paged K-index cache is resident state (it is written once per token, not per step).
+    `between` (untimed) runs the rest of the bench step before each timed call, so that the
+    call meets the memory system in the state the in-step headline does."""
     h_q = wsc["q_idx"].cpu().pin_memory()
     h_pt = wsc["page_table"].cpu().pin_memory()
     h_sl = wsc["seq_lens"].cpu().pin_memory()
@@ -549,19 +561,22 @@ def e2e_score(msa, wsc, wsp, dev, steps: int, ws: int):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        if between is not None:
+            between()
+        s.record()
         one()
-    e.record()
+        e.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks([s.elapsed_time(e) / steps], ws, dev)[0]
+    ms = max_over_ranks([sum(s.elapsed_time(e) for s, e in evs) / steps], ws, dev)[0]
     h2d = h_q.numel() * 2 + h_pt.numel() * 4 + h_sl.numel() * 4
     d2h = h_ids.numel() * 4 + h_sc.numel() * 4
     return {"value": round(job_throughput(wsc["bytes"], ms, ws) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "per-step inputs copied from pinned host memory; paged K-index resident"}
+            "note": "per-step inputs copied from pinned host memory; paged K-index resident; "
+                    "each timed call follows the step's other stages, as in the timed step"}
 
 
 # --------------------------------------------------------------------------- extra stages

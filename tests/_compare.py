@@ -40,7 +40,7 @@ def check_attention(o_gpu: torch.Tensor, lse_gpu, ref: dict, units=None, what=""
 
 
 def check_selection(ids_gpu: np.ndarray, ids_ref: np.ndarray, scores_ref: np.ndarray):
-    """Bit-exact block ids, except near-tie swaps judged on the oracle's block scores.
+    """Bit-exact block ids, except near-tie swaps decided on the oracle's block scores.
 
     ids_* [R, Hkv, k]; scores_ref [R, Hkv, max_blocks] (oracle block scores).
     Returns the number of (row, group) lists that differ only by near-tie swaps.
