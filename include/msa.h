@@ -14,11 +14,13 @@
  *  - GQA: Hq query heads, Hkv KV groups, G = Hq/Hkv heads per group; head h belongs to
  *    group h/G. One index head per KV group (index dim Di).
  *  - bf16 tensors are passed as uint16_t* (raw bf16 bit patterns); int32 tables as
- *    int32_t*; fp32 as float*. Every tensor is dense, row-major, in the layout stated.
+ *    int32_t*; fp32 as float*. Every tensor is dense, row-major, in the layout stated: the
+ *    calls take plain pointers and cannot see strides, so a strided view must be made
+ *    contiguous by the caller (the Python binding checks this and raises).
  *  - Query rows: request b of a batch of B requests holds N query rows r = b*N + i
  *    (i = 0..N-1) at positions seq_lens[b] - N + i, i.e. the last N tokens of the request,
  *    whose K/V/K-index are already in the cache. Decode is N = 1; multi-token decode
- *    (speculative verify) is N = 2..8; a prefill chunk of one request is B = 1, N = T.
+ *    (speculative verify) is N = 2..16; a prefill chunk of one request is B = 1, N = T.
  *  - q is pre-scaled by 1/sqrt(D): the kernels apply no softmax scale. LSE is the natural
  *    log-sum-exp of the scaled scores, fp32.
  *
@@ -111,9 +113,10 @@ MSA_API int msa_index_score_topk(const uint16_t* q_idx, const uint16_t* k_idx_pa
 
 /* ------------------------------------------------------------------------------------
  * msa_index_score_topk followed by msa_build_sparse_page_table on its selection, in one
- * call: for N <= 8 the warp that selects a row's blocks in the scorer's last CTA for the
+ * call: for N = 1 the warp that selects a row's blocks in the scorer's last CTA for the
  * request also writes the row's sparse page table and length, so no separate launch and no
- * round trip of block_ids sits between the selection and the paged decode.
+ * round trip of block_ids sits between the selection and the paged decode; for N > 1 the
+ * page-table kernel follows the top-k kernel within the call.
  *
  * Passages: as msa_index_score_topk and msa_build_sparse_page_table (Together AI MiniMax-M3
  * serving article, sections "The index scorer becomes the decode critical path" and "MSA
