@@ -76,6 +76,7 @@ struct SelectParams {
   int32_t ph;                // per-warp pair histogram length (0: windowed CTA-wide selection)
   int32_t* counts;           // [Hkv*nwin, nblk], zero on entry
   int32_t* epos;             // [T, Hkv, topk]: place of each counted selection in its list
+  bool vec4;                 // topk % 4 == 0 and block_ids 16-byte aligned: rows move as int4
 };
 
 // Blocks per pair histogram for the one-warp-per-pair selection (smaller key ranges); longer
@@ -85,8 +86,43 @@ constexpr int kPairHist = 1024;
 // atomics, whose returned place is stored) are all in flight before any result is used.
 constexpr int kIdBatch = 16;
 
+// Writes j[0..n) (a batch of one row's slots) to dst[at..]: four at a time when the batch is
+// whole and the rows are int4-aligned.
+__device__ __forceinline__ void store_batch(const SelectParams& p, int32_t* dst, int64_t at,
+                                            const int32_t (&j)[kIdBatch], int n) {
+  if (p.vec4 && n >= kIdBatch) {
+#pragma unroll
+    for (int q = 0; q < kIdBatch / 4; ++q)
+      reinterpret_cast<int4*>(dst + at)[q] = make_int4(j[4 * q], j[4 * q + 1], j[4 * q + 2], j[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int u = 0; u < kIdBatch; ++u)
+      if (u < n) dst[at + u] = j[u];
+  }
+}
+
+// Loads slots k0.. of selection row `row` (a batch; -1 past topk or for an invalid row).
+__device__ __forceinline__ void load_batch(const SelectParams& p, int64_t row, int k0, bool valid,
+                                           int32_t (&j)[kIdBatch]) {
+  if (p.vec4 && k0 + kIdBatch <= p.topk) {
+    const int4* src = reinterpret_cast<const int4*>(p.block_ids + row * p.topk + k0);
+#pragma unroll
+    for (int q = 0; q < kIdBatch / 4; ++q) {
+      const int4 v = valid ? src[q] : make_int4(-1, -1, -1, -1);
+      j[4 * q] = v.x;
+      j[4 * q + 1] = v.y;
+      j[4 * q + 2] = v.z;
+      j[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kIdBatch; ++u)
+      j[u] = valid && k0 + u < p.topk ? p.block_ids[row * p.topk + k0 + u] : -1;
+  }
+}
+
 // Counts up to kIdBatch selections (ids j[], -1 = none; `n` of them valid slots) of one row into
-// their lists; each one's place in its list goes to epos[at + u].
+// their lists; each one's place in its list goes to epos[at + u] (-1 for a slot not counted).
 __device__ __forceinline__ void count_batch(const SelectParams& p, const int32_t (&j)[kIdBatch],
                                             int64_t list0, int64_t at, int n) {
   int32_t pos[kIdBatch];
@@ -98,9 +134,7 @@ __device__ __forceinline__ void count_batch(const SelectParams& p, const int32_t
       else msa_record_error(kErrBadBlock);
     }
   }
-#pragma unroll
-  for (int u = 0; u < kIdBatch; ++u)
-    if (pos[u] >= 0) p.epos[at + u] = pos[u];
+  store_batch(p, p.epos, at, pos, n);
 }
 
 // One CTA per (group g, 128-query span), one thread per query of the span. The span's ids are
@@ -139,9 +173,7 @@ __global__ void __launch_bounds__(kSpan)
     const int64_t list0 = ((int64_t)g * p.nwin + t_me / p.win) * p.nblk;
     for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
       int32_t j[kIdBatch];
-#pragma unroll
-      for (int u = 0; u < kIdBatch; ++u)
-        j[u] = k0 + u < p.topk ? p.block_ids[row_me * p.topk + k0 + u] : -1;
+      load_batch(p, row_me, k0, true, j);
       count_batch(p, j, list0, row_me * p.topk + k0, p.topk - k0);
     }
     return;
@@ -152,9 +184,7 @@ __global__ void __launch_bounds__(kSpan)
   uint8_t* hist = sel_smem + (size_t)kSpan * p.topk * 4;
   for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
     int32_t j[kIdBatch];  // a row's ids requested together, then stored
-#pragma unroll
-    for (int u = 0; u < kIdBatch; ++u)
-      j[u] = valid && k0 + u < p.topk ? p.block_ids[row_me * p.topk + k0 + u] : -1;
+    load_batch(p, row_me, k0, valid, j);
 #pragma unroll
     for (int u = 0; u < kIdBatch; ++u)
       if (k0 + u < p.topk) s_ids[(k0 + u) * kSpan + r] = j[u];
@@ -221,9 +251,11 @@ __global__ void __launch_bounds__(kSpan)
   const int nq = 2 * p.qpt;
   const int pairs = kSpan / nq;
   const int64_t nb = (p.q_start + span * kSpan + nvalid - 1) / 128 + 1;  // blocks the span sees
-  for (int rr = r; rr < kSpan * p.G; rr += kSpan) {
-    const int32_t t = s_query[rr / p.G];
-    if (t >= 0) p.part_lse[((int64_t)t * p.Hkv + g) * p.G + rr % p.G] = -INFINITY;
+  for (int rr = r; rr < kSpan * p.G / 4; rr += kSpan) {  // G 8 / 16: four heads per store
+    const int32_t t = s_query[rr / (p.G / 4)];
+    if (t >= 0)
+      reinterpret_cast<float4*>(p.part_lse + ((int64_t)t * p.Hkv + g) * p.G)[rr % (p.G / 4)] =
+          make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   }
   if (p.ph > 0 && nb <= p.ph) {
     // one warp per pair (pairs of 32 slots) or per two pairs (16 slots): lane = slot of the pair
@@ -346,10 +378,8 @@ __global__ void __launch_bounds__(kSpan)
   for (int k0 = 0; k0 < p.topk; k0 += kIdBatch) {
     int32_t j[kIdBatch];
 #pragma unroll
-    for (int u = 0; u < kIdBatch; ++u) {
-      j[u] = k0 + u < p.topk ? s_ids[(k0 + u) * kSpan + r] : -1;
-      if (k0 + u < p.topk) p.residual[row_me * p.topk + k0 + u] = j[u];
-    }
+    for (int u = 0; u < kIdBatch; ++u) j[u] = k0 + u < p.topk ? s_ids[(k0 + u) * kSpan + r] : -1;
+    store_batch(p, p.residual, row_me * p.topk + k0, j, p.topk - k0);
     count_batch(p, j, list0, row_me * p.topk + k0, p.topk - k0);
   }
 }
@@ -409,6 +439,7 @@ cudaError_t launch_select_count(const int32_t* block_ids, int32_t T, int64_t S_k
   p.nwin = (T + win - 1) / win;
   p.counts = counts;
   p.epos = epos;
+  p.vec4 = (topk % 4) == 0 && (reinterpret_cast<uintptr_t>(block_ids) & 15) == 0;
   p.ph = pair_hist_len(S_kv);
   const size_t smem = p.hybrid ? select_count_smem_bytes(S_kv, G, topk) : 16;
   cudaError_t e = cudaFuncSetAttribute(select_count_kernel,
