@@ -308,50 +308,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-    if (warp == 0) {
-      // ================================================================ producer (whole warp)
-      // Each lane gathers the query rows of up to kMaxQPerLane query slots of the tile (lane,
-      // lane+32, ...). Descriptors are prefetched two tiles ahead and entries one tile ahead so
-      // that no global-memory latency sits between two tiles' copies.
-      if (lane == 0) {
-        tma_prefetch_desc(&qmap);
+    if (warp == 0 || warp == 3) {
+      // ================================================================ query producers
+      // Warps 0 and 3 gather the query rows of alternate tiles (warp 0 the even ones): each
+      // lane copies up to kMaxQPerLane query slots of the tile (lane, lane+32, ...) with one
+      // tensor copy per query. A warp's tensor copies issue one after another, about a
+      // hundred cycles each under load (measured), so one warp alone bounds the tile rate.
+      // Descriptors are read two of the warp's tiles ahead and entries one, so that no
+      // global-memory latency sits between two tiles' copies.
+      if (lane == 0 && warp == 0) tma_prefetch_desc(&qmap);
+      if (lane == 0 && warp == 3) {
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
       }
       constexpr int kMaxQPerLane = 4;  // qpt = 128/G <= 128
-      int4 d0 = load_desc(p, tile_of(0));
-      int4 d1 = n > 1 ? load_desc(p, tile_of(1)) : d0;
-      int32_t e0[kMaxQPerLane];
+      const int qw = warp == 0 ? 0 : 1;
+      const int4 dz = make_int4(0, 0, 0, 0);
+      auto load_entries = [&](const int4 d, int32_t (&e)[kMaxQPerLane]) {
   #pragma unroll
-      for (int r = 0; r < kMaxQPerLane; ++r) {
-        const int q = lane + 32 * r;
-        e0[r] = q < d0.z ? p.entries[d0.y + q] : -1;
-      }
-      for (int i = 0; i < n; ++i) {
-        const int qs = i % kQStages;
-        const int4 d = d0;
-        int32_t e[kMaxQPerLane];
-  #pragma unroll
-        for (int r = 0; r < kMaxQPerLane; ++r) e[r] = e0[r];
-        if (i + 1 < n) {  // prefetch: entries of tile i+1, descriptor of tile i+2
-  #pragma unroll
-          for (int r = 0; r < kMaxQPerLane; ++r) {
-            const int q = lane + 32 * r;
-            e0[r] = q < d1.z ? p.entries[d1.y + q] : -1;
-          }
-          d0 = d1;
-          if (i + 2 < n) d1 = load_desc(p, tile_of(i + 2));
+        for (int r = 0; r < kMaxQPerLane; ++r) {
+          const int q = lane + 32 * r;
+          e[r] = q < d.z ? p.entries[d.y + q] : -1;
         }
+      };
+      int4 dc = qw < n ? load_desc(p, tile_of(qw)) : dz;              // tile i
+      int4 dn = qw + 2 < n ? load_desc(p, tile_of(qw + 2)) : dz;      // tile i+2
+      int4 dnn = qw + 4 < n ? load_desc(p, tile_of(qw + 4)) : dz;     // tile i+4
+      int32_t ec[kMaxQPerLane], en[kMaxQPerLane];
+      load_entries(dc, ec);
+      load_entries(dn, en);
+      for (int i = qw; i < n; i += 2) {
+        const int qs = i % kQStages;
         if (i >= kQStages && !wait_or_fail(&B.q_empty[qs], (i / kQStages - 1) & 1, fail)) break;
-        const int g = (int)(d.x / lists_per_group);
+        const int g = (int)(dc.x / lists_per_group);
         uint8_t* qdst = smem + kOffQ + qs * kTileBytes;
-        if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(d.z * p.G * 256));
+        if (lane == 0) mbar_expect_tx(&B.q_full[qs], (uint32_t)(dc.z * p.G * 256));
         __syncwarp();
   #pragma unroll
         for (int r = 0; r < kMaxQPerLane; ++r) {
           const int q = lane + 32 * r;
-          if (q < d.z) {
-            const int t = e[r] / p.topk;
+          if (q < dc.z) {
+            const int t = ec[r] / p.topk;
             if (p.q_atoms) {
               tma_load_5d(qdst + q * p.G * 256, &qmap, &B.q_full[qs], 0, 0, 0, 0, t * p.Hkv + g);
             } else {
@@ -360,6 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // shift the read-ahead by one of this warp's tiles
+        dc = dn;
+        dn = dnn;
+  #pragma unroll
+        for (int r = 0; r < kMaxQPerLane; ++r) ec[r] = en[r];
+        load_entries(i + 4 < n ? dnn : dz, en);
+        dnn = i + 6 < n ? load_desc(p, tile_of(i + 6)) : dz;
       }
       __syncwarp();
     } else if (warp == 2) {
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ent >= 0) {
         const int64_t t = ent / p.topk;
         const int64_t prow_idx = ((t * p.Hkv + d.x / lists_per_group) * p.topk + ent % p.topk) * G + h;
-        p.part_lse[prow_idx] = l > 0.f ? mx + __logf(l) : -INFINITY;
+        __stcs(p.part_lse + prow_idx, l > 0.f ? mx + __logf(l) : -INFINITY);
         uint4* dst = reinterpret_cast<uint4*>(p.part_o) + prow_idx;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           u.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
           u.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
           u.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
-          dst[(int64_t)c * p.part_rows] = u;
+          __stcs(dst + (int64_t)c * p.part_rows, u);  // read once, by the merge
         }
       }
       __syncwarp();

@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_fence_before();
       if (valid) {
         const int64_t prow = (t * p.Hkv + g) * G + h;
-        p.part_lse[prow] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+        __stcs(p.part_lse + prow, l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY);
         const float inv = l > 0.f ? 1.0f / l : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(p.part_o) + prow;
 #pragma unroll
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           u.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
           u.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
           u.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
-          dst[(int64_t)c * p.part_rows] = u;
+          __stcs(dst + (int64_t)c * p.part_rows, u);  // read once, by the merge
         }
       }
       __syncwarp();
