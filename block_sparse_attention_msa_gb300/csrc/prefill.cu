@@ -687,6 +687,7 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const int32_t* ids = a.block_ids;
   if (hybrid) {
     dw.qperm = reinterpret_cast<int32_t*>(a.workspace + W.qperm);
+    dw.porder = reinterpret_cast<int32_t*>(a.workspace + W.porder);
     dw.residual = reinterpret_cast<int32_t*>(a.workspace + W.residual);
     dw.dcnt = reinterpret_cast<int32_t*>(a.workspace + W.dcnt);
     dw.dblk = reinterpret_cast<int32_t*>(a.workspace + W.dblk);

@@ -492,6 +492,8 @@ struct DenseKParams {
   int32_t T, Hkv, G, qpt, ppg, q_atoms;
   int64_t npairs, q_start;
   int64_t pair0;              // first pair of this launch (launches cover kMaxRounds rounds)
+  const int32_t* porder;      // pair of each (round, CTA) slot, -1: none
+  int64_t nslots;             // slots in porder: whole rounds of gridDim.x
   const int32_t* page_table;  // null: contiguous K/V; else the page of each block
   int64_t num_pages;
   uint16_t* part_o;   // chunk-major [16][part_rows][8] bf16
@@ -507,13 +509,71 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   return false;
 }
 
-// The r-th pair of this CTA (-1: none). Round r covers pairs [r*grid, (r+1)*grid), and the
-// CTA's place in it moves by one each round: pairs are ordered by span and the ordered spans
-// put light pairs (few shared blocks) at fixed positions, which a fixed place would hand to
-// the same CTAs every round.
-__device__ __forceinline__ int64_t cta_pair(int64_t r, int64_t pair0, int64_t npairs) {
-  const int64_t pr = pair0 + r * gridDim.x + (blockIdx.x + r) % gridDim.x;
-  return pr < npairs ? pr : -1;
+// The pair of this CTA in round r (-1: none), from the deal written by pair_deal_kernel.
+__device__ __forceinline__ int64_t cta_pair(const DenseKParams& p, int64_t r) {
+  const int64_t idx = p.pair0 + r * gridDim.x + blockIdx.x;
+  return idx < p.nslots ? p.porder[idx] : -1;
+}
+
+// Deal of the pairs to the persistent CTAs, one CTA per window of `rounds_per_window` rounds
+// (rounds_per_window * grid consecutive pairs, at most the block size): a CTA's time is close
+// to proportional to its blocks, and a plain round-robin deal leaves some CTAs about 8 % more
+// blocks than the mean, which the kernel's end waits for. Within the window the pairs are
+// ranked by block count (descending; ties by pair index) and rank i goes to round i / grid,
+// place i % grid on even rounds and grid - 1 - i % grid on odd ones, so that each CTA's sum is
+// near the window's mean; the places map to CTAs turned by 97 per window. Windows keep the pairs that run at once near one another in the
+// chunk, which keeps their K/V blocks in L2. Slots past the last pair get -1.
+__global__ void __launch_bounds__(1024)
+    pair_deal_kernel(const int32_t* __restrict__ dcnt, int64_t npairs, int32_t grid,
+                     int32_t rounds_per_window, int32_t* __restrict__ porder) {
+  __shared__ int32_t cnt[32][kMaxDense + 1];  // per warp and block count: pairs, then prefix
+  __shared__ int32_t base[kMaxDense + 1];     // per block count: first rank
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int W = rounds_per_window * grid;
+  const int64_t w0 = (int64_t)blockIdx.x * W;
+  for (int i = tid; i < 32 * (kMaxDense + 1); i += blockDim.x) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+  const bool valid = tid < W && w0 + tid < npairs;
+  int L = -1;
+  if (valid) {
+    const int c = dcnt[w0 + tid];
+    L = c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c);
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, L);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank_in_warp == 0) cnt[warp][L] = __popc(peers);
+  __syncthreads();
+  if (tid <= kMaxDense) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w][tid];
+      cnt[w][tid] = run;
+      run += c;
+    }
+    base[tid] = run;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = kMaxDense; b >= 0; --b) {
+      const int c = base[b];
+      base[b] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  if (tid < W) {
+    const int nvalid = (int)min((int64_t)W, npairs - w0);
+    // valid pairs take ranks [0, nvalid), the empty ranks [nvalid, W) get no pair
+    const int rank = valid ? base[L] + cnt[warp][L] + rank_in_warp : tid;
+    if (valid || tid >= nvalid) {
+      const int rl = rank / grid, place = rank % grid;
+      // the snake, turned by a stride prime to the grid from one window to the next, so that
+      // the heaviest pair of every window (rank 0) does not always land on the same CTA
+      const int cta = (int)(((rl & 1 ? grid - 1 - place : place) + blockIdx.x * 97LL) % grid);
+      porder[w0 + (int64_t)rl * grid + cta] = valid ? (int32_t)(w0 + tid) : -1;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -548,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   {
-    const int nr = (int)min((int64_t)kMaxRounds, (p.npairs - p.pair0 + gridDim.x - 1) / gridDim.x);
+    const int nr = (int)min((int64_t)kMaxRounds, (p.nslots - p.pair0) / gridDim.x);
     for (int r = tid; r < nr; r += kThreads) {
-      const int64_t pr = cta_pair(r, p.pair0, p.npairs);
+      const int64_t pr = cta_pair(p, r);
       const int c = pr < 0 ? 0 : p.dcnt[pr];
       smem[kOffCnt + r] = (uint8_t)(c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c));
     }
@@ -561,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = B.tmem_base;
   const uint32_t sbase = smem_u32(smem);
   const int G = p.G, qpt = p.qpt;
-  const int rounds = (int)min((int64_t)kMaxRounds, (p.npairs - p.pair0 + gridDim.x - 1) / gridDim.x);
+  const int rounds = (int)min((int64_t)kMaxRounds, (p.nslots - p.pair0) / gridDim.x);
   uint8_t* rcnt = smem + kOffCnt;  // blocks of this CTA's pair of round r
 
   static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split");
@@ -579,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && !*fail; ++r) {
         const int L = rcnt[r];
         if (L == 0) continue;
-        const int64_t pr = cta_pair(r, p.pair0, p.npairs);
+        const int64_t pr = cta_pair(p, r);
         const int g = (int)(pr / p.ppg);
         const int64_t t0 = (pr % p.ppg) * 2 * qpt;  // first pair slot
         const int64_t tq = lane < 2 * qpt ? slot_query(p.qperm, p.npos, g, t0 + lane, p.T) : -1;
@@ -753,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < rounds && !*fail; ++r) {
       const int L = rcnt[r];
       if (L == 0) continue;
-      const int64_t pr = cta_pair(r, p.pair0, p.npairs);
+      const int64_t pr = cta_pair(p, r);
       const int g = (int)(pr / p.ppg);
       const int64_t t = slot_query(p.qperm, p.npos, g, (pr % p.ppg) * 2 * qpt + X * qpt + qi, p.T);
       const bool valid = t >= 0;
@@ -912,9 +972,21 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
   e = cudaFuncGetAttributes(&fa, prefill_dense_tc_kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  const int64_t grid = std::min<int64_t>(p.npairs, sm_count());
+  const int64_t grid = std::min<int64_t>(std::min<int64_t>(p.npairs, sm_count()), kMaxPairGrid);
+  // the deal: windows of a power-of-two number of rounds (at most 8, at most 1024 pairs; a
+  // divisor of kMaxRounds, so that no window straddles two launches)
+  int32_t rpw = 1;
+  while (rpw < 8 && 2 * rpw * grid <= 1024) rpw *= 2;
+  const int64_t W = rpw * grid;
+  const int64_t nwin = (p.npairs + W - 1) / W;
+  p.porder = w.porder;
+  p.nslots = nwin * W;
+  pair_deal_kernel<<<(unsigned)nwin, 1024, 0, stream>>>(w.dcnt, p.npairs, (int32_t)grid, rpw,
+                                                        w.porder);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   // one launch per kMaxRounds rounds of pairs (the per-round counts live in shared memory)
-  for (int64_t pair0 = 0; pair0 < p.npairs; pair0 += grid * kMaxRounds) {
+  for (int64_t pair0 = 0; pair0 < p.nslots; pair0 += grid * kMaxRounds) {
     p.pair0 = pair0;
     prefill_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
     e = cudaGetLastError();
