@@ -190,6 +190,10 @@ cudaError_t launch_select_count(const int32_t* block_ids, int32_t T, int64_t S_k
                                 int32_t G, int32_t topk, int32_t nblk, int32_t win,
                                 const DenseWorkspace& w, int32_t* counts, int32_t* epos,
                                 cudaStream_t stream);
+// The deal of the pairs to the query-major kernel's CTAs (w.porder), from the pairs' block
+// counts; any time between launch_select_count and launch_dense_attention.
+cudaError_t launch_pair_deal(int32_t T, int32_t Hkv, int32_t G, const DenseWorkspace& w,
+                             cudaStream_t stream);
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
                                    int64_t S_kv, int32_t Hkv, int32_t G,

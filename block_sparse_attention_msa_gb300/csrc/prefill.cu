@@ -703,6 +703,10 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   e = launch_select_count(a.block_ids, a.T, a.S_kv, a.Hkv, G, a.topk, a.nblk, win, dw, counts,
                           epos, stream);
   if (e != cudaSuccess) return e;
+  if (hybrid) {  // the pairs' deal to the query-major CTAs, here rather than between the passes
+    e = launch_pair_deal(a.T, a.Hkv, G, dw, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = launch_bucket_lists(ids, epos, a.T, a.Hkv, a.topk, a.nblk, win, qpt, counts, offsets,
                           entries, group_base, tile_offsets, tile_desc, stream);
   if (e != cudaSuccess) return e;

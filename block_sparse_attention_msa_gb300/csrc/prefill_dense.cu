@@ -940,6 +940,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+// Geometry of the pair deal: the persistent CTAs, and windows of a power-of-two number of
+// rounds (at most 8, at most 1024 pairs; a divisor of kMaxRounds, so that no window straddles
+// two launches).
+struct PairDeal {
+  int64_t grid;
+  int32_t rpw;
+  int64_t nwin, nslots;
+};
+PairDeal pair_deal_geometry(int64_t npairs) {
+  PairDeal d;
+  d.grid = std::min<int64_t>(std::min<int64_t>(npairs, sm_count()), kMaxPairGrid);
+  d.rpw = 1;
+  while (d.rpw < 8 && 2 * d.rpw * d.grid <= 1024) d.rpw *= 2;
+  const int64_t W = d.rpw * d.grid;
+  d.nwin = (npairs + W - 1) / W;
+  d.nslots = d.nwin * W;
+  return d;
+}
+}  // namespace
+
+cudaError_t launch_pair_deal(int32_t T, int32_t Hkv, int32_t G, const DenseWorkspace& w,
+                             cudaStream_t stream) {
+  const int64_t npairs = prefill_pairs(T, Hkv, G);
+  if (npairs <= 0) return cudaSuccess;
+  const PairDeal d = pair_deal_geometry(npairs);
+  pair_deal_kernel<<<(unsigned)d.nwin, 1024, 0, stream>>>(w.dcnt, npairs, (int32_t)d.grid, d.rpw,
+                                                          w.porder);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
                                    int64_t S_kv, int32_t Hkv, int32_t G,
@@ -972,19 +1003,10 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
   e = cudaFuncGetAttributes(&fa, prefill_dense_tc_kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  const int64_t grid = std::min<int64_t>(std::min<int64_t>(p.npairs, sm_count()), kMaxPairGrid);
-  // the deal: windows of a power-of-two number of rounds (at most 8, at most 1024 pairs; a
-  // divisor of kMaxRounds, so that no window straddles two launches)
-  int32_t rpw = 1;
-  while (rpw < 8 && 2 * rpw * grid <= 1024) rpw *= 2;
-  const int64_t W = rpw * grid;
-  const int64_t nwin = (p.npairs + W - 1) / W;
+  const PairDeal pd = pair_deal_geometry(p.npairs);
+  const int64_t grid = pd.grid;
   p.porder = w.porder;
-  p.nslots = nwin * W;
-  pair_deal_kernel<<<(unsigned)nwin, 1024, 0, stream>>>(w.dcnt, p.npairs, (int32_t)grid, rpw,
-                                                        w.porder);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  p.nslots = pd.nslots;
   // one launch per kMaxRounds rounds of pairs (the per-round counts live in shared memory)
   for (int64_t pair0 = 0; pair0 < p.nslots; pair0 += grid * kMaxRounds) {
     p.pair0 = pair0;
