@@ -301,7 +301,7 @@ def prefill_stage(wpf, pre_ms, pk):
             "frac_bf16": round(tfl / pk["bf16_tflops"], 4),
             "peak": pk["bf16_tflops"], "peak_kind": "burst (measured)",
             "frac_bf16_sustained": round(tfl / pk["bf16_tflops_sustained"], 4),
-            "kernels": "selection + counting; pair deal; list offsets; placement; block-major attention "
+            "kernels": "selection + counting; list offsets + pair deal; placement; block-major attention "
                        "for the scattered selections; query-major attention for blocks shared "
                        "by a query pair; LSE merge "
                        "(per-kernel times: profiles/launches_bench_default.md)",
@@ -348,8 +348,7 @@ def recorded_traffic(kernel: str, source_hash: str):
 
 
 # Every kernel of one msa_sparse_prefill call and the source file it is built from.
-PREFILL_KERNELS = (("select_count_kernel", "prefill_dense.cu"), ("pair_deal_kernel", "prefill_dense.cu"),
-                   ("bucket_lists_kernel", "prefill.cu"),
+PREFILL_KERNELS = (("select_count_kernel", "prefill_dense.cu"), ("bucket_lists_kernel", "prefill.cu"),
                    ("bucket_place_kernel", "prefill.cu"), ("prefill_block_tc_kernel", "prefill.cu"),
                    ("prefill_dense_tc_kernel", "prefill_dense.cu"),
                    ("lse_merge_chunked_kernel", "page_table_merge.cu"))
@@ -502,10 +501,10 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "stages": stages, "e2e": e2e,
         # kernels of this library per step: scorer with its top-k (1); page table, decode,
-        # merge (3); selection with counting, pair deal, list offsets, placement, block-major
-        # attention, query-major attention, merge (7). Memsets not counted.
+        # merge (3); selection with counting, list offsets with the query-major pairs' deal,
+        # placement, block-major attention, query-major attention, merge (6). Memsets not counted.
         "gpu_launches": args.steps * (("score" in run) * 1 + ("decode" in run) * 3
-                                      + ("prefill" in run) * 7),
+                                      + ("prefill" in run) * 6),
         "clocks": clk.summary(), "device_error_word": err,
     }
     for key, name in (("score", "index_score_topk"), ("decode", "sparse_decode"), ("prefill", "sparse_prefill")):

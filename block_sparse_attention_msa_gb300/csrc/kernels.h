@@ -190,10 +190,6 @@ cudaError_t launch_select_count(const int32_t* block_ids, int32_t T, int64_t S_k
                                 int32_t G, int32_t topk, int32_t nblk, int32_t win,
                                 const DenseWorkspace& w, int32_t* counts, int32_t* epos,
                                 cudaStream_t stream);
-// The deal of the pairs to the query-major kernel's CTAs (w.porder), from the pairs' block
-// counts; any time between launch_select_count and launch_dense_attention.
-cudaError_t launch_pair_deal(int32_t T, int32_t Hkv, int32_t G, const DenseWorkspace& w,
-                             cudaStream_t stream);
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
                                    int64_t S_kv, int32_t Hkv, int32_t G,
@@ -204,11 +200,13 @@ cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& k
 // List of selection (t, slot) of group g: ((g * nwin + t / win) * nblk + j); the per-list
 // offsets are relative to their (group, window) segment, segments in (g, w) order.
 // launch_bucket_lists finishes lists counted by launch_select_count (offsets, tile descriptors
-// when `desc` is set, entries); launch_bucket runs all of it on plain selections.
+// when `desc` is set, entries; with `dcnt` also the query-major pairs' deal into `porder`, in
+// extra blocks); launch_bucket runs all of it on plain selections.
 cudaError_t launch_bucket_lists(const int32_t* ids, const int32_t* epos, int32_t T, int32_t Hkv,
                                 int32_t topk, int32_t nblk, int32_t win, int32_t qpt,
                                 const int32_t* counts, int32_t* offsets, int32_t* entries,
                                 int32_t* group_base, int32_t* tile_offsets, int4* desc,
+                                const int32_t* dcnt, int64_t npairs, int32_t* porder,
                                 cudaStream_t stream);
 cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int32_t topk,
                           int32_t nblk, int32_t win, int32_t qpt, int32_t* offsets,

@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "pair_deal.cuh"
 #include "softmax_math.cuh"
 
 MSA_DEFINE_ERROR_WORD(pre)
@@ -80,7 +81,14 @@ __global__ void __launch_bounds__(kListThreads)
     bucket_lists_kernel(const int32_t* __restrict__ counts, int32_t nseg, int32_t nblk,
                         int32_t qpt, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ tile_local, int32_t* __restrict__ group_base,
-                        int32_t* __restrict__ seg_tile_base, int4* __restrict__ desc) {
+                        int32_t* __restrict__ seg_tile_base, int4* __restrict__ desc,
+                        const int32_t* __restrict__ dcnt, int64_t npairs, int32_t deal_grid,
+                        int32_t deal_rpw, int32_t* __restrict__ porder) {
+  // blocks past the segments deal the query-major pairs, one window each (same launch)
+  if (blockIdx.x >= (unsigned)nseg) {
+    pair_deal_window(dcnt, npairs, deal_grid, deal_rpw, porder, (int64_t)blockIdx.x - nseg);
+    return;
+  }
   extern __shared__ int32_t seg_tot[];  // [2 * nseg]: entries, tiles per segment
   __shared__ int warp_sums[33];
   __shared__ int32_t s_base[2];
@@ -624,6 +632,7 @@ cudaError_t launch_bucket_lists(const int32_t* ids, const int32_t* epos, int32_t
                                 int32_t topk, int32_t nblk, int32_t win, int32_t qpt,
                                 const int32_t* counts, int32_t* offsets, int32_t* entries,
                                 int32_t* group_base, int32_t* tile_offsets, int4* desc,
+                                const int32_t* dcnt, int64_t npairs, int32_t* porder,
                                 cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int32_t nwin = (T + win - 1) / win;
@@ -638,9 +647,11 @@ cudaError_t launch_bucket_lists(const int32_t* ids, const int32_t* epos, int32_t
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  bucket_lists_kernel<<<nseg, kListThreads, smem, stream>>>(counts, nseg, nblk, qpt, offsets,
-                                                            tile_local, group_base, seg_tile_base,
-                                                            desc);
+  // the query-major pairs' deal in extra blocks, one per window
+  const PairDeal deal = dcnt && npairs > 0 ? pair_deal_geometry(npairs) : PairDeal{1, 1, 0, 0};
+  bucket_lists_kernel<<<(unsigned)(nseg + deal.nwin), kListThreads, smem, stream>>>(
+      counts, nseg, nblk, qpt, offsets, tile_local, group_base, seg_tile_base, desc, dcnt, npairs,
+      (int32_t)deal.grid, deal.rpw, porder);
   const int32_t rows = T * Hkv;  // T*Hkv*topk fits in int32 (checked by the callers)
   const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 255) / 256, (int64_t)sm_count() * 8));
   const bool vec4 = topk % 4 == 0 && (reinterpret_cast<uintptr_t>(ids) & 15) == 0 &&
@@ -662,7 +673,8 @@ cudaError_t launch_bucket(const int32_t* block_ids, int32_t T, int32_t Hkv, int3
                           DenseWorkspace{}, counts, epos, stream);
   if (e != cudaSuccess) return e;
   return launch_bucket_lists(block_ids, epos, T, Hkv, topk, nblk, win, qpt, counts, offsets,
-                             entries, group_base, tile_offsets, nullptr, stream);
+                             entries, group_base, tile_offsets, nullptr, nullptr, 0, nullptr,
+                             stream);
 }
 
 cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
@@ -703,12 +715,10 @@ cudaError_t launch_sparse_prefill(const PrefillArgs& a, cudaStream_t stream) {
   e = launch_select_count(a.block_ids, a.T, a.S_kv, a.Hkv, G, a.topk, a.nblk, win, dw, counts,
                           epos, stream);
   if (e != cudaSuccess) return e;
-  if (hybrid) {  // the pairs' deal to the query-major CTAs, here rather than between the passes
-    e = launch_pair_deal(a.T, a.Hkv, G, dw, stream);
-    if (e != cudaSuccess) return e;
-  }
+  // the list offsets, with the query-major pairs' deal to the CTAs in the same launch
   e = launch_bucket_lists(ids, epos, a.T, a.Hkv, a.topk, a.nblk, win, qpt, counts, offsets,
-                          entries, group_base, tile_offsets, tile_desc, stream);
+                          entries, group_base, tile_offsets, tile_desc, hybrid ? dw.dcnt : nullptr,
+                          hybrid ? prefill_pairs(a.T, a.Hkv, G) : 0, dw.porder, stream);
   if (e != cudaSuccess) return e;
 
   CUtensorMap qmap, kmap, vmap;

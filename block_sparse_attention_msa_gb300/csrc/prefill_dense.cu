@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "pair_deal.cuh"
 #include "softmax_math.cuh"
 
 MSA_DEFINE_ERROR_WORD(dense)
@@ -509,72 +510,12 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   return false;
 }
 
-// The pair of this CTA in round r (-1: none), from the deal written by pair_deal_kernel.
+// The pair of this CTA in round r (-1: none), from the deal written by pair_deal_window.
 __device__ __forceinline__ int64_t cta_pair(const DenseKParams& p, int64_t r) {
   const int64_t idx = p.pair0 + r * gridDim.x + blockIdx.x;
   return idx < p.nslots ? p.porder[idx] : -1;
 }
 
-// Deal of the pairs to the persistent CTAs, one CTA per window of `rounds_per_window` rounds
-// (rounds_per_window * grid consecutive pairs, at most the block size): a CTA's time is close
-// to proportional to its blocks, and a plain round-robin deal leaves some CTAs about 8 % more
-// blocks than the mean, which the kernel's end waits for. Within the window the pairs are
-// ranked by block count (descending; ties by pair index) and rank i goes to round i / grid,
-// place i % grid on even rounds and grid - 1 - i % grid on odd ones, so that each CTA's sum is
-// near the window's mean; the places map to CTAs turned by 97 per window. Windows keep the pairs that run at once near one another in the
-// chunk, which keeps their K/V blocks in L2. Slots past the last pair get -1.
-__global__ void __launch_bounds__(1024)
-    pair_deal_kernel(const int32_t* __restrict__ dcnt, int64_t npairs, int32_t grid,
-                     int32_t rounds_per_window, int32_t* __restrict__ porder) {
-  __shared__ int32_t cnt[32][kMaxDense + 1];  // per warp and block count: pairs, then prefix
-  __shared__ int32_t base[kMaxDense + 1];     // per block count: first rank
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int W = rounds_per_window * grid;
-  const int64_t w0 = (int64_t)blockIdx.x * W;
-  for (int i = tid; i < 32 * (kMaxDense + 1); i += blockDim.x) (&cnt[0][0])[i] = 0;
-  __syncthreads();
-  const bool valid = tid < W && w0 + tid < npairs;
-  int L = -1;
-  if (valid) {
-    const int c = dcnt[w0 + tid];
-    L = c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c);
-  }
-  const unsigned peers = __match_any_sync(0xffffffffu, L);
-  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
-  if (valid && rank_in_warp == 0) cnt[warp][L] = __popc(peers);
-  __syncthreads();
-  if (tid <= kMaxDense) {
-    int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int c = cnt[w][tid];
-      cnt[w][tid] = run;
-      run += c;
-    }
-    base[tid] = run;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int b = kMaxDense; b >= 0; --b) {
-      const int c = base[b];
-      base[b] = acc;
-      acc += c;
-    }
-  }
-  __syncthreads();
-  if (tid < W) {
-    const int nvalid = (int)min((int64_t)W, npairs - w0);
-    // valid pairs take ranks [0, nvalid), the empty ranks [nvalid, W) get no pair
-    const int rank = valid ? base[L] + cnt[warp][L] + rank_in_warp : tid;
-    if (valid || tid >= nvalid) {
-      const int rl = rank / grid, place = rank % grid;
-      // the snake, turned by a stride prime to the grid from one window to the next, so that
-      // the heaviest pair of every window (rank 0) does not always land on the same CTA
-      const int cta = (int)(((rl & 1 ? grid - 1 - place : place) + blockIdx.x * 97LL) % grid);
-      porder[w0 + (int64_t)rl * grid + cta] = valid ? (int32_t)(w0 + tid) : -1;
-    }
-  }
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_dense_tc_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -939,37 +880,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-
-namespace {
-// Geometry of the pair deal: the persistent CTAs, and windows of a power-of-two number of
-// rounds (at most 8, at most 1024 pairs; a divisor of kMaxRounds, so that no window straddles
-// two launches).
-struct PairDeal {
-  int64_t grid;
-  int32_t rpw;
-  int64_t nwin, nslots;
-};
-PairDeal pair_deal_geometry(int64_t npairs) {
-  PairDeal d;
-  d.grid = std::min<int64_t>(std::min<int64_t>(npairs, sm_count()), kMaxPairGrid);
-  d.rpw = 1;
-  while (d.rpw < 8 && 2 * d.rpw * d.grid <= 1024) d.rpw *= 2;
-  const int64_t W = d.rpw * d.grid;
-  d.nwin = (npairs + W - 1) / W;
-  d.nslots = d.nwin * W;
-  return d;
-}
-}  // namespace
-
-cudaError_t launch_pair_deal(int32_t T, int32_t Hkv, int32_t G, const DenseWorkspace& w,
-                             cudaStream_t stream) {
-  const int64_t npairs = prefill_pairs(T, Hkv, G);
-  if (npairs <= 0) return cudaSuccess;
-  const PairDeal d = pair_deal_geometry(npairs);
-  pair_deal_kernel<<<(unsigned)d.nwin, 1024, 0, stream>>>(w.dcnt, npairs, (int32_t)d.grid, d.rpw,
-                                                          w.porder);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_dense_attention(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int32_t q_atoms, int32_t T,
