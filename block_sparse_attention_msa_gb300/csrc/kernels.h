@@ -91,10 +91,8 @@ cudaError_t launch_lse_merge_chunked(const void* part_o, const float* lse_parts,
 // each 256-byte aligned.
 // Query-major part (G in {8, 16}): pairs of 128/G-query tiles, at most kMaxDense shared blocks each.
 constexpr int kMaxDense = 64;
-// Most persistent CTAs of the query-major kernel, and most pairs in one window of its deal (the
-// deal pads the pairs to whole windows of rounds).
+// Most persistent CTAs of the query-major kernel (the pair deal pads the pairs to whole rounds).
 constexpr int kMaxPairGrid = 1024;
-constexpr int kMaxDealWindow = 2048;
 inline bool prefill_hybrid(int32_t G) { return G == 8 || G == 16; }
 inline int64_t prefill_pairs(int64_t T, int32_t Hkv, int32_t G) {
   const int64_t q2 = 2 * (128 / G);
@@ -155,7 +153,7 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
       w.dense_o = off;    off = ws_align(off + 2 * rows * 128);
       w.dense_lse = off;  off = ws_align(off + 4 * rows);
       w.qperm = off;      off = ws_align(off + 4 * (size_t)Hkv * prefill_qpos(T));
-      w.porder = off;     off = ws_align(off + 4 * (pairs + kMaxDealWindow));
+      w.porder = off;     off = ws_align(off + 4 * (pairs + kMaxPairGrid));
     }
   }
   w.total = off;
@@ -166,7 +164,7 @@ inline PrefillWorkspace prefill_ws_layout(int64_t T, int32_t Hkv, int32_t topk, 
 // the queries that chose each; the residual selections go to the block-major pass.
 struct DenseWorkspace {
   int32_t* qperm;      // [Hkv, prefill_qpos(T)]: query of each pair slot (-1: none)
-  int32_t* porder;     // [pairs + kMaxDealWindow]: pair of each (round, CTA) of the query-major
+  int32_t* porder;     // [pairs + kMaxPairGrid]: pair of each (round, CTA) of the query-major
                        // kernel (-1: none), written by its launcher
   int32_t* residual;   // [T, Hkv, k]
   int32_t* dcnt;       // [pairs]

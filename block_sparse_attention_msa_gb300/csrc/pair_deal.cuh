@@ -11,11 +11,8 @@
 
 namespace msa {
 
-// The persistent CTAs, and windows of a power-of-two number of rounds (at most 8, at most
-// 1024 * kDealPasses pairs; a divisor of kMaxRounds, so that no window straddles two launches).
-// A window is dealt by one block of 1024 threads, kDealPasses pairs per thread.
-constexpr int kDealPasses = 2;
-static_assert(1024 * kDealPasses <= kMaxDealWindow, "the deal's windows fit the slot padding");
+// The persistent CTAs, and windows of a power-of-two number of rounds (at most 8, at most 1024
+// pairs; a divisor of kMaxRounds, so that no window straddles two launches of the kernel).
 struct PairDeal {
   int64_t grid;
   int32_t rpw;
@@ -25,7 +22,7 @@ inline PairDeal pair_deal_geometry(int64_t npairs) {
   PairDeal d;
   d.grid = std::min<int64_t>(std::min<int64_t>(npairs, sm_count()), kMaxPairGrid);
   d.rpw = 1;
-  while (d.rpw < 8 && 2 * d.rpw * d.grid <= 1024 * kDealPasses) d.rpw *= 2;
+  while (d.rpw < 8 && 2 * d.rpw * d.grid <= 1024) d.rpw *= 2;
   const int64_t W = d.rpw * d.grid;
   d.nwin = (npairs + W - 1) / W;
   d.nslots = d.nwin * W;
@@ -33,9 +30,9 @@ inline PairDeal pair_deal_geometry(int64_t npairs) {
 }
 
 // Deal of the pairs to the persistent CTAs, by one block of 1024 threads per window `wi` of
-// `rounds_per_window` rounds (rounds_per_window * grid consecutive pairs, kDealPasses per
-// thread): a CTA's time is close to proportional to its blocks, and a plain round-robin deal
-// leaves some CTAs about 8 % more blocks than the mean, which the kernel's end waits for. Within the window the pairs are
+// `rounds_per_window` rounds (rounds_per_window * grid consecutive pairs, at most the block size): a CTA's time is close
+// to proportional to its blocks, and a plain round-robin deal leaves some CTAs about 8 % more
+// blocks than the mean, which the kernel's end waits for. Within the window the pairs are
 // ranked by block count (descending; ties by pair index) and rank i goes to round i / grid,
 // place i % grid on even rounds and grid - 1 - i % grid on odd ones, so that each CTA's sum is
 // near the window's mean; the places map to CTAs turned by 97 per window. Windows keep the
@@ -44,37 +41,30 @@ inline PairDeal pair_deal_geometry(int64_t npairs) {
 __device__ __forceinline__ void pair_deal_window(const int32_t* __restrict__ dcnt, int64_t npairs,
                                                  int32_t grid, int32_t rounds_per_window,
                                                  int32_t* __restrict__ porder, int64_t wi) {
-  // per pass (pair tid, then tid + blockDim.x), warp and block count: pairs, then prefix
-  __shared__ int32_t cnt[kDealPasses][32][kMaxDense + 1];
-  __shared__ int32_t base[kMaxDense + 1];  // per block count: first rank
+  __shared__ int32_t cnt[32][kMaxDense + 1];  // per warp and block count: pairs, then prefix
+  __shared__ int32_t base[kMaxDense + 1];     // per block count: first rank
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int W = rounds_per_window * grid;
   const int64_t w0 = wi * W;
-  const int nvalid = (int)min((int64_t)W, npairs - w0);
-  for (int i = tid; i < kDealPasses * 32 * (kMaxDense + 1); i += blockDim.x) (&cnt[0][0][0])[i] = 0;
+  for (int i = tid; i < 32 * (kMaxDense + 1); i += blockDim.x) (&cnt[0][0])[i] = 0;
   __syncthreads();
-  int L[kDealPasses], rank_in_warp[kDealPasses];
-#pragma unroll
-  for (int ps = 0; ps < kDealPasses; ++ps) {
-    const int idx = ps * blockDim.x + tid;
-    L[ps] = -1;
-    if (idx < nvalid) {
-      const int c = dcnt[w0 + idx];
-      L[ps] = c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c);
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, L[ps]);
-    rank_in_warp[ps] = __popc(peers & ((1u << lane) - 1u));
-    if (L[ps] >= 0 && rank_in_warp[ps] == 0) cnt[ps][warp][L[ps]] = __popc(peers);
+  const bool valid = tid < W && w0 + tid < npairs;
+  int L = -1;
+  if (valid) {
+    const int c = dcnt[w0 + tid];
+    L = c < 0 ? 0 : (c > kMaxDense ? kMaxDense : c);
   }
+  const unsigned peers = __match_any_sync(0xffffffffu, L);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank_in_warp == 0) cnt[warp][L] = __popc(peers);
   __syncthreads();
-  if (tid <= kMaxDense) {  // ranks within a block count follow the pair index
+  if (tid <= kMaxDense) {
     int run = 0;
-    for (int ps = 0; ps < kDealPasses; ++ps)
-      for (int w = 0; w < 32; ++w) {
-        const int c = cnt[ps][w][tid];
-        cnt[ps][w][tid] = run;
-        run += c;
-      }
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w][tid];
+      cnt[w][tid] = run;
+      run += c;
+    }
     base[tid] = run;
   }
   __syncthreads();
@@ -87,18 +77,17 @@ __device__ __forceinline__ void pair_deal_window(const int32_t* __restrict__ dcn
     }
   }
   __syncthreads();
-#pragma unroll
-  for (int ps = 0; ps < kDealPasses; ++ps) {
-    const int idx = ps * blockDim.x + tid;
-    if (idx >= W) continue;
+  if (tid < W) {
+    const int nvalid = (int)min((int64_t)W, npairs - w0);
     // valid pairs take ranks [0, nvalid), the empty ranks [nvalid, W) get no pair
-    const bool valid = idx < nvalid;
-    const int rank = valid ? base[L[ps]] + cnt[ps][warp][L[ps]] + rank_in_warp[ps] : idx;
-    const int rl = rank / grid, place = rank % grid;
-    // the snake, turned by a stride prime to the grid from one window to the next, so that
-    // the heaviest pair of every window (rank 0) does not always land on the same CTA
-    const int cta = (int)(((rl & 1 ? grid - 1 - place : place) + wi * 97) % grid);
-    porder[w0 + (int64_t)rl * grid + cta] = valid ? (int32_t)(w0 + idx) : -1;
+    const int rank = valid ? base[L] + cnt[warp][L] + rank_in_warp : tid;
+    if (valid || tid >= nvalid) {
+      const int rl = rank / grid, place = rank % grid;
+      // the snake, turned by a stride prime to the grid from one window to the next, so that
+      // the heaviest pair of every window (rank 0) does not always land on the same CTA
+      const int cta = (int)(((rl & 1 ? grid - 1 - place : place) + wi * 97) % grid);
+      porder[w0 + (int64_t)rl * grid + cta] = valid ? (int32_t)(w0 + tid) : -1;
+    }
   }
 }
 
