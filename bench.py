@@ -347,19 +347,22 @@ def recorded_traffic(kernel: str, source_hash: str):
     return rec.get("bytes_per_launch")
 
 
-# Every kernel of one msa_sparse_prefill call and the source file it is built from.
-PREFILL_KERNELS = (("select_count_kernel", "prefill_dense.cu"), ("bucket_lists_kernel", "prefill.cu"),
-                   ("bucket_place_kernel", "prefill.cu"), ("prefill_block_tc_kernel", "prefill.cu"),
-                   ("prefill_dense_tc_kernel", "prefill_dense.cu"),
-                   ("lse_merge_chunked_kernel", "page_table_merge.cu"))
+# Every kernel of one msa_sparse_prefill call and the source files its code comes from (the
+# .cu file, and a kernel-specific header where it has one).
+PREFILL_KERNELS = (("select_count_kernel", ("prefill_dense.cu",)),
+                   ("bucket_lists_kernel", ("prefill.cu", "pair_deal.cuh")),
+                   ("bucket_place_kernel", ("prefill.cu",)),
+                   ("prefill_block_tc_kernel", ("prefill.cu",)),
+                   ("prefill_dense_tc_kernel", ("prefill_dense.cu",)),
+                   ("lse_merge_chunked_kernel", ("page_table_merge.cu",)))
 
 
 def prefill_traffic():
     """DRAM bytes of one prefill call: the sum over its kernels' recorded captures (null while
     any of them is missing or its source changed since it was captured)."""
     tot = 0
-    for name, src in PREFILL_KERNELS:
-        b = recorded_traffic(name, src_hash(src))
+    for name, srcs in PREFILL_KERNELS:
+        b = recorded_traffic(name, src_hash(*srcs))
         if b is None:
             return None
         tot += b

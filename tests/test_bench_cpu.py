@@ -106,7 +106,7 @@ def test_recorded_traffic_needs_the_profiled_source():
 
 def test_prefill_traffic_is_the_sum_over_the_calls_kernels():
     got = bench.prefill_traffic()
-    parts = [bench.recorded_traffic(k, bench.src_hash(src)) for k, src in bench.PREFILL_KERNELS]
+    parts = [bench.recorded_traffic(k, bench.src_hash(*srcs)) for k, srcs in bench.PREFILL_KERNELS]
     if any(p is None for p in parts):
         assert got is None
     else:
