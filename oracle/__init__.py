@@ -35,15 +35,20 @@ _lib = None
 BLOCK = 128
 
 
+def gcc_command(src: str, out: str) -> list:
+    """The gcc line that builds a shared library from an oracle source file (portable C, no
+    target-specific flags, no contraction of multiply-adds)."""
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+            src, "-o", out, "-lm", "-lpthread"]
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (portable C, no target-specific flags)."""
+    """Compile the oracle with gcc."""
     os.makedirs(_BUILD, exist_ok=True)
     stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-               "-fno-fast-math", _SRC, "-o", tmp, "-lm", "-lpthread"]
-        subprocess.run(cmd, check=True)
+        subprocess.run(gcc_command(_SRC, tmp), check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

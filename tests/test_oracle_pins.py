@@ -273,6 +273,37 @@ def test_decode_full_selection_equals_dense_causal(N):
             assert abs(res["lse"][u] - lse) < 1e-10
 
 
+@pytest.mark.parametrize("N", [1, 2])
+def test_decode_sparse_equals_masked_dense(N):
+    # k below the causal block count, selections drawn per KV group: each head attends to
+    # the causal keys of its own group's kept blocks only (masked dense attention, scipy)
+    seq_lens = [700, 1030, 129]
+    Hq, Hkv, D, k = 8, 4, 32, 3
+    w = workloads.decode_workload(seq_lens, N, Hq, Hkv, D, topk=k, seed=13, device="cpu")
+    q, kc, vc = u16(w["q"]), u16(w["k_cache"]), u16(w["v_cache"])
+    pt, sl, ids = w["page_table"].numpy(), w["seq_lens"].numpy(), w["block_ids"].numpy()
+    # the groups of one row keep different blocks (else a group mix-up goes unseen)
+    assert any(not np.array_equal(ids[r, 0], ids[r, g]) for r in range(ids.shape[0])
+               for g in range(1, Hkv))
+    res = oracle.sparse_decode(q, kc, vc, pt, sl, ids, N)
+    qf, kf, vf = (oracle.bf16_to_f32(x).astype(np.float64) for x in (q, kc, vc))
+    G = Hq // Hkv
+    for r in range(len(seq_lens) * N):
+        b = r // N
+        q_pos = sl[b] - N + r % N
+        pos = np.arange(sl[b])
+        for h in range(Hq):
+            g = h // G
+            keys = kf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
+            vals = vf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
+            sel = np.isin(pos // 128, ids[r, g][ids[r, g] >= 0]) & (pos <= q_pos)
+            s = np.where(sel, keys @ qf[r, h], -np.inf)
+            lse = logsumexp(s)
+            u = r * Hq + h
+            np.testing.assert_allclose(res["o"][u], np.exp(s - lse) @ vals, rtol=1e-10, atol=1e-12)
+            assert abs(res["lse"][u] - lse) < 1e-10
+
+
 def test_prefill_sparse_equals_masked_dense():
     T, S, Hq, Hkv, D, k = 300, 700, 4, 2, 32, 4
     w = workloads.prefill_workload(T, S, Hq, Hkv, D, k, seed=1, device="cpu", n_shared=2)
