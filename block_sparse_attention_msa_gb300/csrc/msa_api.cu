@@ -68,14 +68,13 @@ size_t msa_index_score_topk_workspace_size(int32_t B, int32_t N, int32_t Hkv, in
   return score_ws_scores_bytes(B, N, Hkv, max_blocks) + msa::ws_align((size_t)B * sizeof(int32_t));
 }
 
-static int index_score_topk_impl(const char* name, const uint16_t* q_idx,
-                                 const uint16_t* k_idx_pages, const int32_t* page_table,
-                                 const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,
-                                 int32_t Di, int32_t max_blocks, int64_t num_pages, int32_t topk,
-                                 int32_t* block_ids, float* scores, int32_t* fpt,
-                                 int32_t* fpt_lens, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
-  if (B == 0 || N == 0) return ok();
+// Host checks of a stage-1 call's tensors and sizes (not its workspace), before any CUDA
+// call: shared by the workspace and the scratch-array entry points, so that both report the
+// same error for the same arguments.
+static int check_score_args(const char* name, const uint16_t* q_idx, const uint16_t* k_idx_pages,
+                            const int32_t* page_table, const int32_t* seq_lens, int32_t B,
+                            int32_t N, int32_t Hkv, int32_t Di, int32_t max_blocks,
+                            int64_t num_pages, int32_t topk, const int32_t* block_ids) {
   if (!q_idx || !k_idx_pages || !page_table || !seq_lens || !block_ids)
     return fail(MSA_ERR_ARG, "%s: null tensor pointer", name);
   if (B < 0 || N < 0 || max_blocks <= 0 || num_pages <= 0)
@@ -91,6 +90,20 @@ static int index_score_topk_impl(const char* name, const uint16_t* q_idx,
     return fail(MSA_ERR_SHAPE, "%s: sizes exceed int32", name);
   if ((int64_t)N > (int64_t)max_blocks * 128)
     return fail(MSA_ERR_SHAPE, "%s: N=%d exceeds max_blocks*128", name, N);
+  return MSA_OK;
+}
+
+static int index_score_topk_impl(const char* name, const uint16_t* q_idx,
+                                 const uint16_t* k_idx_pages, const int32_t* page_table,
+                                 const int32_t* seq_lens, int32_t B, int32_t N, int32_t Hkv,
+                                 int32_t Di, int32_t max_blocks, int64_t num_pages, int32_t topk,
+                                 int32_t* block_ids, float* scores, int32_t* fpt,
+                                 int32_t* fpt_lens, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (B == 0 || N == 0) return ok();
+  const int rc = check_score_args(name, q_idx, k_idx_pages, page_table, seq_lens, B, N, Hkv, Di,
+                                  max_blocks, num_pages, topk, block_ids);
+  if (rc != MSA_OK) return rc;
   const size_t need = msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(MSA_ERR_WORKSPACE,
@@ -418,6 +431,10 @@ int msa_index_score_topk_noalloc(const uint16_t* q_idx, const uint16_t* k_idx_pa
                                  int64_t num_pages, int32_t topk, int32_t* block_ids,
                                  float* scores, void* stream) {
   if (B == 0 || N == 0) return ok();
+  const int rc_args = check_score_args("msa_index_score_topk_noalloc", q_idx, k_idx_pages,
+                                       page_table, seq_lens, B, N, Hkv, Di, max_blocks, num_pages,
+                                       topk, block_ids);
+  if (rc_args != MSA_OK) return rc_args;
   const size_t need = msa_index_score_topk_workspace_size(B, N, Hkv, max_blocks);
   if (need > (size_t)MSA_NOALLOC_SCRATCH_BYTES)
     return fail(MSA_ERR_UNSUPPORTED,

@@ -110,6 +110,40 @@ def test_argument_validation_rejects_before_launch(lib):
                                   0, None) == 0
 
 
+def test_fused_scratch_and_bucket_entry_points_reject_before_launch(lib):
+    ws = ctypes.c_void_p(0x10000)
+    # scorer + page table: a null page-table output, then the scorer's own checks
+    assert lib.msa_index_score_topk_page_table(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 128, 4, 4, 16,
+                                               FAKE, None, None, FAKE, ws, 1 << 20, None) == -1
+    assert "page-table output" in _err(lib)
+    assert lib.msa_index_score_topk_page_table(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 96, 4, 4, 16,
+                                               FAKE, None, FAKE, FAKE, ws, 1 << 20, None) == -3
+    assert lib.msa_index_score_topk_page_table(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 128, 4, 4, 16,
+                                               FAKE, None, FAKE, FAKE, ws, 16, None) == -4
+    # scorer without a workspace: the same argument errors as the workspace entry point, found
+    # before the call looks for its device scratch (no device here)
+    assert lib.msa_index_score_topk_noalloc(None, FAKE, FAKE, FAKE, 1, 1, 8, 128, 4, 4, 16,
+                                            FAKE, None, None) == -1
+    assert "null" in _err(lib) and "noalloc" in _err(lib)
+    assert lib.msa_index_score_topk_noalloc(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 128, 4, 4, 65,
+                                            FAKE, None, None) == -3
+    assert lib.msa_index_score_topk_noalloc(FAKE, FAKE, FAKE, FAKE, 1, 600, 8, 128, 4, 4, 16,
+                                            FAKE, None, None) == -2
+    # ... and calls whose block scores exceed the 8 MiB scratch, before any device work
+    assert lib.msa_index_score_topk_noalloc(FAKE, FAKE, FAKE, FAKE, 64, 1, 8, 128, 8192, 1, 16,
+                                            FAKE, None, None) == -3
+    assert "scratch" in _err(lib)
+    assert lib.msa_index_score_topk_noalloc(None, None, None, None, 0, 1, 8, 128, 4, 4, 16,
+                                            None, None, None) == 0
+    # bucketing: null output, group count, list sizes beyond int32, workspace
+    assert lib.msa_prefill_bucket(FAKE, 100, 8, 16, 4, None, FAKE, ws, 1 << 20, None) == -1
+    assert lib.msa_prefill_bucket(FAKE, 100, 17, 16, 4, FAKE, FAKE, ws, 1 << 20, None) == -1
+    assert lib.msa_prefill_bucket(FAKE, 1 << 30, 8, 16, 4, FAKE, FAKE, ws, 1 << 20, None) == -3
+    assert lib.msa_prefill_bucket(FAKE, 100, 8, 16, 4, FAKE, FAKE, ws, 16, None) == -4
+    assert lib.msa_prefill_bucket(FAKE, 100, 8, 16, 4, FAKE, FAKE, ctypes.c_void_p(0x10010),
+                                  1 << 20, None) == -4
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(ValueError, match="CUDA"):
