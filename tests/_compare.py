@@ -65,7 +65,10 @@ def check_selection(ids_gpu: np.ndarray, ids_ref: np.ndarray, scores_ref: np.nda
         a = set(int(x) for x in ids_gpu[r, g] if x >= 0)
         b = set(int(x) for x in ids_ref[r, g] if x >= 0)
         assert len(a) == len(b), f"row {r} group {g}: {sorted(a)} vs {sorted(b)}"
-        assert sorted(a) == [int(x) for x in ids_gpu[r, g] if x >= 0], "gpu ids not ascending"
+        # distinct ids ascending, then -1 padding: the layout of every selection list
+        row = [int(x) for x in ids_gpu[r, g]]
+        assert row == sorted(a) + [-1] * (len(row) - len(a)), (
+            f"row {r} group {g}: {row} is not distinct ascending ids followed by -1 padding")
         s = scores_ref[r, g]
         for x in a - b:
             for y in b - a:

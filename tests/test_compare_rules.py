@@ -1,6 +1,7 @@
 """The parity comparators themselves (CPU): the selection rule must reject a GPU selection
 that drops a forced block (sink block 0, the query's local block) even when the block kept in
-its place scores higher, and accept a near-tie swap of two non-forced blocks."""
+its place scores higher, or that breaks the list layout (ids ascending, then -1 padding), and
+accept a near-tie swap of two non-forced blocks."""
 import numpy as np
 import pytest
 
@@ -38,3 +39,20 @@ def test_clear_loss_fails():
     s[0, 0, 2] = 4.0  # block 2 now clearly below block 1
     with pytest.raises(AssertionError, match="chose block 2"):
         check_selection(np.array([[[0, 2, 3]]], dtype=np.int32), ids_ref, s)
+
+
+def _padded_case():
+    # one row, one group, 3 causal blocks (local block 2) and k 4: one slot of padding
+    s = np.full((1, 1, 6), -np.inf)
+    s[0, 0, :3] = [1.0, 2.0, 0.5]
+    return s, np.array([[[0, 1, 2, -1]]], dtype=np.int32)
+
+
+@pytest.mark.parametrize("gpu", [[0, -1, 1, 2],    # padding inside the list
+                                 [0, 1, 2, -2],    # padding other than -1
+                                 [0, 2, 1, -1],    # ids not ascending
+                                 [0, 1, 1, 2]])    # a repeated id in place of the padding
+def test_broken_list_layout_fails(gpu):
+    s, ids_ref = _padded_case()
+    with pytest.raises(AssertionError):
+        check_selection(np.array([gpu], dtype=np.int32)[None], ids_ref, s)
