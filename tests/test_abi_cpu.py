@@ -151,3 +151,12 @@ def test_binding_refuses_cpu_tensors(lib):
                            torch.zeros(1, 1, 128, dtype=torch.bfloat16),
                            torch.zeros(1, 1, 128, dtype=torch.bfloat16),
                            torch.zeros(1, 1, 2, dtype=torch.int32))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no CPU fallback: without the built library every call path stops at load()
+    from block_sparse_attention_msa_gb300 import build as _build
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "libmsa_gb300.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        msa.load()
