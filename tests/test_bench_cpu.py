@@ -129,3 +129,26 @@ def test_clock_summary():
 def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(1e9, 2.0, 1) == 5e11
     assert bench.job_throughput(1e9, 2.0, 4) == 2e12
+
+
+def test_visible_keys_equal_the_oracle_page_table_lengths():
+    # the oracle's sparse page table counts, per flattened row, the tokens its query sees in
+    # the kept blocks: the same quantity the bench turns into bytes and FLOPs
+    import oracle
+    import workloads
+    N = 2
+    w = workloads.decode_workload([517, 1500, 129, 128, 2], N, Hq=8, Hkv=4, D=16, topk=5,
+                                  seed=3, device="cpu")
+    sl = w["seq_lens"].numpy()
+    q_pos = torch.from_numpy(oracle.query_positions(sl, N))
+    got = bench.visible_keys(w["block_ids"], q_pos)                       # [R, Hkv]
+    _, lens = oracle.build_sparse_page_table(w["block_ids"].numpy(), w["page_table"].numpy(), sl, N)
+    assert np.array_equal(got.numpy().reshape(-1), np.asarray(lens).reshape(-1))
+
+
+def test_headline_flops_equal_the_split_total():
+    T, prefix, Hkv, k, G, D = 300, 2048, 2, 8, 8, 128
+    ids = torch.from_numpy(_selection(T, prefix, Hkv, k, seed=6))
+    q_pos = torch.arange(prefix, prefix + T, dtype=torch.int64)
+    flops = 4 * D * G * int(bench.visible_keys(ids, q_pos).sum())
+    assert flops == bench.prefill_split(ids, prefix + T, G, D)["flops_total"]
