@@ -152,3 +152,4 @@ def test_headline_flops_equal_the_split_total():
     q_pos = torch.arange(prefix, prefix + T, dtype=torch.int64)
     flops = 4 * D * G * int(bench.visible_keys(ids, q_pos).sum())
     assert flops == bench.prefill_split(ids, prefix + T, G, D)["flops_total"]
+
