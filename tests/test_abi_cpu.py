@@ -160,3 +160,40 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         msa.load()
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "msa.h"
+
+int main(void) {
+  /* a C caller sees the library only through msa.h */
+  if (strcmp(msa_version(), "0.1.0") != 0) return 1;
+  size_t need = msa_index_score_topk_workspace_size(8, 1, 8, 469);
+  if (need < (size_t)8 * 8 * 469 * 4) return 2;
+  /* host checks run before any device call: a null q_idx is MSA_ERR_ARG */
+  int32_t ids[16];
+  int rc = msa_index_score_topk(NULL, NULL, NULL, NULL, 1, 1, 8, 128, 4, 4, 16, ids, NULL,
+                                NULL, 0, NULL);
+  if (rc != MSA_ERR_ARG || strstr(msa_last_error(), "null") == NULL) return 3;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links_the_library(lib, tmp_path):
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    so = msa.library_path()
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-pedantic", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-o", str(exe), so,
+                    "-Wl,-rpath," + os.path.dirname(so)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
