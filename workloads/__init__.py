@@ -82,8 +82,9 @@ def sample_selection(q_pos: torch.Tensor, Hkv: int, topk: int, gen: torch.Genera
     ``shared`` set (a [R, Hkv, n_shared] tensor of candidate ids, -1 = none). Ids are
     ascending, then -1 padding when fewer causal blocks exist.
 
-    This equals the top-k rule applied to iid N(0,1) block scores with +10 added to the
-    shared blocks of boosted rows, without computing any score.
+    This has the distribution of the top-k rule applied to iid continuous block scores in
+    which the shared blocks of boosted rows get a bonus that ranks them above every other
+    candidate, without computing any score.
     """
     device = q_pos.device
     R = q_pos.numel()
