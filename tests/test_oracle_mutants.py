@@ -3,7 +3,8 @@
 Each case below plants one plausible slip in a copy of the oracle's C source: an off-by-one
 causal mask, a wrong KV group, page or request index, a reversed tie rule, a dropped forced
 block, a dropped softmax normaliser or max shift, a wrong merge weight, a wrong bucket
-offset, a wrong bf16 rounding. The copy is compiled on its own and the whole pin suite
+offset, a wrong bf16 rounding, an ignored unit list, rows skipped by the thread split. The
+copy is compiled on its own and the whole pin suite
 (``test_oracle_pins.py``) runs against it in a child process; every copy must fail at least
 one pin. An unmodified copy run the same way must pass, so a broken harness cannot make
 every slip look caught. Mistakes are planted only in these temporary copies, never in the
@@ -122,6 +123,19 @@ MUTANTS = [
     ("buckets: every group's lists from offset 0", "base += off[nblk];", ""),
     ("buckets: last block never counted",
      "if (j >= 0 && j < nblk) off[j + 1] += 1;", "if (j >= 0 && j < nblk - 1) off[j + 1] += 1;"),
+    # unit and row lists (the sampled form of the full-size comparisons), thread split
+    ("decode: unit list ignored",
+     "  dec_ctx* c = (dec_ctx*)p;\n  int64_t u = c->units ? c->units[slot] : slot;",
+     "  dec_ctx* c = (dec_ctx*)p;\n  int64_t u = slot;"),
+    ("strided view: unit list ignored",
+     "  flat_ctx* c = (flat_ctx*)p;\n  int64_t u = c->units ? c->units[slot] : slot;",
+     "  flat_ctx* c = (flat_ctx*)p;\n  int64_t u = slot;"),
+    ("prefill: unit list ignored",
+     "  pre_ctx* c = (pre_ctx*)p;\n  int64_t u = c->units ? c->units[slot] : slot;",
+     "  pre_ctx* c = (pre_ctx*)p;\n  int64_t u = slot;"),
+    ("score: row list ignored",
+     "int64_t r = c->rows ? c->rows[slot] : slot;", "int64_t r = slot;"),
+    ("threads: rows skipped", "i += a->nthreads) a->fn", "i += a->nthreads + 1) a->fn"),
     # bf16 rounding
     ("bf16: truncation", "y = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
      "y = ldexp(trunc(ldexp(m, 8)), e - 8);"),

@@ -285,23 +285,37 @@ def test_decode_sparse_equals_masked_dense(N):
     # the groups of one row keep different blocks (else a group mix-up goes unseen)
     assert any(not np.array_equal(ids[r, 0], ids[r, g]) for r in range(ids.shape[0])
                for g in range(1, Hkv))
-    res = oracle.sparse_decode(q, kc, vc, pt, sl, ids, N)
     qf, kf, vf = (oracle.bf16_to_f32(x).astype(np.float64) for x in (q, kc, vc))
     G = Hq // Hkv
-    for r in range(len(seq_lens) * N):
-        b = r // N
+    R = len(seq_lens) * N
+
+    def masked_dense(u):
+        r, h = divmod(int(u), Hq)
+        b, g = r // N, h // G
         q_pos = sl[b] - N + r % N
         pos = np.arange(sl[b])
-        for h in range(Hq):
-            g = h // G
-            keys = kf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
-            vals = vf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
-            sel = np.isin(pos // 128, ids[r, g][ids[r, g] >= 0]) & (pos <= q_pos)
-            s = np.where(sel, keys @ qf[r, h], -np.inf)
-            lse = logsumexp(s)
-            u = r * Hq + h
-            np.testing.assert_allclose(res["o"][u], np.exp(s - lse) @ vals, rtol=1e-10, atol=1e-12)
-            assert abs(res["lse"][u] - lse) < 1e-10
+        keys = kf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
+        vals = vf[pt[b]].reshape(-1, Hkv, D)[: sl[b], g]
+        sel = np.isin(pos // 128, ids[r, g][ids[r, g] >= 0]) & (pos <= q_pos)
+        s = np.where(sel, keys @ qf[r, h], -np.inf)
+        lse = logsumexp(s)
+        return np.exp(s - lse) @ vals, lse
+
+    res = oracle.sparse_decode(q, kc, vc, pt, sl, ids, N)
+    for u in range(R * Hq):
+        o, lse = masked_dense(u)
+        np.testing.assert_allclose(res["o"][u], o, rtol=1e-10, atol=1e-12)
+        assert abs(res["lse"][u] - lse) < 1e-10
+    # a shuffled list of units (the sampled form the full-size tests use), logical and through
+    # the strided view: slot i holds unit units[i]
+    units = np.random.default_rng(N).permutation(R * Hq)[: R * Hq // 3].astype(np.int64)
+    fpt, lens = oracle.build_sparse_page_table(ids, pt, sl, N)
+    for sub in (oracle.sparse_decode(q, kc, vc, pt, sl, ids, N, units=units),
+                oracle.paged_decode_flat(q, kc, vc, fpt, lens, units=units)):
+        for i, u in enumerate(units):
+            o, lse = masked_dense(u)
+            np.testing.assert_allclose(sub["o"][i], o, rtol=1e-10, atol=1e-12)
+            assert abs(sub["lse"][i] - lse) < 1e-10
 
 
 def test_prefill_sparse_equals_masked_dense():
