@@ -136,6 +136,27 @@ MUTANTS = [
     ("score: row list ignored",
      "int64_t r = c->rows ? c->rows[slot] : slot;", "int64_t r = slot;"),
     ("threads: rows skipped", "i += a->nthreads) a->fn", "i += a->nthreads + 1) a->fn"),
+    # padding, empty rows and other edge cases
+    ("attention: a row with no visible key gets lse 0",
+     "if (n == 0) { *lse = -INFINITY; return; }", "if (n == 0) { *lse = 0.0; return; }"),
+    ("merge: only -inf partials give a NaN lse",
+     "if (n == 0 || m == -INFINITY) { *lse = -INFINITY; return 0; }",
+     "if (n == 0) { *lse = -INFINITY; return 0; }"),
+    ("attention: scores accumulated in float",
+     "    double acc = 0.0;\n    for (int d = 0; d < D; ++d) acc += (double)",
+     "    float acc = 0.0f;\n    for (int d = 0; d < D; ++d) acc += (double)"),
+    ("score: blocks past the query score 0",
+     "      out[j] = best;", "      out[j] = best == -INFINITY ? 0.0f : best;"),
+    ("topk: block 0 kept twice when it is the local block",
+     "if (local > 0) kept[nk++] = (int)local;", "kept[nk++] = (int)local;"),
+    ("topk: padding id 0", "ids[i] = i < nk ? kept[i] : -1;", "ids[i] = i < nk ? kept[i] : 0;"),
+    ("topk: padding score 0", "i < nk ? s[kept[i]] : -INFINITY;", "i < nk ? s[kept[i]] : 0.0f;"),
+    ("page table: padding on page 0",
+     "if (j < 0) { flat_page_table[f * topk + i] = -1; continue; }",
+     "if (j < 0) { flat_page_table[f * topk + i] = 0; continue; }"),
+    ("bf16: NaN rounded to infinity", "if (isnan(x)) return 0x7fc0;", "if (isnan(x)) return 0x7f80;"),
+    ("bf16: negative zero loses its sign",
+     "if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;", "if (x == 0.0) return 0x0000;"),
     # bf16 rounding
     ("bf16: truncation", "y = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
      "y = ldexp(trunc(ldexp(m, 8)), e - 8);"),

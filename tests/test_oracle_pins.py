@@ -38,12 +38,18 @@ def bf16_bits(x) -> np.ndarray:
 
 def test_round_bf16_matches_torch_on_float_values():
     rng = np.random.default_rng(0)
+    f32max = float(np.finfo(np.float32).max)
     x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-8, 8, 20000),
-                        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, 1e-40, -2.5e-39])])
+                        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, 1e-40, -2.5e-39,
+                                  # overflow to infinity, the largest finite bf16, specials
+                                  f32max, -f32max, 3.3895e38, np.inf, -np.inf])])
     x32 = x.astype(np.float32)
     ref = u16(torch.from_numpy(x32).to(torch.bfloat16))
     got = oracle.round_bf16(x32.astype(np.float64))
     assert np.array_equal(ref, got)
+    # NaN stays NaN (all exponent bits, a nonzero fraction); its payload is not fixed
+    nan = int(oracle.round_bf16([np.nan])[0])
+    assert nan & 0x7F80 == 0x7F80 and nan & 0x007F != 0
 
 
 def test_round_bf16_single_rounding_and_ties():
@@ -399,6 +405,27 @@ def test_lse_merge_closed_forms():
     np.testing.assert_array_equal(o, [0.0, 1.0])
     o, lse = oracle.lse_merge(o2[:0], np.zeros(0, dtype=np.float32))
     assert lse == -np.inf and not o.any()
+    # no partial with a visible key: a unit that sees nothing gives o = 0, lse = -inf
+    o, lse = oracle.lse_merge(o2, np.array([-np.inf, -np.inf], dtype=np.float32))
+    assert lse == -np.inf and not o.any()
+
+
+def test_block_partial_of_a_block_after_the_query_is_empty():
+    # a block whose first key lies after the query has no visible key: weight 0 (lse -inf),
+    # o = 0, and merging it in changes nothing
+    T, S, Hq, Hkv, D = 130, 400, 2, 1, 8
+    w = workloads.prefill_workload(T, S, Hq, Hkv, D, topk=2, seed=3, device="cpu", n_shared=0)
+    q, kk, vv = u16(w["q"]), u16(w["k"]), u16(w["v"])
+    t = 0                                   # position S - T = 270: local block 2
+    o3, lse3 = oracle.prefill_block_partial(q, kk, vv, t, 1, 3)
+    assert lse3 == -np.inf and not np.any(o3)
+    o2, lse2 = oracle.prefill_block_partial(q, kk, vv, t, 1, 2)
+    o0, lse0 = oracle.prefill_block_partial(q, kk, vv, t, 1, 0)
+    parts = np.stack([o0, o2]).astype(np.float32)
+    with_empty = np.stack([o0, o2, o3]).astype(np.float32)
+    a = oracle.lse_merge(parts, np.array([lse0, lse2], dtype=np.float32))
+    b = oracle.lse_merge(with_empty, np.array([lse0, lse2, lse3], dtype=np.float32))
+    assert np.array_equal(a[0], b[0]) and a[1] == b[1]
 
 
 # --------------------------------------------------------------------------- bucketing
